@@ -1,0 +1,231 @@
+"""Plain float64 CPU oracle for absorbed ("forward_mqa") MLA decode.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+module. It is slow on purpose and shares no code, constant or helper with the
+CUDA library: it is written straight from the definitions on the pages.
+
+Every input array holds the values the device sees (bf16 numbers already
+widened to float64 by the caller); every result is float64.
+
+Notation (vLLM ``mla_attention`` API docs, module docstring, "More Extent
+Definitions"): ``Lkv`` latent width (512 in DSV3), ``R`` RoPE width (64),
+``N`` heads, ``P``/``V`` nope / value head dims (128).
+
+Pins (see ``tests/test_oracle.py``):
+  * ``mla_decode_reference`` -- hand-derived golden cases, pure-Python brute
+    force, closed forms, torch ``scaled_dot_product_attention`` in float64,
+    page-table permutation invariance, and the MHA == absorbed-MQA identity.
+  * ``mla_decode_split_partials`` + ``merge_partials`` -- split-and-merge equals
+    the unsplit definition for many split counts, including empty splits; the
+    neutral element (zero output, ``-inf`` LSE) is checked directly.
+  * ``gather_request_latent`` -- golden page-table fixture and permutation.
+  * ``mha_compute_friendly`` / ``absorb_query`` / ``up_project`` -- the
+    identity between the two computing approaches, plus torch SDPA.
+No function here is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def gather_request_latent(cache, block_table_row, seq_len, page_size=None):
+    """Rows ``[0, seq_len)`` of one request's latent cache, in logical order.
+
+    Token ``t`` lives in row ``t % page_size`` of physical block
+    ``block_table_row[t // page_size]``.
+
+    Cache layout ``[num_blocks, page_size, Lkv + R]`` with one KV head: vLLM
+    ``mla/common.py`` (vllm-cpu 0.8.5.post2), ``MLACommonBackend.get_kv_cache_shape``;
+    ModelOpt ``mla_attention_decode`` parameters ``latent_cache`` and
+    ``block_table`` ([batch, max_blocks_per_seq] page table). The pages name
+    the page table but never print the index formula; the page-aligned reading
+    here is the one the chunked-context gather uses (vLLM ``mla_attention``
+    API docs, ``build_mla_chunked_context_metadata``: a split request advances
+    in block-aligned steps). Entries past ``ceil(seq_len / page_size)`` and
+    rows past ``seq_len`` are never touched.
+    """
+    cache = np.asarray(cache)
+    if page_size is None:
+        page_size = cache.shape[1]
+    seq_len = int(seq_len)
+    rows = []
+    for t in range(seq_len):
+        block = int(block_table_row[t // page_size])
+        rows.append(cache[block, t % page_size, :])
+    if not rows:
+        return np.zeros((0, cache.shape[2]), dtype=np.float64)
+    return np.stack(rows).astype(np.float64)
+
+
+def _attend_one(q_heads, k_rows, softmax_scale, kv_lora_rank):
+    """softmax(scale * q K^T) V with K = full entry, V = first Lkv columns.
+
+    vLLM ``mla_attention`` API docs, module docstring, "Data-Movement Friendly
+    Approach (i.e. forward_mqa)": MQA with QK head dim Lkv + R and V head dim
+    Lkv, ``sdpa(cat[ql_nope, q_pe], cat[kv_c, k_pe], kv_c)``. The scale is the
+    caller's (ModelOpt ``mla_attention_decode``, ``softmax_scale``). Returns
+    ``out [N, Lkv]`` and the natural-log LSE ``[N]`` of the scaled scores
+    (ModelOpt ``mla_attention_decode``, ``return_lse``). An empty key set gives
+    the merge's neutral element: zero output, ``-inf`` LSE (vLLM
+    ``mla_attention`` API docs, ``neutralize_empty_context_partials``).
+    """
+    n_heads = q_heads.shape[0]
+    if k_rows.shape[0] == 0:
+        return (np.zeros((n_heads, kv_lora_rank), dtype=np.float64),
+                np.full((n_heads,), -np.inf, dtype=np.float64))
+    scores = softmax_scale * (q_heads @ k_rows.T)            # [N, L]
+    m = scores.max(axis=1, keepdims=True)                    # [N, 1]
+    e = np.exp(scores - m)
+    denom = e.sum(axis=1, keepdims=True)
+    lse = (m + np.log(denom))[:, 0]
+    v_rows = k_rows[:, :kv_lora_rank]                         # V = kv_c
+    out = (e / denom) @ v_rows
+    return out, lse
+
+
+def mla_decode_reference(q, cache, block_table, seq_lens, softmax_scale,
+                         kv_lora_rank=512):
+    """Absorbed MLA decode, by definition: ``out [B, N, Lkv]``, ``lse [B, N]``.
+
+    For request ``b`` with ``L = seq_lens[b]`` every query head attends to all
+    ``L`` cached tokens (no causal mask: the new token is inserted before the
+    attention runs -- vLLM ``mla_attention`` API docs, ``MLAAttention.forward``,
+    ``do_kv_cache_update``). Interface: ModelOpt
+    ``modelopt.torch.kernels.quantization.attention.mla``,
+    ``mla_attention_decode`` (q ``[batch, num_heads, kv_lora_rank +
+    qk_rope_head_dim]``, returns ``out [batch, num_heads, kv_lora_rank]`` and
+    ``lse [batch, num_heads]``).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    batch, n_heads, _ = q.shape
+    out = np.zeros((batch, n_heads, kv_lora_rank), dtype=np.float64)
+    lse = np.zeros((batch, n_heads), dtype=np.float64)
+    for b in range(batch):
+        k_rows = gather_request_latent(cache, block_table[b], seq_lens[b])
+        out[b], lse[b] = _attend_one(q[b], k_rows, softmax_scale, kv_lora_rank)
+    return out, lse
+
+
+def split_token_ranges(seq_len, num_splits, page_size):
+    """Token ranges of the ``num_splits`` splits of one request.
+
+    ModelOpt ``mla_attention_decode``, ``num_kv_splits``: a fixed split count
+    along the token axis. The pages do not print the partition; the reading
+    used here keeps splits page-aligned: split ``s`` covers
+    ``[s*C, min((s+1)*C, L))`` with ``C = page_size * ceil(ceil(L/page_size) / S)``.
+    Splits past the end are empty.
+    """
+    seq_len = int(seq_len)
+    pages = -(-seq_len // page_size)
+    chunk = page_size * (-(-pages // num_splits)) if pages else 0
+    ranges = []
+    for s in range(num_splits):
+        lo = min(s * chunk, seq_len)
+        hi = min((s + 1) * chunk, seq_len)
+        ranges.append((lo, hi))
+    return ranges
+
+
+def mla_decode_split_partials(q, cache, block_table, seq_lens, softmax_scale,
+                              num_splits, kv_lora_rank=512):
+    """Split-KV partials: ``o_part [B, N, S, Lkv]`` (normalised) and
+    ``lse_part [B, N, S]``.
+
+    Each split attends over its own token range exactly as
+    ``mla_decode_reference`` does over the whole sequence; empty splits give
+    the neutral element (zero output, ``-inf`` LSE).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    cache = np.asarray(cache)
+    page_size = cache.shape[1]
+    batch, n_heads, _ = q.shape
+    o_part = np.zeros((batch, n_heads, num_splits, kv_lora_rank), dtype=np.float64)
+    lse_part = np.full((batch, n_heads, num_splits), -np.inf, dtype=np.float64)
+    for b in range(batch):
+        k_all = gather_request_latent(cache, block_table[b], seq_lens[b], page_size)
+        for s, (lo, hi) in enumerate(split_token_ranges(seq_lens[b], num_splits, page_size)):
+            o_part[b, :, s, :], lse_part[b, :, s] = _attend_one(
+                q[b], k_all[lo:hi], softmax_scale, kv_lora_rank)
+    return o_part, lse_part
+
+
+def merge_partials(o_part, lse_part):
+    """LSE-weighted merge of split partials along axis -2 / -1.
+
+    ``o_part [..., S, V]``, ``lse_part [..., S]`` -> ``out [..., V]``,
+    ``lse [...]``. vLLM names this ``merge_attn_states`` (``mla_attention`` API
+    docs, module docstring "Chunked Prefill" and ``accumulate_mla_context_chunk``)
+    but prints no formula; the one used is the exact identity for partials
+    normalised by their own softmax sums:
+    ``lse = M + ln sum_s exp(lse_s - M)``, ``M = max_s lse_s``,
+    ``out = sum_s exp(lse_s - lse) * o_s``. A zero output with ``-inf`` LSE
+    carries no weight (``neutralize_empty_context_partials``); when every
+    partial is neutral, the result is neutral too.
+    """
+    o_part = np.asarray(o_part, dtype=np.float64)
+    lse_part = np.asarray(lse_part, dtype=np.float64)
+    lead = lse_part.shape[:-1]
+    out = np.zeros(lead + (o_part.shape[-1],), dtype=np.float64)
+    lse = np.full(lead, -np.inf, dtype=np.float64)
+    for idx in np.ndindex(*lead):
+        ls = lse_part[idx]
+        big = ls.max()
+        if big == -np.inf:
+            continue
+        total = big + math.log(np.exp(ls - big).sum())
+        lse[idx] = total
+        weights = np.exp(ls - total)
+        out[idx] = weights @ o_part[idx]
+    return out, lse
+
+
+def absorb_query(q_nope, w_uk):
+    """``ql_nope = einsum("snh,lnh->snl", q_nope, W_UK)``.
+
+    vLLM ``mla_attention`` API docs, module docstring, "Data-Movement Friendly
+    Approach": ``q_nope [Sq, N, P]``, ``W_UK [Lkv, N, P]`` -> ``[Sq, N, Lkv]``.
+    """
+    return np.einsum("snh,lnh->snl", np.asarray(q_nope, np.float64),
+                     np.asarray(w_uk, np.float64))
+
+
+def up_project(latent_out, w_uv):
+    """``o = einsum("snl,lnv->snv", sdpa_o, W_UV)`` (same section as above)."""
+    return np.einsum("snl,lnv->snv", np.asarray(latent_out, np.float64),
+                     np.asarray(w_uv, np.float64))
+
+
+def mha_compute_friendly(q_nope, q_pe, kv_c, k_pe, w_uk, w_uv, softmax_scale):
+    """The compute-friendly path ("forward_mha") for one query token.
+
+    vLLM ``mla_attention`` API docs, module docstring, "Compute Friendly
+    Approach": ``k_nope = kv_c @ W_UK``, ``v = kv_c @ W_UV``, then MHA with QK
+    head dim P + R over ``cat[k_nope, k_pe expanded over heads]``.
+    Shapes: ``q_nope [N, P]``, ``q_pe [N, R]``, ``kv_c [L, Lkv]``,
+    ``k_pe [L, R]``, ``W_UK [Lkv, N, P]``, ``W_UV [Lkv, N, V]``.
+    Returns ``out [N, V]`` and ``lse [N]``.
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_pe = np.asarray(q_pe, np.float64)
+    kv_c = np.asarray(kv_c, np.float64)
+    k_pe = np.asarray(k_pe, np.float64)
+    w_uk = np.asarray(w_uk, np.float64)
+    w_uv = np.asarray(w_uv, np.float64)
+    n_heads = q_nope.shape[0]
+    k_nope = np.einsum("tl,lnp->tnp", kv_c, w_uk)            # [L, N, P]
+    v = np.einsum("tl,lnv->tnv", kv_c, w_uv)                 # [L, N, V]
+    out = np.zeros((n_heads, w_uv.shape[2]), dtype=np.float64)
+    lse = np.zeros((n_heads,), dtype=np.float64)
+    for h in range(n_heads):
+        q_h = np.concatenate([q_nope[h], q_pe[h]])
+        k_h = np.concatenate([k_nope[:, h, :], k_pe], axis=1)  # k_pe shared by heads
+        scores = softmax_scale * (k_h @ q_h)
+        m = scores.max()
+        e = np.exp(scores - m)
+        lse[h] = m + math.log(e.sum())
+        out[h] = (e / e.sum()) @ v[:, h, :]
+    return out, lse

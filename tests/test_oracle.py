@@ -1,0 +1,297 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+Hand-worked golden cases, pure-Python brute force, closed forms, torch's
+float64 SDPA, exact identities (MHA == absorbed MQA, split+merge == unsplit,
+page-table permutation invariance). CPU only.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import (absorb_query, gather_request_latent, merge_partials,
+                    mha_compute_friendly, mla_decode_reference,
+                    mla_decode_split_partials, split_token_ranges, up_project)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _exact(text):
+    """Evaluate the fixtures' exact forms: 'ln 6', '4 ln 2', '0', '-inf'."""
+    text = text.strip()
+    if text == "-inf":
+        return -math.inf
+    if "ln" not in text:
+        return float(text)
+    coef, _, arg = text.partition("ln")
+    coef = float(coef) if coef.strip() else 1.0
+    return coef * math.log(float(arg))
+
+
+def _paged_from_dense(rng, dense_rows_per_req, page_size, extra_blocks=3, fill=77.0):
+    """Scatter dense per-request rows into a randomly permuted page pool."""
+    pages = [-(-len(r) // page_size) for r in dense_rows_per_req]
+    nb = sum(pages) + extra_blocks
+    width = dense_rows_per_req[0].shape[1]
+    cache = np.full((nb, page_size, width), fill, dtype=np.float64)
+    perm = rng.permutation(nb)
+    table = np.full((len(pages), max(pages + [1])), -1, dtype=np.int64)
+    pos = 0
+    for b, rows in enumerate(dense_rows_per_req):
+        for j in range(pages[b]):
+            blk = perm[pos]
+            pos += 1
+            table[b, j] = blk
+            chunk = rows[j * page_size:(j + 1) * page_size]
+            cache[blk, :len(chunk)] = chunk
+    return cache, table
+
+
+# ---------------------------------------------------------------- golden cases
+
+def test_golden_hand_worked_decode():
+    with open(os.path.join(GOLDEN, "decode_hand_worked.json")) as f:
+        g = json.load(f)
+    cache = np.array(g["cache"], dtype=np.float64)
+    table = np.array(g["block_table"], dtype=np.int64)
+    seq = np.array(g["seq_lens"])
+    q = np.array(g["q"], dtype=np.float64)
+    for b in range(len(seq)):
+        got = gather_request_latent(cache, table[b], seq[b], g["page_size"])
+        np.testing.assert_array_equal(got, np.array(g["gathered"][b], dtype=np.float64))
+    out, lse = mla_decode_reference(q, cache, table, seq, math.log(2.0),
+                                    kv_lora_rank=g["kv_lora_rank"])
+    np.testing.assert_allclose(out, np.array(g["expected_out"]), rtol=0, atol=1e-14)
+    exact = np.array([[_exact(x) for x in row] for row in g["expected_lse_exact"]])
+    np.testing.assert_allclose(lse, exact, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, np.array(g["expected_lse"]), rtol=0, atol=1e-14)
+
+
+def test_golden_hand_worked_merge():
+    with open(os.path.join(GOLDEN, "merge_hand_worked.json")) as f:
+        g = json.load(f)
+    o_part = np.array(g["o_part"], dtype=np.float64)
+    lse_part = np.array([[_exact(x) for x in row] for row in g["lse_part_exact"]])
+    out, lse = merge_partials(o_part, lse_part)
+    np.testing.assert_allclose(out, np.array(g["expected_out"]), rtol=0, atol=1e-14)
+    exact = np.array([_exact(x) for x in g["expected_lse_exact"]])
+    assert np.isneginf(lse[2]) and np.isneginf(exact[2])
+    np.testing.assert_allclose(lse[:2], exact[:2], rtol=0, atol=1e-14)
+
+
+# ------------------------------------------------------------- brute force
+
+def _brute_force(q, rows, scale, lkv):
+    """Pure-Python loops: no numpy, no vectorisation, straight from the sum."""
+    n_heads = len(q)
+    outs, lses = [], []
+    for h in range(n_heads):
+        s = [scale * sum(q[h][d] * rows[t][d] for d in range(len(q[h])))
+             for t in range(len(rows))]
+        big = max(s)
+        z = sum(math.exp(x - big) for x in s)
+        lses.append(big + math.log(z))
+        outs.append([sum(math.exp(s[t] - big) / z * rows[t][d] for t in range(len(rows)))
+                     for d in range(lkv)])
+    return outs, lses
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_brute_force_tiny(seed):
+    rng = np.random.default_rng(seed)
+    lkv, rope, ps, n = 6, 3, 4, 3
+    lens = [1, 5, 9]
+    dense = [rng.standard_normal((L, lkv + rope)) for L in lens]
+    cache, table = _paged_from_dense(rng, dense, ps)
+    q = rng.standard_normal((len(lens), n, lkv + rope))
+    scale = 0.37
+    out, lse = mla_decode_reference(q, cache, table, lens, scale, kv_lora_rank=lkv)
+    for b in range(len(lens)):
+        bo, bl = _brute_force(q[b].tolist(), dense[b].tolist(), scale, lkv)
+        np.testing.assert_allclose(out[b], np.array(bo), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse[b], np.array(bl), rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------- closed forms
+
+def test_zero_query_gives_mean_and_log_length():
+    rng = np.random.default_rng(5)
+    lens = [1, 7, 64, 130]
+    dense = [rng.standard_normal((L, 576)) for L in lens]
+    cache, table = _paged_from_dense(rng, dense, 64)
+    q = np.zeros((len(lens), 4, 576))
+    out, lse = mla_decode_reference(q, cache, table, lens, 0.072)
+    for b, L in enumerate(lens):
+        np.testing.assert_allclose(lse[b], math.log(L), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(out[b], np.broadcast_to(dense[b][:, :512].mean(0), (4, 512)),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_single_token_returns_its_latent_row():
+    rng = np.random.default_rng(6)
+    dense = [rng.standard_normal((1, 576))]
+    cache, table = _paged_from_dense(rng, dense, 64)
+    q = rng.standard_normal((1, 8, 576))
+    scale = 1 / math.sqrt(192)
+    out, lse = mla_decode_reference(q, cache, table, [1], scale)
+    np.testing.assert_array_equal(out[0], np.broadcast_to(dense[0][0, :512], (8, 512)))
+    np.testing.assert_allclose(lse[0], scale * (q[0] @ dense[0][0]), rtol=1e-14, atol=1e-14)
+
+
+def test_identical_rows_give_uniform_weights():
+    rng = np.random.default_rng(7)
+    row = rng.standard_normal(576)
+    L = 100
+    dense = [np.tile(row, (L, 1))]
+    cache, table = _paged_from_dense(rng, dense, 64)
+    q = rng.standard_normal((1, 3, 576))
+    scale = 0.05
+    out, lse = mla_decode_reference(q, cache, table, [L], scale)
+    np.testing.assert_allclose(out[0], np.broadcast_to(row[:512], (3, 512)), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse[0], scale * (q[0] @ row) + math.log(L), rtol=1e-13, atol=1e-13)
+
+
+def test_empty_request_is_neutral():
+    rng = np.random.default_rng(8)
+    cache = rng.standard_normal((2, 64, 576))
+    table = np.array([[0, 1]])
+    out, lse = mla_decode_reference(rng.standard_normal((1, 2, 576)), cache, table, [0], 0.1)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+# ------------------------------------------------- library special case
+
+def test_matches_torch_sdpa_float64():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(9)
+    lens = [3, 64, 65, 200]
+    n = 16
+    dense = [rng.standard_normal((L, 576)) for L in lens]
+    cache, table = _paged_from_dense(rng, dense, 64)
+    q = rng.standard_normal((len(lens), n, 576))
+    scale = 1 / math.sqrt(192)
+    out, lse = mla_decode_reference(q, cache, table, lens, scale)
+    for b, L in enumerate(lens):
+        qt = torch.from_numpy(q[b]).view(1, n, 1, 576)
+        kt = torch.from_numpy(dense[b]).view(1, 1, L, 576).expand(1, n, L, 576)
+        vt = torch.from_numpy(dense[b][:, :512]).view(1, 1, L, 512).expand(1, n, L, 512)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+        np.testing.assert_allclose(out[b], ref.view(n, 512).numpy(), rtol=1e-11, atol=1e-12)
+        ref_lse = torch.logsumexp(scale * (qt.view(n, 576) @ kt[0, 0].T), dim=-1)
+        np.testing.assert_allclose(lse[b], ref_lse.numpy(), rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------- identities
+
+def test_absorbed_mqa_equals_compute_friendly_mha():
+    """forward_mqa followed by the W_UV up-projection equals forward_mha."""
+    rng = np.random.default_rng(10)
+    n, p, r, v, lkv, L = 4, 16, 8, 16, 32, 37
+    w_uk = rng.standard_normal((lkv, n, p)) / math.sqrt(lkv)
+    w_uv = rng.standard_normal((lkv, n, v)) / math.sqrt(lkv)
+    q_nope = rng.standard_normal((n, p))
+    q_pe = rng.standard_normal((n, r))
+    kv_c = rng.standard_normal((L, lkv))
+    k_pe = rng.standard_normal((L, r))
+    scale = (p + r) ** -0.5
+    ref_out, ref_lse = mha_compute_friendly(q_nope, q_pe, kv_c, k_pe, w_uk, w_uv, scale)
+
+    ql_nope = absorb_query(q_nope[None], w_uk)[0]                   # [N, Lkv]
+    q_abs = np.concatenate([ql_nope, q_pe], axis=1)[None]           # [1, N, Lkv+R]
+    cache, table = _paged_from_dense(rng, [np.concatenate([kv_c, k_pe], axis=1)], 8)
+    lat, lse = mla_decode_reference(q_abs, cache, table, [L], scale, kv_lora_rank=lkv)
+    out = up_project(lat, w_uv)[0]
+    np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse[0], ref_lse, rtol=1e-12, atol=1e-13)
+
+
+def test_absorb_query_against_explicit_sum():
+    rng = np.random.default_rng(11)
+    q_nope = rng.standard_normal((2, 3, 5))
+    w_uk = rng.standard_normal((7, 3, 5))
+    got = absorb_query(q_nope, w_uk)
+    for s in range(2):
+        for nh in range(3):
+            for l in range(7):
+                want = sum(q_nope[s, nh, h] * w_uk[l, nh, h] for h in range(5))
+                assert abs(got[s, nh, l] - want) < 1e-12
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 7, 64])
+def test_split_then_merge_equals_unsplit(num_splits):
+    rng = np.random.default_rng(100 + num_splits)
+    lens = [1, 63, 64, 65, 300, 1000]
+    dense = [rng.standard_normal((L, 576)) for L in lens]
+    cache, table = _paged_from_dense(rng, dense, 64)
+    q = rng.standard_normal((len(lens), 4, 576))
+    scale = 1 / math.sqrt(192)
+    ref_out, ref_lse = mla_decode_reference(q, cache, table, lens, scale)
+    o_part, lse_part = mla_decode_split_partials(q, cache, table, lens, scale, num_splits)
+    if num_splits >= 7:
+        assert np.isneginf(lse_part).any(), "expected some empty splits"
+    out, lse = merge_partials(o_part, lse_part)
+    np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+
+
+def test_merge_neutral_element_changes_nothing():
+    rng = np.random.default_rng(12)
+    o = rng.standard_normal((5, 3, 8))
+    ls = rng.standard_normal((5, 3))
+    base_out, base_lse = merge_partials(o, ls)
+    o2 = np.concatenate([o, np.zeros((5, 1, 8))], axis=1)
+    ls2 = np.concatenate([ls, np.full((5, 1), -np.inf)], axis=1)
+    out, lse = merge_partials(o2, ls2)
+    np.testing.assert_allclose(out, base_out, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(lse, base_lse, rtol=1e-14, atol=1e-14)
+
+
+def test_split_ranges_cover_and_align():
+    for L in [0, 1, 63, 64, 65, 1000, 8192, 131072]:
+        for S in [1, 2, 3, 7, 32, 64]:
+            rngs = split_token_ranges(L, S, 64)
+            assert len(rngs) == S
+            assert rngs[0][0] == 0 and rngs[-1][1] == L
+            for (lo, hi), (lo2, _) in zip(rngs, rngs[1:]):
+                assert hi == lo2 and lo <= hi
+            for lo, hi in rngs:
+                assert lo % 64 == 0 or lo == L
+
+
+def test_page_permutation_is_bitwise_invariant():
+    rng = np.random.default_rng(13)
+    lens = [5, 128, 190]
+    dense = [rng.standard_normal((L, 576)) for L in lens]
+    q = rng.standard_normal((3, 8, 576))
+    c1, t1 = _paged_from_dense(np.random.default_rng(1), dense, 64)
+    c2, t2 = _paged_from_dense(np.random.default_rng(2), dense, 64, extra_blocks=9)
+    assert not np.array_equal(t1[:, :1], t2[:, :1])
+    o1, l1 = mla_decode_reference(q, c1, t1, lens, 0.07)
+    o2, l2 = mla_decode_reference(q, c2, t2, lens, 0.07)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_rope_columns_enter_scores_but_not_values():
+    """K is the whole 576-wide entry; V is only its first 512 columns."""
+    rng = np.random.default_rng(14)
+    dense = [rng.standard_normal((40, 576))]
+    cache, table = _paged_from_dense(rng, dense, 64)
+    q = rng.standard_normal((1, 2, 576))
+    o1, l1 = mla_decode_reference(q, cache, table, [40], 0.1)
+    cache2 = cache.copy()
+    cache2[..., 512:] *= 2.0          # changes scores only
+    o2, l2 = mla_decode_reference(q, cache2, table, [40], 0.1)
+    assert not np.allclose(l1, l2)
+    q3 = q.copy()
+    q3[..., 512:] = 0.0
+    cache3 = cache.copy()
+    cache3[..., 512:] = 123.0         # with q_pe = 0 the rope columns cannot matter
+    o3, l3 = mla_decode_reference(q3, cache, table, [40], 0.1)
+    o4, l4 = mla_decode_reference(q3, cache3, table, [40], 0.1)
+    np.testing.assert_array_equal(o3, o4)
+    np.testing.assert_array_equal(l3, l4)
+    assert o1.shape[-1] == 512
