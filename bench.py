@@ -1,0 +1,434 @@
+"""Benchmark: absorbed MLA decode over a paged latent cache on GB300.
+
+One step = one ``mla_decode`` call (the decode kernel, plus the split merge
+when the plan splits the sequence) over the whole batch of the headline
+workload: B=128 requests, N=128 heads, 8192 cached tokens each, bf16,
+page_size 64, randomly permuted block table. Inputs (1.24 GB of cache) are
+larger than L2, so no flush runs between steps.
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on
+a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("MLA decode cached-tokens×heads/s and achieved % of roofline "
+          "(HBM vs bf16 TC), 1×GB300")
+UNIT = "cached-tokens*heads/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_KERNEL_SOURCES = {
+    1: ["mla_decode_simt.cu", "mla_device.cuh", "mla_internal.h"],
+    2: ["mla_decode_tc.cu", "mla_device.cuh", "mla_internal.h"],
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (0: enough for about 3 s of timed work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None, help="workload name (default: headline)")
+    ap.add_argument("--force-simt", action="store_true",
+                    help="run the CUDA-core kernel instead of the planner's choice")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work budget of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_work(w):
+    """Bytes the method must move and flops it must do for one decode call.
+
+    bytes = 1152 per cached token (one 576-wide bf16 entry read once for all
+    heads) + 1152 per (request, head) for q + 1024 per (request, head) for the
+    bf16 output + 4 per (request, head) for the LSE + 4 per block-table entry
+    used. flops = 2 * (576 + 512) per (token, head).
+    """
+    T = w.total_tokens
+    BN = w.batch * w.num_heads
+    pages = sum(-(-int(L) // w.page_size) for L in w.seq_lens)
+    nbytes = 1152 * T + 1152 * BN + 1024 * BN + 4 * BN + 4 * pages
+    flops = 2 * (576 + 512) * w.num_heads * T
+    return nbytes, flops
+
+
+def kernel_source_hash(kernel):
+    h = hashlib.sha256()
+    for name in DECODE_KERNEL_SOURCES.get(kernel, []):
+        p = os.path.join(ROOT, "mla_latent_cache_paged_gb300", "csrc", name)
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rows = json.load(f)
+    except (OSError, ValueError):
+        return None, None
+    for r in rows:
+        if r.get("kernel") == kernel and r.get("workload") == workload:
+            if r.get("source_hash") == kernel_source_hash(kernel):
+                return float(r["dram_bytes_per_launch"]), r.get("profile")
+            return None, "stale"
+    return None, None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, budget_s):
+    """The oracle, as it stands, on a bounded sample: whole requests of `w`."""
+    import numpy as np
+    from oracle import mla_decode_reference
+    from mla_latent_cache_paged_gb300.workloads import bf16_bits_to_f64
+
+    order = list(range(w.batch))
+    done_tokens = 0
+    reqs = []
+    t0 = time.perf_counter()
+    for b in order:
+        L = int(w.seq_lens[b])
+        n = -(-L // w.page_size)
+        ids = w.block_table[b, :n].astype(np.int64)
+        pool = bf16_bits_to_f64(w.cache_bits[ids])
+        table = np.arange(n, dtype=np.int64)[None, :]
+        q = bf16_bits_to_f64(w.q_bits[b:b + 1])
+        mla_decode_reference(q, pool, table, [L], w.softmax_scale)
+        done_tokens += L
+        reqs.append(b)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": done_tokens * w.num_heads / dt, "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{len(reqs)} of {w.batch} requests ({done_tokens} cached tokens x "
+                      f"{w.num_heads} heads), numpy float64, {dt:.1f} s",
+            "seconds": dt}
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, w, rank):
+    """--impl reference: the CPU oracle, each step one bounded sample of `w`."""
+    import numpy as np
+    from oracle import mla_decode_reference
+    from mla_latent_cache_paged_gb300.workloads import bf16_bits_to_f64
+
+    if rank != 0:
+        return None
+    steps = args.steps if args.steps > 0 else 5
+    per_step_reqs = 2
+
+    def one_step(i):
+        toks = 0
+        for j in range(per_step_reqs):
+            b = (i * per_step_reqs + j) % w.batch
+            L = int(w.seq_lens[b])
+            n = -(-L // w.page_size)
+            pool = bf16_bits_to_f64(w.cache_bits[w.block_table[b, :n].astype(np.int64)])
+            mla_decode_reference(bf16_bits_to_f64(w.q_bits[b:b + 1]), pool,
+                                 np.arange(n)[None, :], [L], w.softmax_scale)
+            toks += L
+        return toks
+
+    for i in range(args.warmup):
+        one_step(i)
+    t0 = time.perf_counter()
+    toks = sum(one_step(args.warmup + i) for i in range(steps))
+    dt = time.perf_counter() - t0
+    value = toks * w.num_heads / dt
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample_per_step": f"{per_step_reqs} requests"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step_reqs} whole requests per step, numpy float64"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_ours(args, w, rank, world):
+    import torch
+    from mla_latent_cache_paged_gb300 import binding, build
+    from mla_latent_cache_paged_gb300.workloads import to_torch
+
+    build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    q, cache, table, lens = to_torch(w, dev)
+    props = torch.cuda.get_device_properties(dev)
+    plan = binding.make_plan(w.batch, w.num_heads, w.max_blocks_per_seq,
+                             seq_lens_host=w.seq_lens, max_seq_len=w.max_seq_len,
+                             num_kv_splits=w.num_kv_splits, num_sms=props.multi_processor_count,
+                             force_simt=args.force_simt)
+    ws = binding.new_workspace(plan, dev)
+    out = torch.empty((w.batch, w.num_heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.batch, w.num_heads), dtype=torch.float32, device=dev)
+
+    def step():
+        binding.mla_decode(q, cache, table, lens, w.softmax_scale, plan=plan, out=out, lse=lse,
+                           workspace=ws)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    status = binding.read_error(ws)
+    if status != 0:
+        raise RuntimeError(f"device status after warm-up: {binding.status_string(status)}")
+
+    steps = args.steps
+    if steps <= 0:
+        t0 = time.perf_counter()
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 5
+        steps = int(min(20000, max(20, 3.0 / max(per, 1e-6))))
+        if world > 1:
+            t = torch.tensor([steps], device=dev)
+            torch.distributed.broadcast(t, 0)
+            steps = int(t.item())
+
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    barrier()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    barrier()
+    elapsed_ms = start.elapsed_time(end)
+    clocks = sampler.stop() if sampler else None
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    status = binding.read_error(ws)
+    if status != 0:
+        raise RuntimeError(f"device status after timing: {binding.status_string(status)}")
+
+    # End to end through the public call with host buffers: per step, copy the
+    # step's inputs (q, block table, lengths) from pinned host memory, decode,
+    # and read out + lse back into pinned host memory.
+    q_h = q.cpu().pin_memory()
+    table_h = table.cpu().pin_memory()
+    lens_h = lens.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d, table_d, lens_d = torch.empty_like(q), torch.empty_like(table), torch.empty_like(lens)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        table_d.copy_(table_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        binding.mla_decode(q_d, cache, table_d, lens_d, w.softmax_scale, plan=plan, out=out,
+                           lse=lse, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_steps = max(10, steps // 4)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return None
+
+    units = w.total_tokens * w.num_heads
+    ms_per_step = elapsed_ms / steps
+    value = units * world * steps / (elapsed_ms / 1e3)
+    nbytes, flops = algorithmic_work(w)
+    peaks, peak_kind = load_peaks()
+    t_s = ms_per_step / 1e3
+    achieved_gbs = nbytes / t_s / 1e9
+    achieved_tflops = flops / t_s / 1e12
+    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    traffic, profile = recorded_traffic(plan.kernel, w.name)
+    launches_per_step = 1 + (1 if plan.num_kv_splits > 1 else 0)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": w.name, "batch": w.batch, "heads": w.num_heads,
+            "seq_lens": ("all %d" % w.max_seq_len if len(set(w.seq_lens.tolist())) == 1
+                         else f"{int(w.seq_lens.min())}..{int(w.seq_lens.max())}"),
+            "cached_tokens": w.total_tokens, "page_size": w.page_size,
+            "kv_lora_rank": 512, "rope_dim": 64, "softmax_scale": w.softmax_scale,
+            "num_kv_splits": plan.num_kv_splits,
+            "kernel": {1: "simt", 2: "tcgen05"}[plan.kernel],
+            "l2": "inputs larger than L2 (%.2f GB cache), no flush" % (cache.numel() * 2 / 1e9),
+            "parallelism": f"requests replicated per rank x{world} (weak)" if world > 1 else "1 GPU",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "timed": "whole step on its stream: decode kernel" +
+                     (" + split merge kernel" if launches_per_step > 1 else ""),
+            "algorithmic_bytes_per_launch": nbytes,
+            "tensor_achieved_tflops": achieved_tflops,
+            "tensor_peak_tflops": peaks["bf16_tflops"],
+            "frac_of_roofline": t_roof / t_s,
+            "traffic_profile": profile,
+        },
+        "gpu_launches": launches_per_step * steps,
+        "clocks": clocks,
+        "e2e": {"value": units * world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": q.numel() * 2 + table.numel() * 4 + lens.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
+                "ms_per_step": e2e_ms / e2e_steps},
+    }
+    return res
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+
+    from mla_latent_cache_paged_gb300.workloads import HEADLINE, get_workload
+    name = args.workload or HEADLINE
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        w = get_workload(name)
+        res = run_reference(args, w, rank)
+        print(json.dumps(res), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    w = get_workload(name)
+    res = run_ours(args, w, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,216 @@
+/*
+ * mla_decode.h -- C ABI of libmla_decode: absorbed ("forward_mqa") Multi-head
+ * Latent Attention decode over a paged latent KV cache, for GB300 (sm_103a).
+ *
+ * What it computes. For request b with L = seq_lens[b] cached tokens and each
+ * head h < N:
+ *     K[t]   = latent_cache[block_table[b, t / page_size], t % page_size, 0:576]
+ *     V[t]   = K[t][0:512]
+ *     s[t]   = softmax_scale * dot(q[b, h, 0:576], K[t])
+ *     lse    = ln sum_t exp(s[t])
+ *     out    = sum_t exp(s[t] - lse) * V[t]
+ * This is the data-movement friendly MLA path: MQA with QK head dim Lkv+R and
+ * V head dim Lkv, sdpa(cat[ql_nope, q_pe], cat[kv_c, k_pe], kv_c)
+ * (vLLM "mla_attention" API docs, module docstring, "Data-Movement Friendly
+ * Approach (i.e. forward_mqa)"). The problem statement and argument list
+ * follow ModelOpt "modelopt.torch.kernels.quantization.attention.mla",
+ * mla_attention_decode (q, latent_cache, block_table, b_seq_len,
+ * softmax_scale, kv_lora_rank, qk_rope_head_dim, page_size, num_kv_splits,
+ * return_lse). The cache layout [num_blocks, block_size, head_size] with one
+ * latent KV head is vLLM mla/common.py (vllm-cpu 0.8.5.post2),
+ * MLACommonBackend.get_kv_cache_shape.
+ *
+ * Conventions for every entry point.
+ *   - All device pointers are caller-owned; the library never allocates or
+ *     frees device memory. Scratch space is the caller's `workspace`, sized
+ *     by mla_decode_plan.
+ *   - Every call returns an int status: MLA_OK (0) or a negative MLA_ERR_*.
+ *     Argument errors are detected on the host before anything is enqueued.
+ *   - Device work is enqueued asynchronously on `stream` (a cudaStream_t
+ *     passed as void*, NULL = legacy default stream). No entry point except
+ *     mla_read_error synchronises the host with the device, so mla_decode can
+ *     be captured in a CUDA graph.
+ *   - Errors the device detects (a block id outside [0, num_blocks), a
+ *     seq_len longer than the block table allows) are recorded in a status
+ *     word at the start of `workspace`; the offending page is treated as
+ *     absent. Nothing traps. Read them with mla_read_error.
+ *   - Supported shapes: kv_lora_rank = 512, rope_dim = 64, page_size = 64,
+ *     1 <= num_heads <= 128. Anything else returns MLA_ERR_UNSUPPORTED.
+ *   - bf16 data are raw IEEE bfloat16 bit patterns (uint16), little endian.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_DECODE_ABI_VERSION 1
+
+/* Status codes. */
+#define MLA_OK                 0
+#define MLA_ERR_INVALID_ARG   -1  /* null pointer, negative size, inconsistent plan */
+#define MLA_ERR_UNSUPPORTED   -2  /* shape outside the supported set */
+#define MLA_ERR_WORKSPACE     -3  /* workspace missing, too small or misaligned */
+#define MLA_ERR_CUDA          -4  /* a CUDA runtime call or launch failed */
+#define MLA_ERR_BAD_BLOCK_ID  -5  /* device: block_table entry outside [0, num_blocks) */
+#define MLA_ERR_BAD_SEQ_LEN   -6  /* device: seq_len < 0 or > max_blocks_per_seq*page_size */
+#define MLA_ERR_TIMEOUT       -7  /* device: a bounded wait inside a kernel expired */
+
+/* Kernel variants the planner can choose (mla_decode_plan_t.kernel). */
+#define MLA_KERNEL_SIMT   1  /* CUDA-core split kernel, any 1 <= N <= 128 */
+#define MLA_KERNEL_TC     2  /* tcgen05/TMEM + TMA CTA-pair kernel, heads padded to 128 */
+
+/* Plan flags (mla_decode_plan_t.flags, and the `flags` argument). */
+#define MLA_PLAN_FORCE_SIMT  0x1u  /* use MLA_KERNEL_SIMT even where MLA_KERNEL_TC applies */
+
+/*
+ * A decode plan: the sizes, the split count S and the kernel variant. It is
+ * plain data computed on the host; mla_decode reads it and never changes it.
+ *
+ * Split-KV (ModelOpt mla_attention_decode, num_kv_splits: a fixed split count
+ * along the token axis). Split s of request b covers tokens
+ * [s*C_b, min((s+1)*C_b, L_b)) with C_b = page_size * ceil(ceil(L_b/page_size)/S);
+ * empty splits contribute nothing. With S = 1 the decode kernel writes `out`
+ * and `lse` itself; with S > 1 it writes fp32 partials into the workspace and
+ * mla_merge_splits combines them.
+ */
+typedef struct mla_decode_plan {
+    int32_t  batch;               /* B */
+    int32_t  num_heads;           /* N */
+    int32_t  kv_lora_rank;        /* Lkv = 512 */
+    int32_t  rope_dim;            /* R = 64 */
+    int32_t  page_size;           /* tokens per block = 64 */
+    int32_t  max_blocks_per_seq;  /* block_table row length */
+    int32_t  max_seq_len;         /* upper bound of seq_lens used for planning */
+    int32_t  num_kv_splits;       /* S used by mla_decode, >= 1 */
+    int32_t  kernel;              /* MLA_KERNEL_* */
+    int32_t  num_sms;             /* SM count the plan was made for */
+    int32_t  grid_ctas;           /* CTAs the decode kernel launches */
+    uint32_t flags;               /* MLA_PLAN_* as requested */
+    uint64_t workspace_bytes;     /* bytes of `workspace` mla_decode needs */
+    uint64_t partial_offset;      /* byte offset of o_part [B,N,S,Lkv] fp32 */
+    uint64_t lse_partial_offset;  /* byte offset of lse_part [B,N,S] fp32 */
+    uint32_t reserved[8];
+} mla_decode_plan_t;
+
+/*
+ * mla_decode_plan -- choose S and the kernel, size the workspace. Host only.
+ *
+ *   batch, num_heads           B >= 0, 1 <= N <= 128.
+ *   kv_lora_rank, rope_dim     must be 512 and 64.
+ *   page_size                  must be 64.
+ *   max_blocks_per_seq         block_table row length, >= 1.
+ *   max_seq_len                upper bound of every seq_lens[b] (0..max_blocks_per_seq*page_size).
+ *   seq_lens_host              optional host copy of seq_lens [B] (NULL allowed);
+ *                              when given, the planner sizes S from the real lengths.
+ *   num_kv_splits              S > 0 is used as given (fixed, batch-invariant);
+ *                              0 lets the planner choose from the SM count.
+ *   num_sms                    SMs of the target device (152 on GB300), >= 1.
+ *   flags                      MLA_PLAN_* bits.
+ *   plan                       out: filled on MLA_OK.
+ */
+int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int rope_dim,
+                    int page_size, int max_blocks_per_seq, int max_seq_len,
+                    const int32_t* seq_lens_host, int num_kv_splits, int num_sms,
+                    uint32_t flags, mla_decode_plan_t* plan);
+
+/*
+ * mla_workspace_init -- zero the status header of a fresh workspace
+ * (cudaMemsetAsync of its first 256 bytes on `stream`). Call once per
+ * workspace allocation before its first mla_decode.
+ */
+int mla_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode -- absorbed MLA decode (the `forward_mqa` of the vLLM pages).
+ *
+ *   plan             from mla_decode_plan with the same B, N, max_blocks_per_seq.
+ *   q                device, bf16 [B, N, 576] contiguous: [ql_nope (512) | q_pe (64)]
+ *                    (vLLM mla_attention API docs, MLAAttention.forward_impl:
+ *                    mqa_q = cat(ql_nope, q_pe)). 16-byte aligned.
+ *   latent_cache     device, bf16 [num_blocks, 64, 576] contiguous:
+ *                    [kv_c (512) | k_pe (64)] per token. 16-byte aligned.
+ *   num_blocks       blocks in latent_cache, >= 1.
+ *   block_table      device, int32 [B, max_blocks_per_seq]; entries past
+ *                    ceil(L_b/64) are never read.
+ *   seq_lens         device, int32 [B]; rows past L_b in the last page are
+ *                    never read or weighted.
+ *   softmax_scale    multiplies q.K before the softmax (the model's
+ *                    qk_head_dim**-0.5, times mscale^2 under yarn RoPE).
+ *   out              device, bf16 [B, N, 512]; rounded to nearest even.
+ *   lse              device, fp32 [B, N], natural log of sum exp(scaled
+ *                    scores); NULL skips it (return_lse=False). An empty
+ *                    request (L_b = 0) gives out = 0, lse = -inf.
+ *   workspace        device, >= plan->workspace_bytes, 256-byte aligned,
+ *                    initialised once with mla_workspace_init.
+ *   stream           cudaStream_t as void*.
+ * Calls that share a workspace must not overlap on the device.
+ */
+int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
+               int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+               float softmax_scale, void* out, float* lse,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_merge_splits -- LSE-weighted merge of S partial attention results.
+ *
+ * vLLM names this merge_attn_states (mla_attention API docs, module docstring
+ * "Chunked Prefill"; accumulate_mla_context_chunk) and uses it for the
+ * decode-context-parallel combine as well. For each (b, h):
+ *     M   = max_s lse_part[b,h,s]
+ *     lse = M + ln sum_s exp(lse_part[b,h,s] - M)
+ *     out = sum_s exp(lse_part[b,h,s] - lse) * o_part[b,h,s,:]
+ * A partial with lse = -inf carries no weight; if all are -inf the result is
+ * out = 0, lse = -inf (neutralize_empty_context_partials on the same page).
+ *
+ *   o_part     device, fp32 [B, N, S, v_dim], each partial already normalised.
+ *   lse_part   device, fp32 [B, N, S], natural log.
+ *   v_dim      a multiple of 8, 8 <= v_dim <= 2048.
+ *   out        device, bf16 [B, N, v_dim].
+ *   lse        device, fp32 [B, N], or NULL.
+ */
+int mla_merge_splits(const float* o_part, const float* lse_part, int batch, int num_heads,
+                     int num_splits, int v_dim, void* out, float* lse, void* stream);
+
+/*
+ * mla_read_error -- synchronise `stream`, then read and clear the device
+ * status word of `workspace`. *device_status receives MLA_OK or the first
+ * MLA_ERR_* a kernel recorded since the last read. Returns MLA_ERR_CUDA if
+ * the synchronisation or copy fails.
+ */
+int mla_read_error(void* workspace, int* device_status, void* stream);
+
+/* Human-readable text for a status code (static storage). */
+const char* mla_status_string(int status);
+
+/* ABI version (MLA_DECODE_ABI_VERSION) of the loaded library. */
+int mla_abi_version(void);
+
+/*
+ * mla_debug_gather_pages -- test hook for the page-table indexing.
+ *
+ * Copies, for every request b and token t < seq_lens[b], the 576-wide cache
+ * row the decode kernels read for that token into
+ * dst[b, t, 0:576] (bf16 [B, dst_max_tokens, 576], contiguous), moving it
+ * with the same TMA tensor map and page loader the tensor-core decode kernel
+ * uses. Rows t >= seq_lens[b] of dst are left untouched. Block ids outside
+ * [0, num_blocks) are recorded in the workspace status word and their rows
+ * are left untouched. This is the semantics of vLLM's gather_cache /
+ * cp_gather_cache (mla_attention API docs, _compute_prefill_context), used
+ * here only to check the indexing bit for bit.
+ */
+int mla_debug_gather_pages(const void* latent_cache, int64_t num_blocks,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           int batch, int max_blocks_per_seq, int dst_max_tokens,
+                           void* dst, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MLA_DECODE_H */

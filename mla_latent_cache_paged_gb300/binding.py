@@ -1,0 +1,251 @@
+"""Thin ctypes binding of libmla_decode (include/mla_decode.h).
+
+Only argument marshalling lives here: torch tensors become device pointers,
+the current torch stream becomes the ``stream`` argument, and non-zero
+status codes become ``MlaError``. Every arithmetic step runs in the CUDA
+library; if the library is missing the calls raise instead of falling back.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+MLA_OK = 0
+MLA_ERR_INVALID_ARG = -1
+MLA_ERR_UNSUPPORTED = -2
+MLA_ERR_WORKSPACE = -3
+MLA_ERR_CUDA = -4
+MLA_ERR_BAD_BLOCK_ID = -5
+MLA_ERR_BAD_SEQ_LEN = -6
+MLA_ERR_TIMEOUT = -7
+
+MLA_KERNEL_SIMT = 1
+MLA_KERNEL_TC = 2
+MLA_PLAN_FORCE_SIMT = 0x1
+
+KV_LORA_RANK = 512
+ROPE_DIM = 64
+HEAD_DIM = KV_LORA_RANK + ROPE_DIM
+PAGE_SIZE = 64
+STATUS_BYTES = 256
+
+EXPORTED_SYMBOLS = (
+    "mla_decode_plan", "mla_workspace_init", "mla_decode", "mla_merge_splits",
+    "mla_read_error", "mla_status_string", "mla_abi_version", "mla_debug_gather_pages",
+)
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class MlaDecodePlan(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("kv_lora_rank", ctypes.c_int32),
+        ("rope_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("max_seq_len", ctypes.c_int32),
+        ("num_kv_splits", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32),
+        ("grid_ctas", ctypes.c_int32),
+        ("flags", ctypes.c_uint32),
+        ("workspace_bytes", ctypes.c_uint64),
+        ("partial_offset", ctypes.c_uint64),
+        ("lse_partial_offset", ctypes.c_uint64),
+        ("reserved", ctypes.c_uint32 * 8),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+
+
+_LIB = None
+
+
+def load_library(path=None):
+    """Load libmla_decode.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (mla_latent_cache_paged_gb300.build)")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz, f32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                             ctypes.c_float)
+    lib.mla_decode_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, i32, i32,
+                                    ctypes.c_uint32, ctypes.POINTER(MlaDecodePlan)]
+    lib.mla_workspace_init.argtypes = [vp, sz, vp]
+    lib.mla_decode.argtypes = [ctypes.POINTER(MlaDecodePlan), vp, vp, i64, vp, vp, f32, vp, vp,
+                               vp, sz, vp]
+    lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
+    lib.mla_read_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
+    lib.mla_status_string.argtypes = [i32]
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_abi_version.argtypes = []
+    lib.mla_debug_gather_pages.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, sz, vp]
+    for name in EXPORTED_SYMBOLS:
+        if name not in ("mla_status_string",):
+            getattr(lib, name).restype = ctypes.c_int
+    if path == LIB_PATH:
+        _LIB = lib
+    return lib
+
+
+def status_string(status):
+    try:
+        return load_library().mla_status_string(int(status)).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _check(status, what):
+    if status != MLA_OK:
+        raise MlaError(status, what)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_plan(batch, num_heads, max_blocks_per_seq, max_seq_len=None, *, seq_lens_host=None,
+              num_kv_splits=0, num_sms=None, force_simt=False):
+    """Call mla_decode_plan (host only; no device work)."""
+    lib = load_library()
+    if max_seq_len is None:
+        max_seq_len = max_blocks_per_seq * PAGE_SIZE
+    if num_sms is None:
+        import torch
+        num_sms = (torch.cuda.get_device_properties(0).multi_processor_count
+                   if torch.cuda.is_available() else 152)
+    lens_ptr = ctypes.c_void_p(0)
+    keep = None
+    if seq_lens_host is not None:
+        import numpy as np
+        keep = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+        lens_ptr = ctypes.c_void_p(keep.ctypes.data)
+    plan = MlaDecodePlan()
+    rc = lib.mla_decode_plan(int(batch), int(num_heads), KV_LORA_RANK, ROPE_DIM, PAGE_SIZE,
+                             int(max_blocks_per_seq), int(max_seq_len), lens_ptr,
+                             int(num_kv_splits), int(num_sms),
+                             MLA_PLAN_FORCE_SIMT if force_simt else 0, ctypes.byref(plan))
+    del keep
+    _check(rc, "mla_decode_plan")
+    return plan
+
+
+def new_workspace(plan, device=None, stream=None):
+    """Allocate (through torch) and initialise a workspace for `plan`."""
+    import torch
+    nbytes = max(int(plan.workspace_bytes), STATUS_BYTES)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+    _check(load_library().mla_workspace_init(_ptr(ws), nbytes, _stream_ptr(stream)),
+           "mla_workspace_init")
+    return ws
+
+
+def _check_tensor(t, name, dtype, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def mla_decode(q, latent_cache, block_table, seq_lens, softmax_scale, *, plan=None,
+               num_kv_splits=0, out=None, lse=None, return_lse=True, workspace=None,
+               stream=None, force_simt=False):
+    """Absorbed MLA decode. Returns ``(out bf16 [B,N,512], lse fp32 [B,N] | None)``.
+
+    Mirrors the argument list of ModelOpt's ``mla_attention_decode``; the work
+    is one ``mla_decode`` call of the C library on the current stream.
+    """
+    import torch
+    B, N, D = q.shape
+    if D != HEAD_DIM:
+        raise ValueError(f"q last dim must be {HEAD_DIM}")
+    _check_tensor(q, "q", torch.bfloat16)
+    _check_tensor(latent_cache, "latent_cache", torch.bfloat16)
+    if latent_cache.dim() != 3 or latent_cache.shape[1:] != (PAGE_SIZE, HEAD_DIM):
+        raise ValueError("latent_cache must be [num_blocks, 64, 576]")
+    _check_tensor(block_table, "block_table", torch.int32)
+    _check_tensor(seq_lens, "seq_lens", torch.int32, (B,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks_per_seq]")
+    if plan is None:
+        plan = make_plan(B, N, block_table.shape[1], num_kv_splits=num_kv_splits,
+                         force_simt=force_simt)
+    if out is None:
+        out = torch.empty((B, N, KV_LORA_RANK), dtype=torch.bfloat16, device=q.device)
+    _check_tensor(out, "out", torch.bfloat16, (B, N, KV_LORA_RANK))
+    if lse is None and return_lse:
+        lse = torch.empty((B, N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32, (B, N))
+    if workspace is None:
+        workspace = new_workspace(plan, q.device, stream)
+    rc = load_library().mla_decode(
+        ctypes.byref(plan), _ptr(q), _ptr(latent_cache), int(latent_cache.shape[0]),
+        _ptr(block_table), _ptr(seq_lens), float(softmax_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), int(workspace.numel()), _stream_ptr(stream))
+    _check(rc, "mla_decode")
+    return out, lse
+
+
+def mla_merge_splits(o_part, lse_part, *, out=None, lse=None, return_lse=True, stream=None):
+    """LSE merge of fp32 partials ``[B,N,S,V]`` / ``[B,N,S]`` -> bf16 ``[B,N,V]``, fp32 ``[B,N]``."""
+    import torch
+    B, N, S, V = o_part.shape
+    _check_tensor(o_part, "o_part", torch.float32)
+    _check_tensor(lse_part, "lse_part", torch.float32, (B, N, S))
+    if out is None:
+        out = torch.empty((B, N, V), dtype=torch.bfloat16, device=o_part.device)
+    _check_tensor(out, "out", torch.bfloat16, (B, N, V))
+    if lse is None and return_lse:
+        lse = torch.empty((B, N), dtype=torch.float32, device=o_part.device)
+    rc = load_library().mla_merge_splits(_ptr(o_part), _ptr(lse_part), B, N, S, V, _ptr(out),
+                                         _ptr(lse), _stream_ptr(stream))
+    _check(rc, "mla_merge_splits")
+    return out, lse
+
+
+def read_error(workspace, stream=None):
+    """Synchronise and return (and clear) the device status word of `workspace`."""
+    st = ctypes.c_int(0)
+    _check(load_library().mla_read_error(_ptr(workspace), ctypes.byref(st), _stream_ptr(stream)),
+           "mla_read_error")
+    return st.value
+
+
+def debug_gather_pages(latent_cache, block_table, seq_lens, dst, workspace, stream=None):
+    """Test hook: dense gather of every request's rows into ``dst [B, T, 576]``."""
+    import torch
+    _check_tensor(latent_cache, "latent_cache", torch.bfloat16)
+    _check_tensor(dst, "dst", torch.bfloat16)
+    B = block_table.shape[0]
+    rc = load_library().mla_debug_gather_pages(
+        _ptr(latent_cache), int(latent_cache.shape[0]), _ptr(block_table), _ptr(seq_lens), B,
+        int(block_table.shape[1]), int(dst.shape[1]), _ptr(dst), _ptr(workspace),
+        int(workspace.numel()), _stream_ptr(stream))
+    _check(rc, "mla_debug_gather_pages")
+    return dst

@@ -1,0 +1,118 @@
+// C ABI entry points of libmla_decode (declared in include/mla_decode.h).
+// Host-side argument checks happen before anything is enqueued; device work
+// goes onto the caller's stream without any host synchronisation.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "mla_internal.h"
+
+using namespace mla;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_status(int e) { return e == 0 ? MLA_OK : MLA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" int mla_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || workspace_bytes < kStatusBytes || !aligned(workspace, 256))
+        return MLA_ERR_WORKSPACE;
+    return cuda_status(int(cudaMemsetAsync(workspace, 0, kStatusBytes,
+                                           static_cast<cudaStream_t>(stream))));
+}
+
+extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
+                          int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                          float softmax_scale, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    int rc = validate_plan(plan);
+    if (rc != MLA_OK) return rc;
+    if (!q || !latent_cache || !block_table || !seq_lens || !out) return MLA_ERR_INVALID_ARG;
+    if (num_blocks < 1 || !std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(latent_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)))
+        return MLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < plan->workspace_bytes || !aligned(workspace, 256))
+        return MLA_ERR_WORKSPACE;
+    if (plan->batch == 0) return MLA_OK;
+
+    const int S = plan->num_kv_splits;
+    char* ws = static_cast<char*>(workspace);
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.cache = static_cast<const uint16_t*>(latent_cache);
+    p.num_blocks = num_blocks;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.max_blocks = plan->max_blocks_per_seq;
+    p.batch = plan->batch;
+    p.num_heads = plan->num_heads;
+    p.num_splits = S;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.status = reinterpret_cast<int32_t*>(ws);
+    if (S > 1) {
+        p.o_part = reinterpret_cast<float*>(ws + plan->partial_offset);
+        p.lse_part = reinterpret_cast<float*>(ws + plan->lse_partial_offset);
+    }
+
+    int e = plan->kernel == MLA_KERNEL_TC ? launch_decode_tc(p, plan->grid_ctas, stream)
+                                          : launch_decode_simt(p, stream);
+    if (e != 0) return MLA_ERR_CUDA;
+    if (S > 1) {
+        e = launch_merge(p.o_part, p.lse_part, plan->batch * plan->num_heads, S, kLkv, p.out,
+                         lse, stream);
+        if (e != 0) return MLA_ERR_CUDA;
+    }
+    return MLA_OK;
+}
+
+extern "C" int mla_merge_splits(const float* o_part, const float* lse_part, int batch,
+                                int num_heads, int num_splits, int v_dim, void* out, float* lse,
+                                void* stream) {
+    if (batch < 0 || num_heads < 0 || num_splits < 1 || num_splits > kMaxMergeSplits)
+        return MLA_ERR_INVALID_ARG;
+    if (v_dim < 8 || v_dim > 2048 || v_dim % 8 != 0) return MLA_ERR_UNSUPPORTED;
+    if (batch == 0 || num_heads == 0) return MLA_OK;
+    if (!o_part || !lse_part || !out) return MLA_ERR_INVALID_ARG;
+    if (!aligned(o_part, 16) || !aligned(lse_part, 4) || !aligned(out, 8) ||
+        (lse && !aligned(lse, 4)))
+        return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_merge(o_part, lse_part, batch * num_heads, num_splits, v_dim,
+                                    static_cast<uint16_t*>(out), lse, stream));
+}
+
+extern "C" int mla_read_error(void* workspace, int* device_status, void* stream) {
+    if (!workspace || !device_status) return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+    int32_t words[2] = {0, 0};
+    if (cudaMemcpy(words, workspace, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (cudaMemset(workspace, 0, sizeof(words)) != cudaSuccess) return MLA_ERR_CUDA;
+    *device_status = words[0];
+    return MLA_OK;
+}
+
+extern "C" int mla_debug_gather_pages(const void* latent_cache, int64_t num_blocks,
+                                      const int32_t* block_table, const int32_t* seq_lens,
+                                      int batch, int max_blocks_per_seq, int dst_max_tokens,
+                                      void* dst, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+    if (batch < 0 || max_blocks_per_seq < 1 || dst_max_tokens < 0 || num_blocks < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (batch == 0) return MLA_OK;
+    if (!latent_cache || !block_table || !seq_lens || !dst) return MLA_ERR_INVALID_ARG;
+    if (!aligned(latent_cache, 16) || !aligned(dst, 16)) return MLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kStatusBytes || !aligned(workspace, 256))
+        return MLA_ERR_WORKSPACE;
+    return cuda_status(launch_gather(static_cast<const uint16_t*>(latent_cache), num_blocks,
+                                     block_table, seq_lens, batch, max_blocks_per_seq,
+                                     dst_max_tokens, static_cast<uint16_t*>(dst),
+                                     static_cast<int32_t*>(workspace), stream));
+}

@@ -1,0 +1,59 @@
+// Internal declarations shared by the translation units of libmla_decode.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "mla_decode.h"
+
+namespace mla {
+
+constexpr int kLkv = 512;          // latent width = V head dim of the absorbed path
+constexpr int kRope = 64;          // RoPE width
+constexpr int kD = kLkv + kRope;   // one cache entry = absorbed q/k head dim
+constexpr int kPageSize = 64;      // tokens per block
+constexpr int kMaxHeads = 128;
+constexpr size_t kStatusBytes = 256;   // status header at the start of the workspace
+constexpr int kMaxMergeSplits = 1024;
+
+// Layout of the status header (int32 words).
+//   [0] first MLA_ERR_* recorded by a kernel (0 = none)
+//   [1] detail: the offending block id / seq_len / wait site
+struct StatusWords {
+    int32_t code;
+    int32_t detail;
+};
+
+// Everything a decode kernel needs for one call.
+struct DecodeParams {
+    const uint16_t* q;            // bf16 [B, N, 576]
+    const uint16_t* cache;        // bf16 [num_blocks, 64, 576]
+    int64_t num_blocks;
+    const int32_t* block_table;   // [B, max_blocks]
+    const int32_t* seq_lens;      // [B]
+    int32_t max_blocks;
+    int32_t batch;
+    int32_t num_heads;
+    int32_t num_splits;
+    float scale_log2;             // softmax_scale * log2(e)
+    uint16_t* out;                // bf16 [B, N, 512]          (num_splits == 1)
+    float* lse;                   // fp32 [B, N] or null       (num_splits == 1)
+    float* o_part;                // fp32 [B, N, S, 512]       (num_splits > 1)
+    float* lse_part;              // fp32 [B, N, S]            (num_splits > 1)
+    int32_t* status;              // status header in the workspace
+};
+
+// Launchers (return a cudaError_t as int; 0 = success).
+int launch_decode_simt(const DecodeParams& p, void* stream);
+int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream);
+int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,
+                 int v_dim, uint16_t* out, float* lse, void* stream);
+int launch_gather(const uint16_t* cache, int64_t num_blocks, const int32_t* block_table,
+                  const int32_t* seq_lens, int batch, int max_blocks, int dst_max_tokens,
+                  uint16_t* dst, int32_t* status, void* stream);
+
+// Host-side helpers from mla_plan.cpp.
+int validate_plan(const mla_decode_plan_t* plan);
+bool tc_kernel_built();
+
+}  // namespace mla

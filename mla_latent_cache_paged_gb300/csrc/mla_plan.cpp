@@ -1,0 +1,176 @@
+// Host-side planning for absorbed MLA decode: argument checks, the split count
+// S, the kernel variant and the workspace layout. No CUDA calls happen here,
+// so everything in this file also runs on a machine without a GPU.
+#include <algorithm>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <vector>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+
+uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// Makespan of items (costs in launch order) greedily placed on `machines`
+// identical workers, which is how the block scheduler hands out CTAs.
+double list_schedule(const std::vector<double>& costs, int machines) {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < machines; ++i) free_at.push(0.0);
+    double makespan = 0.0;
+    for (double c : costs) {
+        double t = free_at.top();
+        free_at.pop();
+        t += c;
+        makespan = std::max(makespan, t);
+        free_at.push(t);
+    }
+    return makespan;
+}
+
+int heads_per_simt_cta() { return 16; }
+
+// Estimated run time, in units of "one page through one worker", of a split
+// count S. Each (request, split) is one work item; partial results cost
+// their write + read through HBM, spread over all workers.
+double estimate(int kernel, int S, int batch, int num_heads, const std::vector<int>& pages,
+                int num_sms) {
+    int workers;
+    int items_per_split;
+    if (kernel == MLA_KERNEL_TC) {
+        workers = std::max(1, num_sms / 2);          // one CTA pair per item
+        items_per_split = 1;
+    } else {
+        workers = std::max(1, num_sms * 2);          // two SIMT CTAs per SM
+        items_per_split = (num_heads + heads_per_simt_cta() - 1) / heads_per_simt_cta();
+    }
+    std::vector<double> costs;
+    costs.reserve(size_t(batch) * S * items_per_split);
+    for (int b = 0; b < batch; ++b) {
+        int per_split = (pages[b] + S - 1) / S;
+        for (int s = 0; s < S; ++s) {
+            int here = std::max(0, std::min(per_split, pages[b] - s * per_split));
+            for (int i = 0; i < items_per_split; ++i) costs.push_back(0.15 + here);
+        }
+    }
+    double t = list_schedule(costs, workers);
+    if (S > 1) {
+        const double page_bytes = double(kPageSize) * kD * 2.0;
+        double partial = double(batch) * num_heads * S * (kLkv * 4.0 + 4.0) * 2.0;
+        double per_round = page_bytes * (kernel == MLA_KERNEL_TC ? workers : workers / 2.0);
+        t += partial / per_round + 4.0;  // + the merge launch
+    }
+    return t;
+}
+
+}  // namespace
+
+int validate_plan(const mla_decode_plan_t* p) {
+    if (!p) return MLA_ERR_INVALID_ARG;
+    if (p->kv_lora_rank != kLkv || p->rope_dim != kRope || p->page_size != kPageSize)
+        return MLA_ERR_UNSUPPORTED;
+    if (p->batch < 0 || p->num_heads < 1 || p->num_heads > kMaxHeads ||
+        p->max_blocks_per_seq < 1 || p->num_kv_splits < 1 ||
+        p->num_kv_splits > kMaxMergeSplits)
+        return MLA_ERR_INVALID_ARG;
+    if (p->kernel != MLA_KERNEL_SIMT && p->kernel != MLA_KERNEL_TC) return MLA_ERR_INVALID_ARG;
+    if (p->kernel == MLA_KERNEL_TC && !tc_kernel_built()) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int rope_dim,
+                               int page_size, int max_blocks_per_seq, int max_seq_len,
+                               const int32_t* seq_lens_host, int num_kv_splits, int num_sms,
+                               uint32_t flags, mla_decode_plan_t* plan) {
+    if (!plan) return MLA_ERR_INVALID_ARG;
+    if (batch < 0 || num_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 0 ||
+        num_kv_splits < 0 || num_sms < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (kv_lora_rank != kLkv || rope_dim != kRope || page_size != kPageSize ||
+        num_heads > kMaxHeads)
+        return MLA_ERR_UNSUPPORTED;
+    if (int64_t(max_seq_len) > int64_t(max_blocks_per_seq) * page_size)
+        return MLA_ERR_INVALID_ARG;
+    if (num_kv_splits > kMaxMergeSplits) return MLA_ERR_UNSUPPORTED;
+
+    std::vector<int> pages(size_t(batch), (max_seq_len + page_size - 1) / page_size);
+    int max_pages = (max_seq_len + page_size - 1) / page_size;
+    if (seq_lens_host) {
+        max_pages = 0;
+        for (int b = 0; b < batch; ++b) {
+            int L = seq_lens_host[b];
+            if (L < 0 || L > max_seq_len) return MLA_ERR_INVALID_ARG;
+            pages[size_t(b)] = (L + page_size - 1) / page_size;
+            max_pages = std::max(max_pages, pages[size_t(b)]);
+        }
+    }
+
+    int kernel = MLA_KERNEL_TC;
+    if ((flags & MLA_PLAN_FORCE_SIMT) || !tc_kernel_built()) kernel = MLA_KERNEL_SIMT;
+
+    int S = num_kv_splits;
+    if (S == 0) {
+        S = 1;
+        if (batch > 0 && max_pages > 1) {
+            double best = estimate(kernel, 1, batch, num_heads, pages, num_sms);
+            int cap = std::min(max_pages, 64);
+            for (int s = 2; s <= cap; ++s) {
+                double t = estimate(kernel, s, batch, num_heads, pages, num_sms);
+                if (t < best * 0.995) {
+                    best = t;
+                    S = s;
+                }
+            }
+        }
+    }
+
+    std::memset(plan, 0, sizeof(*plan));
+    plan->batch = batch;
+    plan->num_heads = num_heads;
+    plan->kv_lora_rank = kv_lora_rank;
+    plan->rope_dim = rope_dim;
+    plan->page_size = page_size;
+    plan->max_blocks_per_seq = max_blocks_per_seq;
+    plan->max_seq_len = max_seq_len;
+    plan->num_kv_splits = S;
+    plan->kernel = kernel;
+    plan->num_sms = num_sms;
+    plan->flags = flags;
+    if (kernel == MLA_KERNEL_TC)
+        plan->grid_ctas = 2 * batch * S;
+    else
+        plan->grid_ctas = ((num_heads + heads_per_simt_cta() - 1) / heads_per_simt_cta()) * batch * S;
+
+    uint64_t off = kStatusBytes;
+    if (S > 1) {
+        plan->partial_offset = off;
+        off = align_up(off + uint64_t(batch) * num_heads * S * kLkv * sizeof(float), 256);
+        plan->lse_partial_offset = off;
+        off = align_up(off + uint64_t(batch) * num_heads * S * sizeof(float), 256);
+    }
+    plan->workspace_bytes = off;
+    return MLA_OK;
+}
+
+extern "C" const char* mla_status_string(int status) {
+    switch (status) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported shape or kernel";
+        case MLA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case MLA_ERR_CUDA: return "CUDA runtime error";
+        case MLA_ERR_BAD_BLOCK_ID: return "block_table entry outside [0, num_blocks)";
+        case MLA_ERR_BAD_SEQ_LEN: return "seq_len negative or beyond the block table";
+        case MLA_ERR_TIMEOUT: return "bounded device wait expired";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int mla_abi_version(void) { return MLA_DECODE_ABI_VERSION; }

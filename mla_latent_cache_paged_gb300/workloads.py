@@ -203,3 +203,19 @@ HEADLINE = "b128_n128_l8192"
 
 def get_workload(name, with_data=True):
     return WORKLOADS[name](with_data=with_data)
+
+
+def to_torch(w, device="cuda"):
+    """Device tensors of a workload: q, latent_cache (bf16), block_table, seq_lens (int32)."""
+    import torch
+    q = torch.from_numpy(w.q_bits.view(np.int16)).view(torch.bfloat16).to(device)
+    cache = torch.from_numpy(w.cache_bits.view(np.int16)).view(torch.bfloat16).to(device)
+    table = torch.from_numpy(np.ascontiguousarray(w.block_table)).to(device)
+    lens = torch.from_numpy(np.ascontiguousarray(w.seq_lens)).to(device)
+    return q, cache, table, lens
+
+
+def bf16_tensor_bits(t):
+    """uint16 bit patterns (numpy) of a bf16 torch tensor."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

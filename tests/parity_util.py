@@ -1,0 +1,92 @@
+"""Shared helpers for the GPU parity tests (CUDA path vs the CPU oracle)."""
+
+import numpy as np
+
+from mla_latent_cache_paged_gb300 import binding
+from mla_latent_cache_paged_gb300.workloads import (bf16_bits_to_f64, bf16_tensor_bits,
+                                                    to_torch)
+from oracle import mla_decode_reference
+
+# Tolerances. bf16 output: |gpu - oracle| <= max(2e-2, one bf16 ulp of the
+# oracle value) -- a bf16 result cannot be closer than half an ulp, and for
+# |out| >= 4 (possible with the x8 outlier rows) half an ulp alone exceeds
+# 2e-2. LSE (fp32): absolute 1e-3.
+OUT_ATOL = 2e-2
+LSE_ATOL = 1e-3
+
+
+def bf16_ulp(x):
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
+def out_tolerance(ref):
+    return np.maximum(OUT_ATOL, bf16_ulp(ref))
+
+
+def assert_out_close(got_f64, ref, what=""):
+    tol = out_tolerance(ref)
+    err = np.abs(got_f64 - ref)
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = np.argwhere(bad)[0]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} outputs outside tolerance; first at {tuple(idx)}: "
+            f"gpu={got_f64[tuple(idx)]!r} oracle={ref[tuple(idx)]!r} tol={tol[tuple(idx)]!r}")
+    return float(err.max()) if err.size else 0.0
+
+
+def assert_lse_close(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    both_inf = np.isneginf(got) & np.isneginf(ref)
+    err = np.where(both_inf, 0.0, np.abs(got - ref))
+    bad = ~(err <= LSE_ATOL)
+    if bad.any():
+        idx = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: lse mismatch at {tuple(idx)}: gpu={got[tuple(idx)]!r} "
+                             f"oracle={ref[tuple(idx)]!r}")
+    return float(err.max()) if err.size else 0.0
+
+
+def run_decode(w, num_kv_splits=None, force_simt=False, device="cuda"):
+    """Run the CUDA path on workload `w`; returns (out_f64, lse, plan, tensors)."""
+    import torch
+    q, cache, table, lens = to_torch(w, device)
+    splits = w.num_kv_splits if num_kv_splits is None else num_kv_splits
+    plan = binding.make_plan(w.batch, w.num_heads, w.max_blocks_per_seq,
+                             seq_lens_host=w.seq_lens, max_seq_len=max(w.max_seq_len, 0),
+                             num_kv_splits=splits, force_simt=force_simt)
+    ws = binding.new_workspace(plan, device)
+    out, lse = binding.mla_decode(q, cache, table, lens, w.softmax_scale, plan=plan,
+                                  workspace=ws)
+    torch.cuda.synchronize()
+    status = binding.read_error(ws)
+    assert status == 0, f"device status {status}: {binding.status_string(status)}"
+    got = bf16_bits_to_f64(bf16_tensor_bits(out))
+    return got, lse.double().cpu().numpy(), plan, dict(q=q, cache=cache, table=table,
+                                                       lens=lens, ws=ws, out=out, lse=lse)
+
+
+def oracle_rows(w, requests):
+    """Oracle out/lse (all heads) for the listed requests of workload `w`.
+
+    Only the blocks those requests reference are widened to float64; they are
+    renumbered into a compact pool (pure re-indexing) and handed, with the
+    matching block table, to ``oracle.mla_decode_reference``.
+    """
+    requests = list(requests)
+    ps = w.page_size
+    used = []
+    for b in requests:
+        used.extend(int(x) for x in w.block_table[b, :-(-int(w.seq_lens[b]) // ps)])
+    ids = sorted(set(used))
+    remap = {old: new for new, old in enumerate(ids)}
+    pool = bf16_bits_to_f64(w.cache_bits[np.array(ids, dtype=np.int64)]) if ids else \
+        np.zeros((1, ps, w.cache_bits.shape[2]))
+    table = np.full((len(requests), w.block_table.shape[1]), -1, dtype=np.int64)
+    for i, b in enumerate(requests):
+        n = -(-int(w.seq_lens[b]) // ps)
+        table[i, :n] = [remap[int(x)] for x in w.block_table[b, :n]]
+    q = bf16_bits_to_f64(w.q_bits[np.array(requests, dtype=np.int64)])
+    return mla_decode_reference(q, pool, table, w.seq_lens[requests], w.softmax_scale)

@@ -1,0 +1,174 @@
+"""The C ABI without a GPU: symbols, struct layout, planner, host-side checks."""
+
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+from mla_latent_cache_paged_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(mla_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 8
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(binding.EXPORTED_SYMBOLS)
+    assert lib.mla_abi_version() == 1
+
+
+def test_plan_struct_layout_matches_the_header(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "mla_decode.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(mla_decode_plan_t),"
+        " offsetof(mla_decode_plan_t, flags), offsetof(mla_decode_plan_t, workspace_bytes),"
+        " offsetof(mla_decode_plan_t, lse_partial_offset), offsetof(mla_decode_plan_t, reserved));"
+        "return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    P = binding.MlaDecodePlan
+    want = [ctypes.sizeof(P), P.flags.offset, P.workspace_bytes.offset,
+            P.lse_partial_offset.offset, P.reserved.offset]
+    assert got == want
+
+
+def _plan(lib, batch=4, heads=128, max_blocks=32, max_seq=2048, lens=None, splits=0,
+          sms=152, flags=0, kv=512, rope=64, ps=64):
+    plan = binding.MlaDecodePlan()
+    ptr = ctypes.c_void_p(0)
+    keep = None
+    if lens is not None:
+        keep = np.ascontiguousarray(np.asarray(lens, np.int32))
+        ptr = ctypes.c_void_p(keep.ctypes.data)
+    rc = lib.mla_decode_plan(batch, heads, kv, rope, ps, max_blocks, max_seq, ptr, splits, sms,
+                             flags, ctypes.byref(plan))
+    return rc, plan
+
+
+def test_plan_fixed_splits_and_workspace_layout(lib):
+    rc, p = _plan(lib, batch=4, heads=128, splits=64)
+    assert rc == 0 and p.num_kv_splits == 64
+    assert p.partial_offset == 256
+    assert p.lse_partial_offset >= p.partial_offset + 4 * 128 * 64 * 512 * 4
+    assert p.workspace_bytes >= p.lse_partial_offset + 4 * 128 * 64 * 4
+    assert p.workspace_bytes % 256 == 0
+    rc, p1 = _plan(lib, splits=1)
+    assert rc == 0 and p1.num_kv_splits == 1 and p1.workspace_bytes == 256
+
+
+def test_planner_choice_is_bounded_and_deterministic(lib):
+    for batch, seq in [(1, 256), (32, 4096), (128, 8192), (4, 131072), (256, 32768)]:
+        mb = -(-seq // 64)
+        rc, p = _plan(lib, batch=batch, max_blocks=mb, max_seq=seq)
+        assert rc == 0
+        assert 1 <= p.num_kv_splits <= min(64, mb)
+        rc2, p2 = _plan(lib, batch=batch, max_blocks=mb, max_seq=seq)
+        assert p2.num_kv_splits == p.num_kv_splits
+    # a long single request must be split to use the GPU
+    rc, p = _plan(lib, batch=1, max_blocks=2048, max_seq=131072)
+    assert p.num_kv_splits > 8
+
+
+def test_planner_uses_host_lengths(lib):
+    lens = [16] * 255 + [32768]
+    rc, p = _plan(lib, batch=256, max_blocks=512, max_seq=32768, lens=lens)
+    assert rc == 0 and p.num_kv_splits >= 1
+    rc, _ = _plan(lib, batch=2, max_blocks=4, max_seq=256, lens=[10, 300])
+    assert rc == binding.MLA_ERR_INVALID_ARG
+
+
+def test_plan_force_simt_flag(lib):
+    rc, p = _plan(lib, flags=binding.MLA_PLAN_FORCE_SIMT)
+    assert rc == 0 and p.kernel == binding.MLA_KERNEL_SIMT
+    assert p.grid_ctas == 8 * p.batch * p.num_kv_splits
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kv=256), binding.MLA_ERR_UNSUPPORTED),
+    (dict(rope=32), binding.MLA_ERR_UNSUPPORTED),
+    (dict(ps=16), binding.MLA_ERR_UNSUPPORTED),
+    (dict(heads=129), binding.MLA_ERR_UNSUPPORTED),
+    (dict(heads=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(batch=-1), binding.MLA_ERR_INVALID_ARG),
+    (dict(max_blocks=0), binding.MLA_ERR_INVALID_ARG),
+    (dict(max_seq=2049), binding.MLA_ERR_INVALID_ARG),
+    (dict(splits=-2), binding.MLA_ERR_INVALID_ARG),
+    (dict(splits=1025), binding.MLA_ERR_UNSUPPORTED),
+    (dict(sms=0), binding.MLA_ERR_INVALID_ARG),
+])
+def test_plan_rejects_bad_arguments(lib, kw, code):
+    rc, _ = _plan(lib, **kw)
+    assert rc == code
+
+
+def test_decode_rejects_bad_arguments_before_touching_the_device(lib):
+    rc, p = _plan(lib, batch=2, heads=16, max_blocks=4, max_seq=256, splits=1)
+    assert rc == 0
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: checks fail first
+    null = ctypes.c_void_p(0)
+    args = lambda **o: [ctypes.byref(o.get("plan", p)), o.get("q", fake), o.get("cache", fake),
+                        o.get("nb", 8), o.get("bt", fake), o.get("sl", fake),
+                        o.get("scale", 0.07), o.get("out", fake), o.get("lse", null),
+                        o.get("ws", fake), o.get("wsb", 4096), null]
+    assert lib.mla_decode(*args(q=null)) == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode(*args(out=null)) == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode(*args(nb=0)) == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode(*args(scale=float("nan"))) == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode(*args(q=ctypes.c_void_p(0x10008))) == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode(*args(ws=null)) == binding.MLA_ERR_WORKSPACE
+    assert lib.mla_decode(*args(wsb=16)) == binding.MLA_ERR_WORKSPACE
+    assert lib.mla_decode(*args(ws=ctypes.c_void_p(0x10010))) == binding.MLA_ERR_WORKSPACE
+    bad = binding.MlaDecodePlan.from_buffer_copy(p)
+    bad.kv_lora_rank = 320
+    assert lib.mla_decode(*args(plan=bad)) == binding.MLA_ERR_UNSUPPORTED
+    bad = binding.MlaDecodePlan.from_buffer_copy(p)
+    bad.num_kv_splits = 0
+    assert lib.mla_decode(*args(plan=bad)) == binding.MLA_ERR_INVALID_ARG
+
+
+def test_merge_and_gather_reject_bad_arguments(lib):
+    fake = ctypes.c_void_p(0x10000)
+    null = ctypes.c_void_p(0)
+    assert lib.mla_merge_splits(fake, fake, 1, 1, 0, 512, fake, null, null) == \
+        binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_splits(fake, fake, 1, 1, 2, 500, fake, null, null) == \
+        binding.MLA_ERR_UNSUPPORTED
+    assert lib.mla_merge_splits(null, fake, 1, 1, 2, 512, fake, null, null) == \
+        binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_debug_gather_pages(fake, 4, fake, fake, 1, 0, 64, fake, fake, 256, null) == \
+        binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_debug_gather_pages(fake, 4, fake, fake, 1, 1, 64, fake, null, 256, null) == \
+        binding.MLA_ERR_WORKSPACE
+
+
+def test_status_strings(lib):
+    for code in range(-7, 1):
+        assert lib.mla_status_string(code)
+    assert b"block" in lib.mla_status_string(binding.MLA_ERR_BAD_BLOCK_ID)
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        binding.load_library(str(tmp_path / "missing.so"))

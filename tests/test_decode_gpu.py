@@ -1,0 +1,181 @@
+"""GPU parity: mla_decode (through the C ABI) against the CPU oracle."""
+
+import math
+
+import numpy as np
+import pytest
+
+from mla_latent_cache_paged_gb300 import binding
+from mla_latent_cache_paged_gb300.workloads import (BF16_NAN, bf16_tensor_bits, get_workload,
+                                                    make_workload, to_torch)
+from oracle import merge_partials, mla_decode_split_partials
+from parity_util import (assert_lse_close, assert_out_close, oracle_rows, run_decode)
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = ["simt", "auto"]
+
+
+def _force(kernel):
+    return kernel == "simt"
+
+
+def _full_check(w, kernel, splits=None):
+    got, lse, plan, _ = run_decode(w, num_kv_splits=splits, force_simt=_force(kernel))
+    ref_out, ref_lse = oracle_rows(w, range(w.batch))
+    e_out = assert_out_close(got, ref_out, w.name)
+    e_lse = assert_lse_close(lse, ref_lse, w.name)
+    return e_out, e_lse, plan
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("heads,lens,splits", [
+    (16, [256], 1),
+    (128, [1, 63, 64, 65, 300, 1000], 1),
+    (128, [1, 63, 64, 65, 300, 1000], 3),
+    (128, [1, 63, 64, 65, 300, 1000], 32),
+    (5, [130, 7], 2),
+    (64, [517, 2048], 0),
+    (128, [0, 100], 1),
+    (128, [0, 100, 0], 4),
+])
+def test_small_parity(kernel, heads, lens, splits):
+    w = make_workload(f"small_n{heads}", len(lens), heads, lens, seed=1000 + heads + len(lens),
+                      extra_blocks=3, num_kv_splits=splits)
+    _full_check(w, kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_single_token_returns_cached_row_bit_exact(kernel):
+    w = make_workload("one_token", 3, 128, [1, 1, 1], seed=7, extra_blocks=2, num_kv_splits=1)
+    got, lse, _, t = run_decode(w, force_simt=_force(kernel))
+    out_bits = bf16_tensor_bits(t["out"])
+    for b in range(3):
+        row = w.cache_bits[w.block_table[b, 0], 0, :512]
+        assert np.array_equal(out_bits[b], np.broadcast_to(row, (128, 512))), b
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_page_permutation_gives_bit_identical_output(kernel):
+    lens = [70, 640, 129]
+    w1 = make_workload("perm", 3, 128, lens, seed=11, extra_blocks=5, num_kv_splits=1)
+    # Same logical rows, another physical arrangement of the pool.
+    rng = np.random.default_rng(99)
+    nb = w1.num_blocks + 4
+    perm = rng.permutation(nb)
+    cache2 = np.full((nb, 64, 576), BF16_NAN, dtype=np.uint16)
+    table2 = np.full_like(w1.block_table, -1)
+    pos = 0
+    for b, L in enumerate(lens):
+        for j in range(-(-L // 64)):
+            cache2[perm[pos]] = w1.cache_bits[w1.block_table[b, j]]
+            table2[b, j] = perm[pos]
+            pos += 1
+    w2 = make_workload("perm", 3, 128, lens, seed=11, extra_blocks=5, num_kv_splits=1)
+    w2.cache_bits, w2.block_table, w2.num_blocks = cache2, table2, nb
+    _, _, _, t1 = run_decode(w1, force_simt=_force(kernel))
+    _, _, _, t2 = run_decode(w2, force_simt=_force(kernel))
+    assert np.array_equal(bf16_tensor_bits(t1["out"]), bf16_tensor_bits(t2["out"]))
+    assert np.array_equal(t1["lse"].cpu().numpy(), t2["lse"].cpu().numpy())
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_split_partials_follow_the_page_aligned_partition(kernel):
+    import torch
+    lens = [1, 65, 640, 1000]
+    S = 5
+    w = make_workload("partials", 4, 128, lens, seed=21, extra_blocks=1, num_kv_splits=S)
+    _, _, plan, t = run_decode(w, force_simt=_force(kernel))
+    ws = t["ws"]
+    B, N = w.batch, w.num_heads
+    o_part = ws[plan.partial_offset:plan.partial_offset + B * N * S * 512 * 4]
+    o_part = o_part.view(torch.float32).view(B, N, S, 512).double().cpu().numpy()
+    l_part = ws[plan.lse_partial_offset:plan.lse_partial_offset + B * N * S * 4]
+    l_part = l_part.view(torch.float32).view(B, N, S).double().cpu().numpy()
+    ref_o, ref_l = mla_decode_split_partials(w.q_f64(), w.cache_f64(), w.block_table,
+                                             w.seq_lens, w.softmax_scale, S)
+    assert np.array_equal(np.isneginf(l_part), np.isneginf(ref_l))
+    assert_lse_close(l_part, ref_l, "lse partials")
+    err = np.abs(o_part - ref_o).max()
+    assert err < 2e-3, err
+
+
+def test_merge_splits_against_oracle():
+    import torch
+    rng = np.random.default_rng(5)
+    B, N, S, V = 3, 7, 9, 512
+    o = rng.standard_normal((B, N, S, V)).astype(np.float32)
+    ls = (rng.standard_normal((B, N, S)) * 3).astype(np.float32)
+    ls[0, 0, :] = -np.inf                  # all neutral
+    ls[1, 2, ::2] = -np.inf                # some neutral
+    o[1, 2, ::2] = np.nan                  # neutral partials' contents are never read
+    o[0, 0] = np.nan
+    out, lse = binding.mla_merge_splits(torch.from_numpy(o).cuda(), torch.from_numpy(ls).cuda())
+    torch.cuda.synchronize()
+    o_ref = np.where(np.isneginf(ls)[..., None], 0.0, o.astype(np.float64))
+    ref_out, ref_lse = merge_partials(o_ref, ls.astype(np.float64))
+    got = bf16_tensor_bits(out).astype(np.uint32) << 16
+    got = got.view(np.float32).astype(np.float64)
+    assert_out_close(got, ref_out, "merge")
+    assert_lse_close(lse.double().cpu().numpy(), ref_lse, "merge lse")
+    assert np.all(got[0, 0] == 0) and np.isneginf(lse[0, 0].item())
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_bad_block_id_is_reported_not_faulted(kernel):
+    import torch
+    w = make_workload("bad_block", 2, 128, [200, 64], seed=31, num_kv_splits=1)
+    q, cache, table, lens = to_torch(w)
+    table[0, 1] = w.num_blocks + 1000
+    table[1, 0] = -5
+    plan = binding.make_plan(2, 128, w.max_blocks_per_seq, num_kv_splits=1,
+                             force_simt=_force(kernel))
+    ws = binding.new_workspace(plan)
+    out, lse = binding.mla_decode(q, cache, table, lens, w.softmax_scale, plan=plan, workspace=ws)
+    assert binding.read_error(ws) == binding.MLA_ERR_BAD_BLOCK_ID
+    assert binding.read_error(ws) == 0           # reading clears the word
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_bad_seq_len_is_reported(kernel):
+    w = make_workload("bad_len", 2, 128, [200, 64], seed=32, num_kv_splits=1)
+    q, cache, table, lens = to_torch(w)
+    lens[1] = w.max_blocks_per_seq * 64 + 1
+    plan = binding.make_plan(2, 128, w.max_blocks_per_seq, num_kv_splits=1,
+                             force_simt=_force(kernel))
+    ws = binding.new_workspace(plan)
+    out, lse = binding.mla_decode(q, cache, table, lens, w.softmax_scale, plan=plan, workspace=ws)
+    assert binding.read_error(ws) == binding.MLA_ERR_BAD_SEQ_LEN
+    assert math.isinf(lse[1, 0].item())
+
+
+# ---------------------------------------------------------------- full size
+
+@pytest.mark.parametrize("name,sample", [
+    ("b1_n16_l256_pool8", None),
+    ("b32_n128_l1k-4k", None),
+    ("b128_n128_l8192", [0, 17, 63, 64, 101, 127]),
+    ("b4_n128_l32k_s64", None),
+    ("b4_n128_l64k_s64", [0, 3]),
+    ("b4_n128_l96k_s64", [1]),
+    ("b4_n128_l128k_s64", [0, 2]),
+    ("b256_n128_logu16-32k_outliers", "mix"),
+])
+def test_full_size_configs(name, sample):
+    """Full-size configs in the launch configuration the benchmark uses
+    (the planner's kernel and split count), checked on sampled requests."""
+    w = get_workload(name)
+    got, lse, plan, _ = run_decode(w)
+    if sample is None:
+        reqs = list(range(w.batch))
+    elif sample == "mix":
+        order = np.argsort(w.seq_lens)
+        reqs = sorted(set(order[:6].tolist() + order[-4:].tolist() + [100, 200]))
+    else:
+        reqs = sample
+    ref_out, ref_lse = oracle_rows(w, reqs)
+    e_out = assert_out_close(got[reqs], ref_out, name)
+    e_lse = assert_lse_close(lse[reqs], ref_lse, name)
+    print(f"{name}: kernel={plan.kernel} S={plan.num_kv_splits} "
+          f"max|out err|={e_out:.3g} max|lse err|={e_lse:.3g}")
