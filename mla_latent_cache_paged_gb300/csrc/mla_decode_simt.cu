@@ -73,10 +73,13 @@ __global__ void __launch_bounds__(kThreads, 2) mla_decode_simt_kernel(DecodePara
     const int my_d0 = warp * kDimsPerWarp + (lane >> 4) * kDimsPerThread;
     float qreg[kDimsPerThread];
     {
-        const bool ok = (h0 + my_h) < N;
-        const uint16_t* qrow = p.q + (size_t(b) * N + (h0 + my_h)) * kD + my_d0;
 #pragma unroll
-        for (int i = 0; i < kDimsPerThread; ++i) qreg[i] = ok ? bf16_bits_to_f32(qrow[i]) : 0.f;
+        for (int i = 0; i < kDimsPerThread; ++i) qreg[i] = 0.f;
+        if ((h0 + my_h) < N) {
+            const uint16_t* qrow = p.q + (size_t(b) * N + (h0 + my_h)) * kD + my_d0;
+#pragma unroll
+            for (int i = 0; i < kDimsPerThread; ++i) qreg[i] = bf16_bits_to_f32(qrow[i]);
+        }
     }
     if (tid < kHG) {
         sm.m[tid] = -INFINITY;
