@@ -38,6 +38,7 @@ extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const vo
         return MLA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < plan->workspace_bytes || !aligned(workspace, 256))
         return MLA_ERR_WORKSPACE;
+    if (plan->kernel == MLA_KERNEL_TC && num_blocks > tc_max_blocks()) return MLA_ERR_UNSUPPORTED;
     if (plan->batch == 0) return MLA_OK;
 
     const int S = plan->num_kv_splits;

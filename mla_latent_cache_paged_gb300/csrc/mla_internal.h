@@ -55,5 +55,6 @@ int launch_gather(const uint16_t* cache, int64_t num_blocks, const int32_t* bloc
 // Host-side helpers from mla_plan.cpp.
 int validate_plan(const mla_decode_plan_t* plan);
 bool tc_kernel_built();
+int tc_max_blocks();
 
 }  // namespace mla

@@ -112,8 +112,11 @@ extern "C" int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int r
         }
     }
 
+    // The tensor-core kernel pads the heads to an M=128 tile; below 32 heads
+    // the CUDA-core kernel is the better fit (little work per cached byte).
     int kernel = MLA_KERNEL_TC;
-    if ((flags & MLA_PLAN_FORCE_SIMT) || !tc_kernel_built()) kernel = MLA_KERNEL_SIMT;
+    if ((flags & MLA_PLAN_FORCE_SIMT) || !tc_kernel_built() || num_heads <= 32)
+        kernel = MLA_KERNEL_SIMT;
 
     int S = num_kv_splits;
     if (S == 0) {

@@ -40,7 +40,8 @@ def assert_out_close(got_f64, ref, what=""):
 def assert_lse_close(got, ref, what=""):
     got = np.asarray(got, dtype=np.float64)
     both_inf = np.isneginf(got) & np.isneginf(ref)
-    err = np.where(both_inf, 0.0, np.abs(got - ref))
+    with np.errstate(invalid="ignore"):
+        err = np.where(both_inf, 0.0, np.abs(got - ref))
     bad = ~(err <= LSE_ATOL)
     if bad.any():
         idx = np.argwhere(bad)[0]

@@ -96,8 +96,11 @@ def test_split_partials_follow_the_page_aligned_partition(kernel):
                                              w.seq_lens, w.softmax_scale, S)
     assert np.array_equal(np.isneginf(l_part), np.isneginf(ref_l))
     assert_lse_close(l_part, ref_l, "lse partials")
+    # fp32 partials: the tensor-core kernel rounds P to bf16 for the P.V MMA
+    # (relative 2^-9 per weight, so up to ~2^-9 * max|V| ~ 0.01 here); the
+    # bound is the one the bf16 output is held to.
     err = np.abs(o_part - ref_o).max()
-    assert err < 2e-3, err
+    assert err < 2e-2, err
 
 
 def test_merge_splits_against_oracle():
