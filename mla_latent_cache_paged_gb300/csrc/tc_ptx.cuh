@@ -51,6 +51,18 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                  : "memory");
 }
 
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -104,6 +116,41 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// Same load, delivered to the same offset of every CTA in `cta_mask` (their
+// mbarriers at `bar`'s offset receive the byte count).
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, int32_t x,
+                                               int32_t y, uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
+// cluster shared-memory address; completes bytes on a (possibly remote) mbarrier.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
+                                                     uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+        " [%0], [%1], %2, [%3];" ::"r"(dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk copy of this thread has read its source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -153,6 +200,16 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
+// when every prior tcgen05 op of this thread completes.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // Arrive once on a local mbarrier when every prior tcgen05 op of this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -198,18 +255,33 @@ __device__ __forceinline__ float ex2(float x) {
 
 // ------------------------------------------------------- UMMA descriptors
 
-// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), version 1.
-//   K-major operand: 8-row groups of 128-byte rows, `sbo` = 1024 between groups.
+// Shared-memory matrix descriptor (version 1) for a swizzled layout.
+//   K-major operand: 8-row groups of swizzle-width rows, `sbo` bytes apart.
 //   MN-major operand: `lbo` = byte stride between 64-element column blocks,
 //                     `sbo` = byte stride between 8-row groups along K.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// layout: 2 = 128-byte swizzle, 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t desc_swz(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                             uint32_t layout) {
     uint64_t d = 0;
     d |= uint64_t((saddr & 0x3FFFFu) >> 4);
     d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
     d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
     d |= uint64_t(1) << 46;
-    d |= uint64_t(2) << 61;
+    d |= uint64_t(layout & 7u) << 61;
     return d;
+}
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return desc_swz(saddr, lbo, sbo, 2);
+}
+
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr, uint32_t sbo) {
+    return desc_swz(saddr, 16, sbo, 4);
+}
+
+// Exact 2^k for an integer k; 0 below the normal range.
+__device__ __forceinline__ float pow2i(int k) {
+    return k < -126 ? 0.f : __int_as_float((127 + min(k, 127)) << 23);
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, M = 128.
