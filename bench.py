@@ -32,7 +32,7 @@ UNIT = "cached-tokens*heads/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_KERNEL_SOURCES = {
     1: ["mla_decode_simt.cu", "mla_device.cuh", "mla_internal.h"],
-    2: ["mla_decode_tc.cu", "mla_device.cuh", "mla_internal.h"],
+    2: ["mla_decode_tc.cu", "tc_ptx.cuh", "mla_device.cuh", "mla_internal.h"],
 }
 
 
