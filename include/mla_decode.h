@@ -23,7 +23,8 @@
  * Conventions for every entry point.
  *   - All device pointers are caller-owned; the library never allocates or
  *     frees device memory. Scratch space is the caller's `workspace`, sized
- *     by mla_decode_plan.
+ *     by mla_decode_plan (mla_decode_noalloc instead uses a fixed array
+ *     inside the library, see its comment).
  *   - Every call returns an int status: MLA_OK (0) or a negative MLA_ERR_*.
  *     Argument errors are detected on the host before anything is enqueued.
  *   - Device work is enqueued asynchronously on `stream` (a cudaStream_t
@@ -59,6 +60,7 @@ extern "C" {
 #define MLA_ERR_BAD_BLOCK_ID  -5  /* device: block_table entry outside [0, num_blocks) */
 #define MLA_ERR_BAD_SEQ_LEN   -6  /* device: seq_len < 0 or > max_blocks_per_seq*page_size */
 #define MLA_ERR_TIMEOUT       -7  /* device: a bounded wait inside a kernel expired */
+#define MLA_ERR_SCRATCH_LIMIT -8  /* mla_decode_noalloc: plan needs more than its fixed scratch */
 
 /* Kernel variants the planner can choose (mla_decode_plan_t.kernel). */
 #define MLA_KERNEL_SIMT   1  /* CUDA-core split kernel, any 1 <= N <= 128 */
@@ -154,6 +156,40 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* latent_
                int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
                float softmax_scale, void* out, float* lse,
                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode_noalloc -- mla_decode for callers that cannot allocate device
+ * memory. The pages have no counterpart to this entry point.
+ *
+ * Who needs it: code that may not allocate while it runs (an allocation can
+ * synchronise the device, and many serving loops forbid it), runtimes that
+ * hand out all device memory from their own pools and have no allocator to
+ * offer, and bindings that can pass only the operation's own tensors. Such a
+ * caller passes the inputs and outputs of mla_decode and no workspace.
+ *
+ * Scratch: the status words and the split partials live in one fixed device
+ * array of 32 MiB inside the library; every GPU that loads the library holds
+ * it until the process exits. A plan whose workspace_bytes exceeds 32 MiB is
+ * rejected with MLA_ERR_SCRATCH_LIMIT (the partials take B*N*S*2,052 bytes:
+ * for example B=32, N=128, S=4 fits; B=4, N=128, S=64 does not).
+ *
+ *   plan, q, latent_cache, num_blocks, block_table, seq_lens, softmax_scale,
+ *   out, lse, stream   as for mla_decode.
+ *   device_status      optional device int32[2] (4-byte aligned) that receives
+ *                      the device-detected status (MLA_OK or MLA_ERR_*) and a
+ *                      detail word; the call zeroes it first. NULL keeps the
+ *                      status inside the library's scratch, unreadable.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture. Every call uses the same array and leaves its contents behind, so
+ * calls that overlap on the GPU (other streams, other host threads, the same
+ * device) race with each other: serialise them.
+ */
+int mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
+                       int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                       float softmax_scale, void* out, float* lse, int32_t* device_status,
+                       void* stream);
 
 /*
  * mla_merge_splits -- LSE-weighted merge of S partial attention results.

@@ -21,6 +21,7 @@ MLA_ERR_CUDA = -4
 MLA_ERR_BAD_BLOCK_ID = -5
 MLA_ERR_BAD_SEQ_LEN = -6
 MLA_ERR_TIMEOUT = -7
+MLA_ERR_SCRATCH_LIMIT = -8
 
 MLA_KERNEL_SIMT = 1
 MLA_KERNEL_TC = 2
@@ -35,6 +36,7 @@ STATUS_BYTES = 256
 EXPORTED_SYMBOLS = (
     "mla_decode_plan", "mla_workspace_init", "mla_decode", "mla_merge_splits",
     "mla_read_error", "mla_status_string", "mla_abi_version", "mla_debug_gather_pages",
+    "mla_decode_noalloc",
 )
 
 
@@ -93,6 +95,8 @@ def load_library(path=None):
     lib.mla_status_string.restype = ctypes.c_char_p
     lib.mla_abi_version.argtypes = []
     lib.mla_debug_gather_pages.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, sz, vp]
+    lib.mla_decode_noalloc.argtypes = [ctypes.POINTER(MlaDecodePlan), vp, vp, i64, vp, vp, f32, vp,
+                                       vp, vp, vp]
     for name in EXPORTED_SYMBOLS:
         if name not in ("mla_status_string",):
             getattr(lib, name).restype = ctypes.c_int
@@ -249,3 +253,23 @@ def debug_gather_pages(latent_cache, block_table, seq_lens, dst, workspace, stre
         int(workspace.numel()), _stream_ptr(stream))
     _check(rc, "mla_debug_gather_pages")
     return dst
+
+
+def mla_decode_noalloc(q, latent_cache, block_table, seq_lens, softmax_scale, *, plan,
+                       out=None, lse=None, device_status=None, stream=None):
+    """The decode without a workspace, for callers that cannot allocate device
+    memory (see ``mla_decode_noalloc`` in include/mla_decode.h): scratch comes
+    from a fixed array inside the library. ``out``/``lse``/``device_status``
+    may be given preallocated; nothing here allocates when all three are."""
+    import torch
+    B, N, _ = q.shape
+    if out is None:
+        out = torch.empty((B, N, KV_LORA_RANK), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, N), dtype=torch.float32, device=q.device)
+    rc = load_library().mla_decode_noalloc(
+        ctypes.byref(plan), _ptr(q), _ptr(latent_cache), int(latent_cache.shape[0]),
+        _ptr(block_table), _ptr(seq_lens), float(softmax_scale), _ptr(out), _ptr(lse),
+        _ptr(device_status), _stream_ptr(stream))
+    _check(rc, "mla_decode_noalloc")
+    return out, lse

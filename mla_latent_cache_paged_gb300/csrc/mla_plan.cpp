@@ -172,6 +172,8 @@ extern "C" const char* mla_status_string(int status) {
         case MLA_ERR_BAD_BLOCK_ID: return "block_table entry outside [0, num_blocks)";
         case MLA_ERR_BAD_SEQ_LEN: return "seq_len negative or beyond the block table";
         case MLA_ERR_TIMEOUT: return "bounded device wait expired";
+        case MLA_ERR_SCRATCH_LIMIT:
+            return "plan needs more scratch than the 32 MiB of mla_decode_noalloc";
         default: return "unknown status";
     }
 }
