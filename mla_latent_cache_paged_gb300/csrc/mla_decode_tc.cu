@@ -31,8 +31,11 @@
 // Two score buffers in TMEM let the score MMAs of the next page run while the
 // softmax works on the current one.
 //
-// Warp roles: 0 = TMA producer, 1 = score MMAs, 6 = P.V MMAs, 2-5 = softmax,
-// O correction and epilogue. Every wait is bounded: on expiry the kernel
+// Warp roles: 0 = K-ring loads (and L2 prefetch), 6 = V-ring loads,
+// 1 = score MMAs, 2-5 = softmax, P.V MMAs, O correction and epilogue. The
+// two rings have their own producers, so a page's K blocks never wait behind
+// the previous page's V slot; the softmax warp that finishes a page last
+// issues its P.V MMAs, with no hand-off to another warp. Every wait is bounded: on expiry the kernel
 // records MLA_ERR_TIMEOUT, lets each role leave its loop, waits (bounded) for
 // its own loads and MMAs, frees TMEM and returns. A block id outside the pool
 // is recorded and loaded from negative rows, which TMA fills with zeros.
@@ -86,11 +89,11 @@ struct TcBars {
     uint64_t kfull[2];    // TMA: K-ring blocks landed
     uint64_t kempty[2];   // score MMAs done with them
     uint64_t s_full[2];   // score MMAs of the page complete
-    uint64_t p_full[2];   // softmax wrote P (128 arrivals)
     uint64_t p_free[2];   // P.V MMA complete: score buffer free, O current
     uint64_t q_ready;     // q staged (128 arrivals)
     uint64_t final_qk;    // drain of the score warp's MMAs
-    uint64_t final_pv;    // drain of the P.V warp's MMAs
+    uint64_t final_sm[4]; // drain of each softmax warp's P.V MMAs
+    uint32_t p_count[2];  // softmax warps done with the pages of each parity
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -98,7 +101,7 @@ static_assert(sizeof(TcBars) <= 256, "barrier block too large");
 
 enum WaitSite : int32_t {
     kSiteVEmpty = 1, kSiteKEmpty, kSiteSFull, kSiteSFree, kSitePvDone, kSiteQReady,
-    kSiteDrain, kSiteKFull, kSiteVFull, kSitePFull
+    kSiteDrain, kSiteKFull, kSiteVFull
 };
 
 __device__ __forceinline__ bool aborting(TcBars* bars) {
@@ -145,13 +148,12 @@ __host__ __device__ constexpr int k_block(int rank, int pos) {
     return rank == 0 ? pos + 4 : (pos < 4 ? pos : 8);
 }
 
-// ------------------------------------------------------------ MMA warps
-// Two warps issue MMAs: one the score MMAs, one the P.V MMAs, each blocking
-// on its own barriers (a suspended wait, not a spin that would take issue
-// slots from the softmax warps). Each runs its loop in lockstep and one
-// elected lane issues every tcgen05 op; a page's score MMAs are unrolled at
-// compile time (a template on the CTA rank), so every operand is a
-// warp-uniform base plus a constant and the issue keeps up with the pipe.
+// ------------------------------------------------------------ MMA issue
+// The score warp blocks on its barriers in a suspended wait (not a spin that
+// would take issue slots from the softmax warps), runs its loop in lockstep
+// and issues every tcgen05 op from one elected lane; a page's score MMAs are
+// unrolled at compile time (a template on the CTA rank), so every operand is
+// a warp-uniform base plus a constant and the issue keeps up with the pipe.
 
 struct MmaWarpArgs {
     uint32_t tmem, sbase;
@@ -267,29 +269,21 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
     warp_drain(b_final, a);
 }
 
-// O += P V for every page once the softmax has written P.
-__device__ __forceinline__ void pv_warp(const MmaWarpArgs& a, const uint32_t* b) {
-    const uint32_t b_pfull = b[0], b_pfree = b[1], b_vempty = b[2], b_final = b[3];
+// O += P V for page np: P the A operand in TMEM, V (MN-major) from the V
+// ring. Issued by one elected lane of the softmax warp that finished the page
+// last; the commits release the V slot and the score buffer.
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int np, uint32_t b_vempty,
+                                         uint32_t b_pfree) {
     constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(256, true);
-    const uint32_t tmem = a.tmem;
-    for (int np = 0; np < a.ntiles; ++np) {
-        const int sl = np & 1;
-        if (!warp_wait(b_pfull + 8 * sl, uint32_t(np >> 1) & 1u, a, kSitePFull)) break;
-        ptx::tc_fence_after();
-        const uint32_t pcol = tmem + kTmemS + uint32_t(sl * 64);
-        const uint32_t vb = a.sbase + uint32_t(kOffV + sl * kVBytes);
-        if (ptx::elect_one()) {
+    const int sl = np & 1;
+    const uint32_t pcol = tmem + kTmemS + uint32_t(sl * 64);
+    const uint32_t vb = sbase + uint32_t(kOffV + sl * kVBytes);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                ptx::mma_ts(tmem + kTmemO, pcol + uint32_t(kk * 8),
-                            desc_vmn(vb + uint32_t(kk * 2048)), idesc_pv,
-                            (np > 0 || kk > 0) ? 1u : 0u);
-            ptx::mma_commit(b_vempty + 8 * sl);
-            ptx::mma_commit(b_pfree + 8 * sl);
-        }
-        __syncwarp();
-    }
-    warp_drain(b_final, a);
+    for (int kk = 0; kk < 4; ++kk)
+        ptx::mma_ts(tmem + kTmemO, pcol + uint32_t(kk * 8), desc_vmn(vb + uint32_t(kk * 2048)),
+                    idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+    ptx::mma_commit(b_vempty + 8 * sl);
+    ptx::mma_commit(b_pfree + 8 * sl);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -321,11 +315,11 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
     const uint32_t b_kfull = ptx::smem_addr(&bars->kfull[0]);
     const uint32_t b_kempty = ptx::smem_addr(&bars->kempty[0]);
     const uint32_t b_sfull = ptx::smem_addr(&bars->s_full[0]);
-    const uint32_t b_pfull = ptx::smem_addr(&bars->p_full[0]);
     const uint32_t b_pfree = ptx::smem_addr(&bars->p_free[0]);
     const uint32_t b_qready = ptx::smem_addr(&bars->q_ready);
     const uint32_t b_final_qk = ptx::smem_addr(&bars->final_qk);
-    const uint32_t b_final_pv = ptx::smem_addr(&bars->final_pv);
+    const uint32_t b_final_sm = ptx::smem_addr(&bars->final_sm[0]);
+    const uint32_t a_pcount = ptx::smem_addr(&bars->p_count[0]);
 
     if (tid == 0) {
         if (!aligned_ok) record_error(p.status, MLA_ERR_UNSUPPORTED, int32_t(sbase));
@@ -335,12 +329,12 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             ptx::mbar_init(b_kfull + 8 * i, 1);
             ptx::mbar_init(b_kempty + 8 * i, 1);
             ptx::mbar_init(b_sfull + 8 * i, 1);
-            ptx::mbar_init(b_pfull + 8 * i, 128);
+            bars->p_count[i] = 0;
             ptx::mbar_init(b_pfree + 8 * i, 1);
         }
         ptx::mbar_init(b_qready, 128);
         ptx::mbar_init(b_final_qk, 1);
-        ptx::mbar_init(b_final_pv, 1);
+        for (int i = 0; i < 4; ++i) ptx::mbar_init(b_final_sm + 8 * i, 1);
         bars->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -348,20 +342,36 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kTmemCols);
         ptx::tmem_relinquish();
     }
+    if (warp >= 2 && warp <= 5) {
+        // q dims 256..575 of head h -> shared memory (the A operand of the
+        // score MMAs for those dims), copied asynchronously right away; the
+        // rows of padded heads are zero-filled.
+        const int h = (warp & 3) * 32 + lane;
+        const bool live = h < N;
+        const uint16_t* qsrc = live ? p.q + (size_t(b) * N + h) * kD : p.q;
+#pragma unroll
+        for (int kb = 0; kb < 5; ++kb)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                ptx::cp_async16(sbase + uint32_t(kOffQS + kb * 16384 + h * 128 + ((c ^ (h & 7)) * 16)),
+                                qsrc + 64 * (kQTmemBlocks + kb) + 8 * c, live ? 16u : 0u);
+    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const MmaWarpArgs margs{tmem, sbase, bars, p.status, ntiles};
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 6) {
+        // ------------------------------------------------------ TMA producers
         if (lane == 0) {
+            const bool k_ring = warp == 0;
             const int32_t* table = p.block_table + size_t(b) * p.max_blocks;
-            // Each CTA of the pair pulls its half of page j + kPrefetchAhead
-            // into L2, so that the ring loads of both CTAs hit L2.
+            // The K producer of each CTA pulls its half of page
+            // j + kPrefetchAhead into L2, so that the ring loads of both CTAs
+            // hit L2.
             auto prefetch = [&](int j) {
-                if (j >= ntiles) return;
+                if (!k_ring || j >= ntiles) return;
                 const int32_t blk = table[page0 + j];
                 if (blk < 0 || int64_t(blk) >= p.num_blocks) return;
                 const unsigned char* page =
@@ -369,8 +379,12 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 ptx::prefetch_l2(page + rank * (kPageBytes / 2), kPageBytes / 2);
             };
             for (int j = 0; j < kPrefetchAhead; ++j) prefetch(j);
+            const uint32_t b_full = k_ring ? b_kfull : b_vfull;
+            const uint32_t b_empty = k_ring ? b_kempty : b_vempty;
+            const int bytes = k_ring ? kKBytes : kVBytes;
+            const uint32_t dst0 = sbase + uint32_t(k_ring ? kOffK : kOffV);
             int next = ntiles > 0 ? table[page0] : 0;
-            int k_issued = 0, v_issued = 0;
+            int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int blk = next;
                 if (j + 1 < ntiles) next = table[page0 + j + 1];
@@ -379,34 +393,31 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 if (blk >= 0 && int64_t(blk) < p.num_blocks) {
                     y = blk * kTile;
                 } else {
-                    record_error(p.status, MLA_ERR_BAD_BLOCK_ID, blk);
+                    if (k_ring) record_error(p.status, MLA_ERR_BAD_BLOCK_ID, blk);
                     y = -kTile;   // wholly outside the tensor: TMA writes zeros
                 }
                 const int sl = j & 1;
-                const uint32_t ph = (uint32_t(j >> 1) & 1u) ^ 1u;
-                // The five K-ring blocks, in score order.
-                if (!wait_phase(b_kempty + 8 * sl, ph, bars, p.status, kSiteKEmpty)) break;
-                ptx::mbar_arrive_expect_tx(b_kfull + 8 * sl, kKBytes);
-                const uint32_t kdst = sbase + uint32_t(kOffK + sl * kKBytes);
-                for (int pos = 0; pos < kKPerPage; ++pos)
-                    ptx::tma_load_2d(kdst + uint32_t(pos * kBlockBytes), &tmap,
-                                     64 * k_block(int(rank), pos), y, b_kfull + 8 * sl);
-                k_issued = j + 1;
-                // This CTA's four value blocks.
-                if (!wait_phase(b_vempty + 8 * sl, ph, bars, p.status, kSiteVEmpty)) break;
-                ptx::mbar_arrive_expect_tx(b_vfull + 8 * sl, kVBytes);
-                const uint32_t vdst = sbase + uint32_t(kOffV + sl * kVBytes);
-                for (int k = 0; k < 4; ++k)
-                    ptx::tma_load_2d(vdst + uint32_t(k * kBlockBytes), &tmap, 256 * int(rank) + 64 * k,
-                                     y, b_vfull + 8 * sl);
-                v_issued = j + 1;
+                if (!wait_phase(b_empty + 8 * sl, (uint32_t(j >> 1) & 1u) ^ 1u, bars, p.status,
+                                k_ring ? kSiteKEmpty : kSiteVEmpty))
+                    break;
+                ptx::mbar_arrive_expect_tx(b_full + 8 * sl, uint32_t(bytes));
+                const uint32_t dst = dst0 + uint32_t(sl * bytes);
+                if (k_ring) {
+                    // The five K-ring blocks, in score order.
+                    for (int pos = 0; pos < kKPerPage; ++pos)
+                        ptx::tma_load_2d(dst + uint32_t(pos * kBlockBytes), &tmap,
+                                         64 * k_block(int(rank), pos), y, b_full + 8 * sl);
+                } else {
+                    // This CTA's four value blocks.
+                    for (int k = 0; k < 4; ++k)
+                        ptx::tma_load_2d(dst + uint32_t(k * kBlockBytes), &tmap,
+                                         256 * int(rank) + 64 * k, y, b_full + 8 * sl);
+                }
+                issued = j + 1;
             }
             // Every issued load lands before the CTA may exit.
-            for (int j = k_issued > 2 ? k_issued - 2 : 0; j < k_issued; ++j)
-                wait_phase(b_kfull + 8 * (j & 1), uint32_t(j >> 1) & 1u, bars, p.status, kSiteDrain,
-                           true);
-            for (int j = v_issued > 2 ? v_issued - 2 : 0; j < v_issued; ++j)
-                wait_phase(b_vfull + 8 * (j & 1), uint32_t(j >> 1) & 1u, bars, p.status, kSiteDrain,
+            for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+                wait_phase(b_full + 8 * (j & 1), uint32_t(j >> 1) & 1u, bars, p.status, kSiteDrain,
                            true);
         }
     } else if (warp == 1) {
@@ -416,10 +427,6 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             score_warp<0>(margs, bq);
         else
             score_warp<1>(margs, bq);
-    } else if (warp == 6) {
-        // ------------------------------------------------------ P.V MMAs
-        const uint32_t bp[4] = {b_pfull, b_pfree, b_vempty, b_final_pv};
-        pv_warp(margs, bp);
     } else {
         // ------------------------------------------- softmax / correction / epilogue
         const int quarter = warp & 3;
@@ -428,42 +435,40 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
         const bool live_head = h < N;
         const uint16_t* qrow = p.q + (size_t(b) * N + h) * kD;
 
-        // q dims 0..255 -> TMEM (A operand), dims 256..575 -> shared memory.
+        // q dims 0..255 -> TMEM (A operand), two 64-dim blocks per round of
+        // loads; the shared-memory part was started before the setup sync.
         {
 #pragma unroll 1
-            for (int c = 0; c < kQTmemBlocks; ++c) {
-                uint32_t r[32];
+            for (int c2 = 0; c2 < kQTmemBlocks; c2 += 2) {
+                uint32_t r0[32], r1[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = 0u;
+                for (int i = 0; i < 32; ++i) r0[i] = r1[i] = 0u;
                 if (live_head) {
-                    const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * c);
+                    const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * c2);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const uint4 v = __ldg(src + i);
-                        r[4 * i + 0] = v.x;
-                        r[4 * i + 1] = v.y;
-                        r[4 * i + 2] = v.z;
-                        r[4 * i + 3] = v.w;
+                        const uint4 w = __ldg(src + 8 + i);
+                        r0[4 * i + 0] = v.x;
+                        r0[4 * i + 1] = v.y;
+                        r0[4 * i + 2] = v.z;
+                        r0[4 * i + 3] = v.w;
+                        r1[4 * i + 0] = w.x;
+                        r1[4 * i + 1] = w.y;
+                        r1[4 * i + 2] = w.z;
+                        r1[4 * i + 3] = w.w;
                     }
                 }
-                ptx::tmem_st32(trow + kTmemQ + uint32_t(c * 32), r);
+                ptx::tmem_st32(trow + kTmemQ + uint32_t(c2 * 32), r0);
+                ptx::tmem_st32(trow + kTmemQ + uint32_t(c2 * 32 + 32), r1);
             }
-#pragma unroll 1
-            for (int kb = 0; kb < 5; ++kb) {
-                unsigned char* row = smem + kOffQS + kb * 16384 + h * 128;
-                const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * (kQTmemBlocks + kb));
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (live_head) v = __ldg(src + c);
-                    *reinterpret_cast<uint4*>(row + ((c ^ (h & 7)) * 16)) = v;
-                }
-            }
+            ptx::cp_async_wait_all();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ptx::mbar_arrive(b_qready);
         }
 
+        bool issued_pv = false;
         float m_ref = -INFINITY;   // log2 units
         float l_sum = 0.f;         // sum of fp32 weights (for the LSE)
         float l_bf = 0.f;          // sum of the bf16 weights the MMA used (for O)
@@ -473,22 +478,29 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             ok = wait_phase(b_sfull + 8 * sl, uint32_t(j >> 1) & 1u, bars, p.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             ptx::tc_fence_after();
-            // The page's scores are read from TMEM twice, 32 tokens at a time
-            // (max, then weights): rolled passes keep this loop's code small
-            // enough to stay in the instruction cache beside the MMA warps'.
+            // The page's 64 scores of this head, scaled to log2 units.
             const uint32_t sbuf = trow + kTmemS + uint32_t(sl * 64);
             const int valid = min(kTile, t_hi - (t_lo + j * kTile));
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t r[32];
-                ptx::tmem_ld32(sbuf + uint32_t(hh * 32), r);
-                const int lim = valid - 32 * hh;
+            const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
+            float x[64];
+            {
+                uint32_t r[64];
+                ptx::tmem_ld64(sbuf, r);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    m4[i & 3] = fmaxf(m4[i & 3],
-                                      i < lim ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY);
+                for (int i = 0; i < 32; ++i) {
+                    const float2 v = __fmul2_rn(
+                        make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), scale2);
+                    x[2 * i] = v.x;
+                    x[2 * i + 1] = v.y;
+                }
             }
+            if (valid < kTile) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) x[i] = i < valid ? x[i] : -INFINITY;
+            }
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
             const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             const float m_new = fmaxf(m_ref, mx);
             const bool rescale = m_new > m_ref + kRescaleThreshold;
@@ -499,29 +511,29 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             }
 
             // Weights: P row of this head, 64 tokens as bf16 pairs, written
-            // over the first 32 columns of the score buffer (half hh's
-            // weights land on columns already read). Masked tokens get 0.
-            float r4[4] = {0.f, 0.f, 0.f, 0.f}, b4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t r[32];
-                ptx::tmem_ld32(sbuf + uint32_t(hh * 32), r);
-                const int lim = valid - 32 * hh;
-                uint32_t pk[16];
+            // over the first 32 columns of the score buffer (all read above).
+            // Masked tokens (x = -inf) get 0.
+            float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 lb2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            {
+                const float2 negm2 = make_float2(-m_ref, -m_ref);
+                uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float x0 = __uint_as_float(r[2 * i]) * p.scale_log2 - m_ref;
-                    const float x1 = __uint_as_float(r[2 * i + 1]) * p.scale_log2 - m_ref;
-                    const float a = 2 * i < lim ? ptx::ex2(x0) : 0.f;
-                    const float c = 2 * i + 1 < lim ? ptx::ex2(x1) : 0.f;
-                    r4[i & 3] += a + c;
+                for (int i = 0; i < 32; ++i) {
+                    const float2 d = __fadd2_rn(make_float2(x[2 * i], x[2 * i + 1]), negm2);
+                    const float a = ptx::ex2(d.x);
+                    const float c = ptx::ex2(d.y);
                     pk[i] = pack_bf16x2(a, c);
-                    b4[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                    ls2[i & 1] = __fadd2_rn(ls2[i & 1], make_float2(a, c));
+                    lb2[i & 1] = __fadd2_rn(lb2[i & 1], make_float2(__uint_as_float(pk[i] << 16),
+                                                                    __uint_as_float(pk[i] & 0xffff0000u)));
                 }
-                ptx::tmem_st16(sbuf + uint32_t(hh * 16), pk);
+                ptx::tmem_st32(sbuf, pk);
             }
-            l_sum = l_sum * alpha + ((r4[0] + r4[1]) + (r4[2] + r4[3]));
-            l_bf = l_bf * alpha + ((b4[0] + b4[1]) + (b4[2] + b4[3]));
+            const float2 ls = __fadd2_rn(ls2[0], ls2[1]);
+            const float2 lb = __fadd2_rn(lb2[0], lb2[1]);
+            l_sum = l_sum * alpha + (ls.x + ls.y);
+            l_bf = l_bf * alpha + (lb.x + lb.y);
 
             // O rescale once the P.V of page j-1 is done.
             if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -553,9 +565,21 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 }
                 ptx::fence_proxy_async_smem();
             }
+            // The fourth softmax warp to finish page j issues its P.V MMAs.
             ptx::tc_fence_before();
-            ptx::mbar_arrive(b_pfull + 8 * sl);
+            __syncwarp();
+            uint32_t done_before = 0;
+            if (lane == 0) done_before = ptx::atom_add_acq_rel_shared(a_pcount + 4 * sl, 1u);
+            done_before = __shfl_sync(0xffffffffu, done_before, 0);
+            if (done_before == 4u * uint32_t(j >> 1) + 3u) {
+                ptx::tc_fence_after();
+                if (ptx::elect_one()) issue_pv(tmem, sbase, j, b_vempty, b_pfree);
+                __syncwarp();
+                issued_pv = true;
+            }
         }
+        // Every P.V MMA this warp issued completes before TMEM is freed.
+        if (issued_pv) warp_drain(b_final_sm + 8 * quarter, margs);
 
         // Epilogue: O / l -> bf16 output, or the fp32 split partial.
         if (ok && ntiles > 0) {
