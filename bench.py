@@ -357,7 +357,7 @@ def run_ours(args, w, rank, world):
     achieved_tflops = flops / t_s / 1e12
     t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
     traffic, profile = recorded_traffic(plan.kernel, w.name)
-    launches_per_step = 1 + (1 if plan.num_kv_splits > 1 else 0)
+    launches_per_step = 1 + (1 if plan.num_kv_splits > 1 or plan.sched_pairs > 0 else 0)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -369,6 +369,8 @@ def run_ours(args, w, rank, world):
             "cached_tokens": w.total_tokens, "page_size": w.page_size,
             "kv_lora_rank": 512, "rope_dim": 64, "softmax_scale": w.softmax_scale,
             "num_kv_splits": plan.num_kv_splits,
+            "schedule": (f"page-balanced over {plan.sched_pairs} CTA pairs + merge"
+                         if plan.sched_pairs > 0 else f"split S={plan.num_kv_splits}"),
             "kernel": {1: "simt", 2: "tcgen05"}[plan.kernel],
             "l2": "inputs larger than L2 (%.2f GB cache), no flush" % (cache.numel() * 2 / 1e9),
             "parallelism": f"requests replicated per rank x{world} (weak)" if world > 1 else "1 GPU",

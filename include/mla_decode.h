@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MLA_DECODE_ABI_VERSION 1
+#define MLA_DECODE_ABI_VERSION 2
 
 /* Status codes. */
 #define MLA_OK                 0
@@ -68,17 +68,34 @@ extern "C" {
 
 /* Plan flags (mla_decode_plan_t.flags, and the `flags` argument). */
 #define MLA_PLAN_FORCE_SIMT  0x1u  /* use MLA_KERNEL_SIMT even where MLA_KERNEL_TC applies */
+#define MLA_PLAN_SPLIT_ONLY  0x2u  /* never choose the page-balanced schedule */
+#define MLA_PLAN_FORCE_BALANCED 0x4u  /* with num_kv_splits = 0: the page-balanced schedule
+                                         wherever it applies, whatever the estimate */
 
 /*
- * A decode plan: the sizes, the split count S and the kernel variant. It is
- * plain data computed on the host; mla_decode reads it and never changes it.
+ * A decode plan: the sizes, the schedule and the kernel variant. It is plain
+ * data computed on the host; mla_decode reads it, never changes it, and
+ * rejects (MLA_ERR_INVALID_ARG) a plan whose launch shape or workspace layout
+ * does not follow from its sizes.
  *
- * Split-KV (ModelOpt mla_attention_decode, num_kv_splits: a fixed split count
- * along the token axis). Split s of request b covers tokens
- * [s*C_b, min((s+1)*C_b, L_b)) with C_b = page_size * ceil(ceil(L_b/page_size)/S);
- * empty splits contribute nothing. With S = 1 the decode kernel writes `out`
- * and `lse` itself; with S > 1 it writes fp32 partials into the workspace and
+ * Split schedule (sched_pairs == 0; ModelOpt mla_attention_decode,
+ * num_kv_splits: a fixed split count along the token axis). Split s of
+ * request b covers tokens [s*C_b, min((s+1)*C_b, L_b)) with
+ * C_b = page_size * ceil(ceil(L_b/page_size)/S); empty splits contribute
+ * nothing. With S = 1 the decode kernel writes `out` and `lse` itself; with
+ * S > 1 it writes fp32 partials [B,N,S,Lkv] / [B,N,S] into the workspace and
  * mla_merge_splits combines them.
+ *
+ * Page-balanced schedule (sched_pairs = C > 0, MLA_KERNEL_TC, B <= 512,
+ * num_kv_splits = 1). This is a work-partitioning choice of this library; the
+ * papers' split-KV has no counterpart of it. The pages of the batch, request
+ * after request, are cut into C contiguous ranges of near-equal length (range
+ * c = pages [floor(c*P/C), floor((c+1)*P/C)) of the P pages, taken from the
+ * device seq_lens at run time), one per CTA pair. A request inside one range
+ * is written directly; one that crosses range boundaries leaves fp32 partial
+ * rows ([2C,N,Lkv] / [2C,N] in the workspace: slot 2c for the first request
+ * of range c, slot 2c+1 for its last) that a second kernel combines with the
+ * LSE-weighted merge. Results agree with the split schedule up to rounding.
  */
 typedef struct mla_decode_plan {
     int32_t  batch;               /* B */
@@ -96,7 +113,8 @@ typedef struct mla_decode_plan {
     uint64_t workspace_bytes;     /* bytes of `workspace` mla_decode needs */
     uint64_t partial_offset;      /* byte offset of o_part [B,N,S,Lkv] fp32 */
     uint64_t lse_partial_offset;  /* byte offset of lse_part [B,N,S] fp32 */
-    uint32_t reserved[8];
+    int32_t  sched_pairs;         /* 0: split schedule; C > 0: page-balanced schedule */
+    uint32_t reserved[7];
 } mla_decode_plan_t;
 
 /*
@@ -110,7 +128,10 @@ typedef struct mla_decode_plan {
  *   seq_lens_host              optional host copy of seq_lens [B] (NULL allowed);
  *                              when given, the planner sizes S from the real lengths.
  *   num_kv_splits              S > 0 is used as given (fixed, batch-invariant);
- *                              0 lets the planner choose from the SM count.
+ *                              0 lets the planner choose S, or the page-balanced
+ *                              schedule over num_sms/2 CTA pairs (MLA_KERNEL_TC,
+ *                              B <= 512, unless MLA_PLAN_SPLIT_ONLY), from its
+ *                              cost estimate.
  *   num_sms                    SMs of the target device (152 on GB300), >= 1.
  *   flags                      MLA_PLAN_* bits.
  *   plan                       out: filled on MLA_OK.

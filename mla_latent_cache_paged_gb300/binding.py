@@ -26,6 +26,8 @@ MLA_ERR_SCRATCH_LIMIT = -8
 MLA_KERNEL_SIMT = 1
 MLA_KERNEL_TC = 2
 MLA_PLAN_FORCE_SIMT = 0x1
+MLA_PLAN_SPLIT_ONLY = 0x2
+MLA_PLAN_FORCE_BALANCED = 0x4
 
 KV_LORA_RANK = 512
 ROPE_DIM = 64
@@ -63,7 +65,8 @@ class MlaDecodePlan(ctypes.Structure):
         ("workspace_bytes", ctypes.c_uint64),
         ("partial_offset", ctypes.c_uint64),
         ("lse_partial_offset", ctypes.c_uint64),
-        ("reserved", ctypes.c_uint32 * 8),
+        ("sched_pairs", ctypes.c_int32),
+        ("reserved", ctypes.c_uint32 * 7),
     ]
 
     def as_dict(self):
@@ -129,8 +132,15 @@ def _stream_ptr(stream):
 
 
 def make_plan(batch, num_heads, max_blocks_per_seq, max_seq_len=None, *, seq_lens_host=None,
-              num_kv_splits=0, num_sms=None, force_simt=False):
-    """Call mla_decode_plan (host only; no device work)."""
+              num_kv_splits=0, num_sms=None, force_simt=False, schedule="auto"):
+    """Call mla_decode_plan (host only; no device work).
+
+    ``schedule``: "auto" (the planner's estimate), "split" (never the
+    page-balanced schedule) or "balanced" (the page-balanced schedule wherever
+    it applies; needs num_kv_splits = 0).
+    """
+    if schedule not in ("auto", "split", "balanced"):
+        raise ValueError(f"schedule must be auto, split or balanced, not {schedule!r}")
     lib = load_library()
     if max_seq_len is None:
         max_seq_len = max_blocks_per_seq * PAGE_SIZE
@@ -148,7 +158,10 @@ def make_plan(batch, num_heads, max_blocks_per_seq, max_seq_len=None, *, seq_len
     rc = lib.mla_decode_plan(int(batch), int(num_heads), KV_LORA_RANK, ROPE_DIM, PAGE_SIZE,
                              int(max_blocks_per_seq), int(max_seq_len), lens_ptr,
                              int(num_kv_splits), int(num_sms),
-                             MLA_PLAN_FORCE_SIMT if force_simt else 0, ctypes.byref(plan))
+                             (MLA_PLAN_FORCE_SIMT if force_simt else 0) |
+                             (MLA_PLAN_SPLIT_ONLY if schedule == "split" else 0) |
+                             (MLA_PLAN_FORCE_BALANCED if schedule == "balanced" else 0),
+                             ctypes.byref(plan))
     del keep
     _check(rc, "mla_decode_plan")
     return plan

@@ -57,7 +57,8 @@ extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const vo
     p.out = static_cast<uint16_t*>(out);
     p.lse = lse;
     p.status = reinterpret_cast<int32_t*>(ws);
-    if (S > 1) {
+    p.sched_pairs = plan->sched_pairs;
+    if (S > 1 || plan->sched_pairs > 0) {
         p.o_part = reinterpret_cast<float*>(ws + plan->partial_offset);
         p.lse_part = reinterpret_cast<float*>(ws + plan->lse_partial_offset);
     }
@@ -65,7 +66,9 @@ extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const vo
     int e = plan->kernel == MLA_KERNEL_TC ? launch_decode_tc(p, plan->grid_ctas, stream)
                                           : launch_decode_simt(p, stream);
     if (e != 0) return MLA_ERR_CUDA;
-    if (S > 1) {
+    if (plan->sched_pairs > 0) {
+        if (launch_merge_balanced(p, stream) != 0) return MLA_ERR_CUDA;
+    } else if (S > 1) {
         e = launch_merge(p.o_part, p.lse_part, plan->batch * plan->num_heads, S, kLkv, p.out,
                          lse, stream);
         if (e != 0) return MLA_ERR_CUDA;

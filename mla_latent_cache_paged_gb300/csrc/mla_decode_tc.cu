@@ -65,7 +65,8 @@ constexpr int kOffQS = 0;                      // q dims 256..575: 5 x [128 x 64
 constexpr int kOffV = 5 * 16384;               // V ring: 2 pages
 constexpr int kOffK = kOffV + 2 * kVBytes;     // K ring: 2 pages
 constexpr int kOffBar = kOffK + 2 * kKBytes;   // 229,376
-constexpr int kSmemBytes = kOffBar + 256;      // dynamic smem base is 1 KB aligned
+constexpr int kOffPfx = kOffBar + 256;         // page offsets of the balanced schedule
+constexpr int kSmemBytes = kOffPfx + (kMaxBalancedBatch + 4) * 4;   // base is 1 KB aligned
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemQ = 0;     // 128 columns: q dims 0..255 as bf16 pairs (A operand)
@@ -148,6 +149,79 @@ __host__ __device__ constexpr int k_block(int rank, int pos) {
     return rank == 0 ? pos + 4 : (pos < 4 ? pos : 8);
 }
 
+// ------------------------------------------------------------ work segments
+// A CTA pair works through one or more segments: tokens [t_lo, t_hi) of a
+// request. The split schedule gives pair `pair` = (b, split) one segment; the
+// page-balanced schedule gives it the requests its page range touches (the
+// page offsets pfx[b] = pages of requests 0..b-1 are in shared memory).
+struct Segment {
+    int b;
+    int t_lo, t_hi;
+    int prow0;         // partial row of head 0, or -1: write out / lse directly
+    int prow_stride;   // partial rows from one head to the next
+};
+
+struct SegmentWalk {
+    int next_b;        // balanced: next request to look at; split: 1 once done
+    int64_t g0, g1;    // balanced: the pair's page range
+};
+
+__device__ __forceinline__ SegmentWalk walk_begin(const DecodeParams& p, const int32_t* pfx,
+                                                  int pair) {
+    SegmentWalk w{0, 0, 0};
+    if (p.sched_pairs > 0) {
+        const int64_t total = pfx[p.batch];
+        if (total > 0) {
+            w.g0 = pair_begin(pair, p.sched_pairs, total);
+            w.g1 = pair_begin(pair + 1, p.sched_pairs, total);
+        }
+        // The first request whose pages reach past g0.
+        int lo = 0, hi = p.batch;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (pfx[mid + 1] > w.g0)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        w.next_b = lo;
+    }
+    return w;
+}
+
+__device__ __forceinline__ bool walk_next(const DecodeParams& p, const int32_t* pfx, int pair,
+                                          SegmentWalk& w, Segment& s) {
+    if (p.sched_pairs == 0) {
+        if (w.next_b != 0) return false;
+        w.next_b = 1;
+        const int S = p.num_splits;
+        const int split = pair % S;
+        s.b = pair / S;
+        split_range(checked_seq_len(p, s.b), S, split, &s.t_lo, &s.t_hi);
+        s.prow0 = S == 1 ? -1 : s.b * p.num_heads * S + split;
+        s.prow_stride = S;
+        return true;
+    }
+    while (w.next_b < p.batch && pfx[w.next_b] < w.g1) {
+        const int b = w.next_b++;
+        const int64_t pb = pfx[b], pe = pfx[b + 1];
+        if (pe == pb) continue;   // no pages: the merge writes this request
+        const int64_t lo = pb > w.g0 ? pb : w.g0;
+        const int64_t hi = pe < w.g1 ? pe : w.g1;
+        s.b = b;
+        s.t_lo = int(lo - pb) * kPageSize;
+        s.t_hi = min(p.seq_lens[b], int(hi - pb) * kPageSize);
+        s.prow0 = (lo == pb && hi == pe) ? -1 : (lo == w.g0 ? 2 * pair : 2 * pair + 1) * p.num_heads;
+        s.prow_stride = 1;
+        return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ int seg_pages(const Segment& s) {
+    return (s.t_hi - s.t_lo + kTile - 1) / kTile;
+}
+
 // ------------------------------------------------------------ MMA issue
 // The score warp blocks on its barriers in a suspended wait (not a spin that
 // would take issue slots from the softmax warps), runs its loop in lockstep
@@ -159,7 +233,6 @@ struct MmaWarpArgs {
     uint32_t tmem, sbase;
     TcBars* bars;
     int32_t* status;
-    int ntiles;
 };
 
 // Slow path of warp_wait, out of line. Called by the whole warp; returns
@@ -229,42 +302,62 @@ __device__ __forceinline__ void score_block(uint32_t d, uint32_t tmem, uint32_t 
 // blocks. CTA 0's K-ring blocks are dims 256..575 (q from shared memory) and
 // its value blocks dims 0..255 (q from TMEM); CTA 1's K-ring blocks are dims
 // 0..255 (TMEM) and 512..575 (shared memory), its value blocks dims 256..511
-// (shared memory).
+// (shared memory). Pages are numbered across segments (jg) for the rings;
+// each segment waits for its own q.
 template <int RANK>
-__device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t* b) {
+__device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t* b,
+                                           const DecodeParams& p, const int32_t* pfx, int pair) {
     const uint32_t b_kfull = b[0], b_kempty = b[1], b_vfull = b[2], b_sfull = b[3],
                    b_pfree = b[4], b_qready = b[5], b_final = b[6];
     const uint32_t tmem = a.tmem;
     const uint32_t qs = a.sbase + uint32_t(kOffQS);
-    bool ok = warp_wait(b_qready, 0, a, kSiteQReady);
-    for (int nq = 0; ok && nq < a.ntiles; ++nq) {
-        const int sl = nq & 1;
-        const uint32_t ph = uint32_t(nq >> 1) & 1u;
-        // The score buffer is free once the P.V MMA of page nq-2 has read P.
-        if (nq >= 2 && !warp_wait(b_pfree + 8 * sl, ph ^ 1u, a, kSiteSFree)) break;
-        if (!warp_wait(b_kfull + 8 * sl, ph, a, kSiteKFull)) break;
-        ptx::tc_fence_after();
-        const uint32_t d = tmem + kTmemS + uint32_t(sl * 64);
-        const uint32_t kslot = a.sbase + uint32_t(kOffK + sl * kKBytes);
-        const uint32_t vslot = a.sbase + uint32_t(kOffV + sl * kVBytes);
-        if (ptx::elect_one()) {
-            score_block<k_block(RANK, 0)>(d, tmem, qs, kslot + 0 * kBlockBytes, true);
-            score_block<k_block(RANK, 1)>(d, tmem, qs, kslot + 1 * kBlockBytes, false);
-            score_block<k_block(RANK, 2)>(d, tmem, qs, kslot + 2 * kBlockBytes, false);
-            score_block<k_block(RANK, 3)>(d, tmem, qs, kslot + 3 * kBlockBytes, false);
-            score_block<k_block(RANK, 4)>(d, tmem, qs, kslot + 4 * kBlockBytes, false);
-            ptx::mma_commit(b_kempty + 8 * sl);
+    SegmentWalk walk = walk_begin(p, pfx, pair);
+    Segment sg;
+    int jg = 0;
+    int nseg = 0;   // segments with pages so far (one q_ready phase each)
+    bool ok = true;
+    while (ok && walk_next(p, pfx, pair, walk, sg)) {
+        const int ntiles = seg_pages(sg);
+        if (ntiles == 0) continue;
+        ok = warp_wait(b_qready, uint32_t(nseg++) & 1u, a, kSiteQReady);
+        for (int j = 0; ok && j < ntiles; ++j, ++jg) {
+            const int sl = jg & 1;
+            const uint32_t ph = uint32_t(jg >> 1) & 1u;
+            // The score buffer is free once the P.V MMA of page jg-2 has read P.
+            if (jg >= 2 && !warp_wait(b_pfree + 8 * sl, ph ^ 1u, a, kSiteSFree)) {
+                ok = false;
+                break;
+            }
+            if (!warp_wait(b_kfull + 8 * sl, ph, a, kSiteKFull)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t d = tmem + kTmemS + uint32_t(sl * 64);
+            const uint32_t kslot = a.sbase + uint32_t(kOffK + sl * kKBytes);
+            const uint32_t vslot = a.sbase + uint32_t(kOffV + sl * kVBytes);
+            if (ptx::elect_one()) {
+                score_block<k_block(RANK, 0)>(d, tmem, qs, kslot + 0 * kBlockBytes, true);
+                score_block<k_block(RANK, 1)>(d, tmem, qs, kslot + 1 * kBlockBytes, false);
+                score_block<k_block(RANK, 2)>(d, tmem, qs, kslot + 2 * kBlockBytes, false);
+                score_block<k_block(RANK, 3)>(d, tmem, qs, kslot + 3 * kBlockBytes, false);
+                score_block<k_block(RANK, 4)>(d, tmem, qs, kslot + 4 * kBlockBytes, false);
+                ptx::mma_commit(b_kempty + 8 * sl);
+            }
+            __syncwarp();
+            if (!warp_wait(b_vfull + 8 * sl, ph, a, kSiteVFull)) {
+                ok = false;
+                break;
+            }
+            if (ptx::elect_one()) {
+                score_block<4 * RANK + 0>(d, tmem, qs, vslot + 0 * kBlockBytes, false);
+                score_block<4 * RANK + 1>(d, tmem, qs, vslot + 1 * kBlockBytes, false);
+                score_block<4 * RANK + 2>(d, tmem, qs, vslot + 2 * kBlockBytes, false);
+                score_block<4 * RANK + 3>(d, tmem, qs, vslot + 3 * kBlockBytes, false);
+                ptx::mma_commit(b_sfull + 8 * sl);
+            }
+            __syncwarp();
         }
-        __syncwarp();
-        if (!warp_wait(b_vfull + 8 * sl, ph, a, kSiteVFull)) break;
-        if (ptx::elect_one()) {
-            score_block<4 * RANK + 0>(d, tmem, qs, vslot + 0 * kBlockBytes, false);
-            score_block<4 * RANK + 1>(d, tmem, qs, vslot + 1 * kBlockBytes, false);
-            score_block<4 * RANK + 2>(d, tmem, qs, vslot + 2 * kBlockBytes, false);
-            score_block<4 * RANK + 3>(d, tmem, qs, vslot + 3 * kBlockBytes, false);
-            ptx::mma_commit(b_sfull + 8 * sl);
-        }
-        __syncwarp();
     }
     warp_drain(b_final, a);
 }
@@ -272,8 +365,8 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
 // O += P V for page np: P the A operand in TMEM, V (MN-major) from the V
 // ring. Issued by one elected lane of the softmax warp that finished the page
 // last; the commits release the V slot and the score buffer.
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int np, uint32_t b_vempty,
-                                         uint32_t b_pfree) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int np, bool accumulate,
+                                         uint32_t b_vempty, uint32_t b_pfree) {
     constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(256, true);
     const int sl = np & 1;
     const uint32_t pcol = tmem + kTmemS + uint32_t(sl * 64);
@@ -281,7 +374,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int np, 
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
         ptx::mma_ts(tmem + kTmemO, pcol + uint32_t(kk * 8), desc_vmn(vb + uint32_t(kk * 2048)),
-                    idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+                    idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
     ptx::mma_commit(b_vempty + 8 * sl);
     ptx::mma_commit(b_pfree + 8 * sl);
 }
@@ -290,25 +383,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap) {
     extern __shared__ __align__(1024) unsigned char smem[];
     TcBars* bars = reinterpret_cast<TcBars*>(smem + kOffBar);
+    int32_t* pfx = reinterpret_cast<int32_t*>(smem + kOffPfx);
     const uint32_t sbase = ptx::smem_addr(smem);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const uint32_t rank = ptx::cluster_ctarank();
-    const int S = p.num_splits;
     const int N = p.num_heads;
-    const int item = blockIdx.x >> 1;
-    const int b = item / S;
-    const int split = item % S;
+    const int pair = blockIdx.x >> 1;
 
     // Swizzled TMA boxes and UMMA descriptors assume a 1 KB aligned base.
     const bool aligned_ok = (sbase & 1023u) == 0u;
-    const int L = checked_seq_len(p, b);
-    int t_lo, t_hi;
-    split_range(L, S, split, &t_lo, &t_hi);
-    const int ntiles = aligned_ok ? (t_hi - t_lo + kTile - 1) / kTile : 0;
-    const int page0 = t_lo / kTile;
 
     const uint32_t b_vfull = ptx::smem_addr(&bars->vfull[0]);
     const uint32_t b_vempty = ptx::smem_addr(&bars->vempty[0]);
@@ -321,102 +407,126 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
     const uint32_t b_final_sm = ptx::smem_addr(&bars->final_sm[0]);
     const uint32_t a_pcount = ptx::smem_addr(&bars->p_count[0]);
 
-    if (tid == 0) {
-        if (!aligned_ok) record_error(p.status, MLA_ERR_UNSUPPORTED, int32_t(sbase));
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(b_vfull + 8 * i, 1);
-            ptx::mbar_init(b_vempty + 8 * i, 1);
-            ptx::mbar_init(b_kfull + 8 * i, 1);
-            ptx::mbar_init(b_kempty + 8 * i, 1);
-            ptx::mbar_init(b_sfull + 8 * i, 1);
-            bars->p_count[i] = 0;
-            ptx::mbar_init(b_pfree + 8 * i, 1);
+    if (warp == 0) {
+        if (lane == 0) {
+            if (!aligned_ok) record_error(p.status, MLA_ERR_UNSUPPORTED, int32_t(sbase));
+            for (int i = 0; i < 2; ++i) {
+                ptx::mbar_init(b_vfull + 8 * i, 1);
+                ptx::mbar_init(b_vempty + 8 * i, 1);
+                ptx::mbar_init(b_kfull + 8 * i, 1);
+                ptx::mbar_init(b_kempty + 8 * i, 1);
+                ptx::mbar_init(b_sfull + 8 * i, 1);
+                ptx::mbar_init(b_pfree + 8 * i, 1);
+                bars->p_count[i] = 0;
+            }
+            ptx::mbar_init(b_qready, 128);
+            ptx::mbar_init(b_final_qk, 1);
+            for (int i = 0; i < 4; ++i) ptx::mbar_init(b_final_sm + 8 * i, 1);
+            bars->abort = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
-        ptx::mbar_init(b_qready, 128);
-        ptx::mbar_init(b_final_qk, 1);
-        for (int i = 0; i < 4; ++i) ptx::mbar_init(b_final_sm + 8 * i, 1);
-        bars->abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (p.sched_pairs > 0) {
+            // Page offsets of the balanced schedule: pfx[b] = pages of
+            // requests 0..b-1 (a request with an invalid length has none).
+            int carry = 0;
+            for (int base = 0; base < p.batch; base += 128) {
+                int pg[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = base + 32 * k + lane;
+                    pg[k] = i < p.batch ? pages_of(checked_seq_len(p, i)) : 0;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    int v = pg[k];
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int n = __shfl_up_sync(0xffffffffu, v, o);
+                        if (lane >= o) v += n;
+                    }
+                    const int i = base + 32 * k + lane;
+                    if (i < p.batch) pfx[i + 1] = carry + v;
+                    carry += __shfl_sync(0xffffffffu, v, 31);
+                }
+            }
+            if (lane == 0) pfx[0] = 0;
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kTmemCols);
         ptx::tmem_relinquish();
     }
-    if (warp >= 2 && warp <= 5) {
-        // q dims 256..575 of head h -> shared memory (the A operand of the
-        // score MMAs for those dims), copied asynchronously right away; the
-        // rows of padded heads are zero-filled.
-        const int h = (warp & 3) * 32 + lane;
-        const bool live = h < N;
-        const uint16_t* qsrc = live ? p.q + (size_t(b) * N + h) * kD : p.q;
-#pragma unroll
-        for (int kb = 0; kb < 5; ++kb)
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                ptx::cp_async16(sbase + uint32_t(kOffQS + kb * 16384 + h * 128 + ((c ^ (h & 7)) * 16)),
-                                qsrc + 64 * (kQTmemBlocks + kb) + 8 * c, live ? 16u : 0u);
-    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const MmaWarpArgs margs{tmem, sbase, bars, p.status, ntiles};
+    const MmaWarpArgs margs{tmem, sbase, bars, p.status};
 
-    if (warp == 0 || warp == 6) {
+    if (!aligned_ok) {
+        // nothing runs; the error is recorded
+    } else if (warp == 0 || warp == 6) {
         // ------------------------------------------------------ TMA producers
         if (lane == 0) {
             const bool k_ring = warp == 0;
-            const int32_t* table = p.block_table + size_t(b) * p.max_blocks;
-            // The K producer of each CTA pulls its half of page
-            // j + kPrefetchAhead into L2, so that the ring loads of both CTAs
-            // hit L2.
-            auto prefetch = [&](int j) {
-                if (!k_ring || j >= ntiles) return;
-                const int32_t blk = table[page0 + j];
-                if (blk < 0 || int64_t(blk) >= p.num_blocks) return;
-                const unsigned char* page =
-                    reinterpret_cast<const unsigned char*>(p.cache) + size_t(blk) * kPageBytes;
-                ptx::prefetch_l2(page + rank * (kPageBytes / 2), kPageBytes / 2);
-            };
-            for (int j = 0; j < kPrefetchAhead; ++j) prefetch(j);
             const uint32_t b_full = k_ring ? b_kfull : b_vfull;
             const uint32_t b_empty = k_ring ? b_kempty : b_vempty;
             const int bytes = k_ring ? kKBytes : kVBytes;
             const uint32_t dst0 = sbase + uint32_t(k_ring ? kOffK : kOffV);
-            int next = ntiles > 0 ? table[page0] : 0;
-            int issued = 0;
-            for (int j = 0; j < ntiles; ++j) {
-                const int blk = next;
-                if (j + 1 < ntiles) next = table[page0 + j + 1];
-                prefetch(j + kPrefetchAhead);
-                int32_t y;
-                if (blk >= 0 && int64_t(blk) < p.num_blocks) {
-                    y = blk * kTile;
-                } else {
-                    if (k_ring) record_error(p.status, MLA_ERR_BAD_BLOCK_ID, blk);
-                    y = -kTile;   // wholly outside the tensor: TMA writes zeros
+            SegmentWalk walk = walk_begin(p, pfx, pair);
+            Segment sg;
+            int jg = 0;   // pages issued so far, across segments
+            bool ok = true;
+            while (ok && walk_next(p, pfx, pair, walk, sg)) {
+                const int ntiles = seg_pages(sg);
+                const int page0 = sg.t_lo / kTile;
+                const int32_t* table = p.block_table + size_t(sg.b) * p.max_blocks;
+                // The K producer of each CTA pulls its half of page
+                // j + kPrefetchAhead into L2, so that the ring loads of both
+                // CTAs hit L2.
+                auto prefetch = [&](int j) {
+                    if (!k_ring || j >= ntiles) return;
+                    const int32_t blk = table[page0 + j];
+                    if (blk < 0 || int64_t(blk) >= p.num_blocks) return;
+                    const unsigned char* page =
+                        reinterpret_cast<const unsigned char*>(p.cache) + size_t(blk) * kPageBytes;
+                    ptx::prefetch_l2(page + rank * (kPageBytes / 2), kPageBytes / 2);
+                };
+                for (int j = 0; j < kPrefetchAhead; ++j) prefetch(j);
+                int next = ntiles > 0 ? table[page0] : 0;
+                for (int j = 0; j < ntiles; ++j, ++jg) {
+                    const int blk = next;
+                    if (j + 1 < ntiles) next = table[page0 + j + 1];
+                    prefetch(j + kPrefetchAhead);
+                    int32_t y;
+                    if (blk >= 0 && int64_t(blk) < p.num_blocks) {
+                        y = blk * kTile;
+                    } else {
+                        if (k_ring) record_error(p.status, MLA_ERR_BAD_BLOCK_ID, blk);
+                        y = -kTile;   // wholly outside the tensor: TMA writes zeros
+                    }
+                    const int sl = jg & 1;
+                    if (!wait_phase(b_empty + 8 * sl, (uint32_t(jg >> 1) & 1u) ^ 1u, bars, p.status,
+                                    k_ring ? kSiteKEmpty : kSiteVEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(b_full + 8 * sl, uint32_t(bytes));
+                    const uint32_t dst = dst0 + uint32_t(sl * bytes);
+                    if (k_ring) {
+                        // The five K-ring blocks, in score order.
+                        for (int pos = 0; pos < kKPerPage; ++pos)
+                            ptx::tma_load_2d(dst + uint32_t(pos * kBlockBytes), &tmap,
+                                             64 * k_block(int(rank), pos), y, b_full + 8 * sl);
+                    } else {
+                        // This CTA's four value blocks.
+                        for (int k = 0; k < 4; ++k)
+                            ptx::tma_load_2d(dst + uint32_t(k * kBlockBytes), &tmap,
+                                             256 * int(rank) + 64 * k, y, b_full + 8 * sl);
+                    }
                 }
-                const int sl = j & 1;
-                if (!wait_phase(b_empty + 8 * sl, (uint32_t(j >> 1) & 1u) ^ 1u, bars, p.status,
-                                k_ring ? kSiteKEmpty : kSiteVEmpty))
-                    break;
-                ptx::mbar_arrive_expect_tx(b_full + 8 * sl, uint32_t(bytes));
-                const uint32_t dst = dst0 + uint32_t(sl * bytes);
-                if (k_ring) {
-                    // The five K-ring blocks, in score order.
-                    for (int pos = 0; pos < kKPerPage; ++pos)
-                        ptx::tma_load_2d(dst + uint32_t(pos * kBlockBytes), &tmap,
-                                         64 * k_block(int(rank), pos), y, b_full + 8 * sl);
-                } else {
-                    // This CTA's four value blocks.
-                    for (int k = 0; k < 4; ++k)
-                        ptx::tma_load_2d(dst + uint32_t(k * kBlockBytes), &tmap,
-                                         256 * int(rank) + 64 * k, y, b_full + 8 * sl);
-                }
-                issued = j + 1;
             }
             // Every issued load lands before the CTA may exit.
-            for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+            for (int j = jg > 2 ? jg - 2 : 0; j < jg; ++j)
                 wait_phase(b_full + 8 * (j & 1), uint32_t(j >> 1) & 1u, bars, p.status, kSiteDrain,
                            true);
         }
@@ -424,175 +534,196 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
         // ------------------------------------------------------ score MMAs
         const uint32_t bq[7] = {b_kfull, b_kempty, b_vfull, b_sfull, b_pfree, b_qready, b_final_qk};
         if (rank == 0)
-            score_warp<0>(margs, bq);
+            score_warp<0>(margs, bq, p, pfx, pair);
         else
-            score_warp<1>(margs, bq);
+            score_warp<1>(margs, bq, p, pfx, pair);
     } else {
-        // ------------------------------------------- softmax / correction / epilogue
+        // ------------------------------- softmax / P.V issue / correction / epilogue
         const int quarter = warp & 3;
         const int h = quarter * 32 + lane;
         const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
         const bool live_head = h < N;
-        const uint16_t* qrow = p.q + (size_t(b) * N + h) * kD;
-
-        // q dims 0..255 -> TMEM (A operand), two 64-dim blocks per round of
-        // loads; the shared-memory part was started before the setup sync.
-        {
-#pragma unroll 1
-            for (int c2 = 0; c2 < kQTmemBlocks; c2 += 2) {
-                uint32_t r0[32], r1[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r0[i] = r1[i] = 0u;
-                if (live_head) {
-                    const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * c2);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint4 v = __ldg(src + i);
-                        const uint4 w = __ldg(src + 8 + i);
-                        r0[4 * i + 0] = v.x;
-                        r0[4 * i + 1] = v.y;
-                        r0[4 * i + 2] = v.z;
-                        r0[4 * i + 3] = v.w;
-                        r1[4 * i + 0] = w.x;
-                        r1[4 * i + 1] = w.y;
-                        r1[4 * i + 2] = w.z;
-                        r1[4 * i + 3] = w.w;
-                    }
-                }
-                ptx::tmem_st32(trow + kTmemQ + uint32_t(c2 * 32), r0);
-                ptx::tmem_st32(trow + kTmemQ + uint32_t(c2 * 32 + 32), r1);
-            }
-            ptx::cp_async_wait_all();
-            ptx::fence_proxy_async_smem();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(b_qready);
-        }
-
         bool issued_pv = false;
-        float m_ref = -INFINITY;   // log2 units
-        float l_sum = 0.f;         // sum of fp32 weights (for the LSE)
-        float l_bf = 0.f;          // sum of the bf16 weights the MMA used (for O)
         bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
-            const int sl = j & 1;
-            ok = wait_phase(b_sfull + 8 * sl, uint32_t(j >> 1) & 1u, bars, p.status, kSiteSFull);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            ptx::tc_fence_after();
-            // The page's 64 scores of this head, scaled to log2 units.
-            const uint32_t sbuf = trow + kTmemS + uint32_t(sl * 64);
-            const int valid = min(kTile, t_hi - (t_lo + j * kTile));
-            const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
-            float x[64];
-            {
-                uint32_t r[64];
-                ptx::tmem_ld64(sbuf, r);
+        SegmentWalk walk = walk_begin(p, pfx, pair);
+        Segment sg;
+        int jg = 0;   // pages done so far, across segments
+        while (ok && walk_next(p, pfx, pair, walk, sg)) {
+            const int ntiles = seg_pages(sg);
+            if (ntiles > 0) {
+                // q of this request: dims 256..575 -> shared memory (cp.async;
+                // padded heads zero-filled), dims 0..255 -> TMEM, two 64-dim
+                // blocks per round of loads. The previous segment's score MMAs
+                // (the only readers of q) are complete: this warp saw their
+                // last s_full.
+                const uint16_t* qrow = p.q + (size_t(sg.b) * N + (live_head ? h : 0)) * kD;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float2 v = __fmul2_rn(
-                        make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), scale2);
-                    x[2 * i] = v.x;
-                    x[2 * i + 1] = v.y;
+                for (int kb = 0; kb < 5; ++kb)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        ptx::cp_async16(
+                            sbase + uint32_t(kOffQS + kb * 16384 + h * 128 + ((c ^ (h & 7)) * 16)),
+                            qrow + 64 * (kQTmemBlocks + kb) + 8 * c, live_head ? 16u : 0u);
+#pragma unroll 1
+                for (int c2 = 0; c2 < kQTmemBlocks; c2 += 2) {
+                    uint32_t r0[32], r1[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r0[i] = r1[i] = 0u;
+                    if (live_head) {
+                        const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * c2);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint4 v = __ldg(src + i);
+                            const uint4 w = __ldg(src + 8 + i);
+                            r0[4 * i + 0] = v.x;
+                            r0[4 * i + 1] = v.y;
+                            r0[4 * i + 2] = v.z;
+                            r0[4 * i + 3] = v.w;
+                            r1[4 * i + 0] = w.x;
+                            r1[4 * i + 1] = w.y;
+                            r1[4 * i + 2] = w.z;
+                            r1[4 * i + 3] = w.w;
+                        }
+                    }
+                    ptx::tmem_st32(trow + kTmemQ + uint32_t(c2 * 32), r0);
+                    ptx::tmem_st32(trow + kTmemQ + uint32_t(c2 * 32 + 32), r1);
                 }
-            }
-            if (valid < kTile) {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) x[i] = i < valid ? x[i] : -INFINITY;
-            }
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            const float m_new = fmaxf(m_ref, mx);
-            const bool rescale = m_new > m_ref + kRescaleThreshold;
-            float alpha = 1.f;
-            if (rescale) {
-                alpha = ptx::ex2(m_ref - m_new);
-                m_ref = m_new;
+                ptx::cp_async_wait_all();
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(b_qready);
             }
 
-            // Weights: P row of this head, 64 tokens as bf16 pairs, written
-            // over the first 32 columns of the score buffer (all read above).
-            // Masked tokens (x = -inf) get 0.
-            float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            float2 lb2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            {
-                const float2 negm2 = make_float2(-m_ref, -m_ref);
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float2 d = __fadd2_rn(make_float2(x[2 * i], x[2 * i + 1]), negm2);
-                    const float a = ptx::ex2(d.x);
-                    const float c = ptx::ex2(d.y);
-                    pk[i] = pack_bf16x2(a, c);
-                    ls2[i & 1] = __fadd2_rn(ls2[i & 1], make_float2(a, c));
-                    lb2[i & 1] = __fadd2_rn(lb2[i & 1], make_float2(__uint_as_float(pk[i] << 16),
-                                                                    __uint_as_float(pk[i] & 0xffff0000u)));
-                }
-                ptx::tmem_st32(sbuf, pk);
-            }
-            const float2 ls = __fadd2_rn(ls2[0], ls2[1]);
-            const float2 lb = __fadd2_rn(lb2[0], lb2[1]);
-            l_sum = l_sum * alpha + (ls.x + ls.y);
-            l_bf = l_bf * alpha + (lb.x + lb.y);
-
-            // O rescale once the P.V of page j-1 is done.
-            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = wait_phase(b_pfree + 8 * ((j - 1) & 1), uint32_t((j - 1) >> 1) & 1u, bars,
-                                p.status, kSitePvDone);
+            float m_ref = -INFINITY;   // log2 units
+            float l_sum = 0.f;         // sum of fp32 weights (for the LSE)
+            float l_bf = 0.f;          // sum of the bf16 weights the MMA used (for O)
+            const int jg0 = jg;
+            for (int j = 0; j < ntiles; ++j, ++jg) {
+                const int sl = jg & 1;
+                ok = wait_phase(b_sfull + 8 * sl, uint32_t(jg >> 1) & 1u, bars, p.status,
+                                kSiteSFull);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 ptx::tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < 256; c += 32) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(trow + kTmemO + uint32_t(c), o);
+                // The page's 64 scores of this head, scaled to log2 units.
+                const uint32_t sbuf = trow + kTmemS + uint32_t(sl * 64);
+                const int valid = min(kTile, sg.t_hi - (sg.t_lo + j * kTile));
+                const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
+                float x[64];
+                {
+                    uint32_t r[64];
+                    ptx::tmem_ld64(sbuf, r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    ptx::tmem_st32(trow + kTmemO + uint32_t(c), o);
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 v = __fmul2_rn(
+                            make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                            scale2);
+                        x[2 * i] = v.x;
+                        x[2 * i + 1] = v.y;
+                    }
                 }
-            }
-            // Rows past the sequence end in the last page may hold anything
-            // (even NaN): zero their value columns so that 0 * V stays 0.
-            if (valid < kTile) {
-                unsigned char* vs = smem + kOffV + sl * kVBytes;
-                const int rows = kTile - valid;
-                for (int idx = h; idx < rows * 32; idx += 128) {
-                    const int row = valid + idx / 32;
-                    const int blk = (idx / 8) & 3;
-                    const int ch = idx & 7;
-                    *reinterpret_cast<uint4*>(vs + blk * kBlockBytes + row * 128 + ch * 16) =
-                        make_uint4(0, 0, 0, 0);
+                if (valid < kTile) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) x[i] = i < valid ? x[i] : -INFINITY;
                 }
-                ptx::fence_proxy_async_smem();
-            }
-            // The fourth softmax warp to finish page j issues its P.V MMAs.
-            ptx::tc_fence_before();
-            __syncwarp();
-            uint32_t done_before = 0;
-            if (lane == 0) done_before = ptx::atom_add_acq_rel_shared(a_pcount + 4 * sl, 1u);
-            done_before = __shfl_sync(0xffffffffu, done_before, 0);
-            if (done_before == 4u * uint32_t(j >> 1) + 3u) {
-                ptx::tc_fence_after();
-                if (ptx::elect_one()) issue_pv(tmem, sbase, j, b_vempty, b_pfree);
-                __syncwarp();
-                issued_pv = true;
-            }
-        }
-        // Every P.V MMA this warp issued completes before TMEM is freed.
-        if (issued_pv) warp_drain(b_final_sm + 8 * quarter, margs);
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                const float m_new = fmaxf(m_ref, mx);
+                const bool rescale = m_new > m_ref + kRescaleThreshold;
+                float alpha = 1.f;
+                if (rescale) {
+                    alpha = ptx::ex2(m_ref - m_new);
+                    m_ref = m_new;
+                }
 
-        // Epilogue: O / l -> bf16 output, or the fp32 split partial.
-        if (ok && ntiles > 0) {
-            // The commit after the last P.V covers every earlier one too.
-            ok = wait_phase(b_pfree + 8 * ((ntiles - 1) & 1), uint32_t((ntiles - 1) >> 1) & 1u,
-                            bars, p.status, kSitePvDone);
-            ok = __all_sync(0xffffffffu, ok);
-            ptx::tc_fence_after();
-        }
-        if (ok && aligned_ok) {
+                // Weights: P row of this head, 64 tokens as bf16 pairs, written
+                // over the first 32 columns of the score buffer (all read
+                // above). Masked tokens (x = -inf) get 0.
+                float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                float2 lb2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                {
+                    const float2 negm2 = make_float2(-m_ref, -m_ref);
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 d = __fadd2_rn(make_float2(x[2 * i], x[2 * i + 1]), negm2);
+                        const float a = ptx::ex2(d.x);
+                        const float c = ptx::ex2(d.y);
+                        pk[i] = pack_bf16x2(a, c);
+                        ls2[i & 1] = __fadd2_rn(ls2[i & 1], make_float2(a, c));
+                        lb2[i & 1] = __fadd2_rn(
+                            lb2[i & 1], make_float2(__uint_as_float(pk[i] << 16),
+                                                    __uint_as_float(pk[i] & 0xffff0000u)));
+                    }
+                    ptx::tmem_st32(sbuf, pk);
+                }
+                const float2 ls = __fadd2_rn(ls2[0], ls2[1]);
+                const float2 lb = __fadd2_rn(lb2[0], lb2[1]);
+                l_sum = l_sum * alpha + (ls.x + ls.y);
+                l_bf = l_bf * alpha + (lb.x + lb.y);
+
+                // O rescale once the P.V of the previous page is done.
+                if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    ok = wait_phase(b_pfree + 8 * ((jg - 1) & 1), uint32_t((jg - 1) >> 1) & 1u, bars,
+                                    p.status, kSitePvDone);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    ptx::tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 256; c += 32) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(trow + kTmemO + uint32_t(c), o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        ptx::tmem_st32(trow + kTmemO + uint32_t(c), o);
+                    }
+                }
+                // Rows past the sequence end in the last page may hold anything
+                // (even NaN): zero their value columns so that 0 * V stays 0.
+                if (valid < kTile) {
+                    unsigned char* vs = smem + kOffV + sl * kVBytes;
+                    const int rows = kTile - valid;
+                    for (int idx = h; idx < rows * 32; idx += 128) {
+                        const int row = valid + idx / 32;
+                        const int blk = (idx / 8) & 3;
+                        const int ch = idx & 7;
+                        *reinterpret_cast<uint4*>(vs + blk * kBlockBytes + row * 128 + ch * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    ptx::fence_proxy_async_smem();
+                }
+                // The fourth softmax warp to finish page jg issues its P.V MMAs
+                // (the first page of a segment starts O afresh).
+                ptx::tc_fence_before();
+                __syncwarp();
+                uint32_t done_before = 0;
+                if (lane == 0) done_before = ptx::atom_add_acq_rel_shared(a_pcount + 4 * sl, 1u);
+                done_before = __shfl_sync(0xffffffffu, done_before, 0);
+                if (done_before == 4u * uint32_t(jg >> 1) + 3u) {
+                    ptx::tc_fence_after();
+                    if (ptx::elect_one()) issue_pv(tmem, sbase, jg, j > 0, b_vempty, b_pfree);
+                    __syncwarp();
+                    issued_pv = true;
+                }
+            }
+            if (!ok) break;
+
+            // Epilogue: O / l -> bf16 output, or the fp32 partial row.
+            if (ntiles > 0) {
+                // The commit after the segment's last P.V covers every
+                // earlier one too.
+                const int jl = jg0 + ntiles - 1;
+                ok = wait_phase(b_pfree + 8 * (jl & 1), uint32_t(jl >> 1) & 1u, bars, p.status,
+                                kSitePvDone);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ptx::tc_fence_after();
+            }
             const float inv = l_bf > 0.f ? 1.f / l_bf : 0.f;
             const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-            const size_t row = size_t(b) * N + h;
+            const size_t row = size_t(sg.b) * N + h;
+            const size_t prow = size_t(sg.prow0) + size_t(h) * sg.prow_stride;
 #pragma unroll 1
             for (int c = 0; c < 256; c += 32) {
                 uint32_t o[32];
@@ -605,7 +736,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 const int col = 256 * int(rank) + c;
                 if (!live_head) {
                     // padded head row: nothing to write
-                } else if (S == 1) {
+                } else if (sg.prow0 < 0) {
                     uint4* dst = reinterpret_cast<uint4*>(p.out + row * kLkv + col);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -621,8 +752,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                         dst[i] = v;
                     }
                 } else {
-                    float4* dst =
-                        reinterpret_cast<float4*>(p.o_part + (row * S + split) * kLkv + col);
+                    float4* dst = reinterpret_cast<float4*>(p.o_part + prow * kLkv + col);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
@@ -632,13 +762,18 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 }
             }
             if (rank == 0 && live_head) {
-                if (S == 1) {
+                if (sg.prow0 < 0) {
                     if (p.lse != nullptr) p.lse[row] = lse;
                 } else {
-                    p.lse_part[row * S + split] = lse;
+                    p.lse_part[prow] = lse;
                 }
             }
+            // The next segment's first P.V overwrites O: every softmax warp
+            // has read it by then, since that P.V waits for all four warps
+            // to finish the segment's first page, which comes after this.
         }
+        // Every P.V MMA this warp issued completes before TMEM is freed.
+        if (issued_pv) warp_drain(b_final_sm + 8 * quarter, margs);
     }
 
     ptx::tc_fence_before();

@@ -46,4 +46,24 @@ __device__ __forceinline__ int checked_seq_len(const DecodeParams& p, int b) {
     return L;
 }
 
+// ------------------------------------------------------ page-balanced schedule
+// The pages of the batch, request after request, are cut into `pairs`
+// contiguous ranges of near-equal length; CTA pair c works through pages
+// [pair_begin(c), pair_begin(c + 1)). A request that lies inside one range is
+// written directly; one that crosses a range boundary leaves a partial result
+// in each range it touches, and the merge combines them. A range holds at
+// most two partial pieces: that of its first request (slot 2c; the range
+// starts inside that request or at its first page) and that of its last
+// request (slot 2c + 1; the range ends inside it).
+__device__ __forceinline__ int64_t pair_begin(int c, int pairs, int64_t total_pages) {
+    return int64_t(c) * total_pages / pairs;
+}
+
+// The range c holding page g (0 <= g < total_pages).
+__device__ __forceinline__ int pair_of_page(int64_t g, int pairs, int64_t total_pages) {
+    return int(((g + 1) * pairs + total_pages - 1) / total_pages) - 1;
+}
+
+__device__ __forceinline__ int pages_of(int L) { return (L + kPageSize - 1) / kPageSize; }
+
 }  // namespace mla

@@ -15,6 +15,8 @@ constexpr int kPageSize = 64;      // tokens per block
 constexpr int kMaxHeads = 128;
 constexpr size_t kStatusBytes = 256;   // status header at the start of the workspace
 constexpr int kMaxMergeSplits = 1024;
+constexpr int kMaxBalancedBatch = 512;   // the page-balanced schedule keeps B+1 offsets in smem
+constexpr int kMaxBalancedPairs = 256;   // pieces one merged row can have
 
 // Layout of the status header (int32 words).
 //   [0] first MLA_ERR_* recorded by a kernel (0 = none)
@@ -34,12 +36,14 @@ struct DecodeParams {
     int32_t max_blocks;
     int32_t batch;
     int32_t num_heads;
-    int32_t num_splits;
+    int32_t num_splits;           // S of the split schedule (1 when sched_pairs > 0)
+    int32_t sched_pairs;          // > 0: page-balanced schedule over this many CTA pairs
     float scale_log2;             // softmax_scale * log2(e)
-    uint16_t* out;                // bf16 [B, N, 512]          (num_splits == 1)
-    float* lse;                   // fp32 [B, N] or null       (num_splits == 1)
-    float* o_part;                // fp32 [B, N, S, 512]       (num_splits > 1)
-    float* lse_part;              // fp32 [B, N, S]            (num_splits > 1)
+    uint16_t* out;                // bf16 [B, N, 512]
+    float* lse;                   // fp32 [B, N] or null
+    float* o_part;                // fp32 partial rows: [B, N, S, 512] (split, S > 1)
+                                  //                    or [2 * pairs, N, 512] (balanced)
+    float* lse_part;              // fp32 [B, N, S] or [2 * pairs, N]
     int32_t* status;              // status header in the workspace
 };
 
@@ -48,6 +52,7 @@ int launch_decode_simt(const DecodeParams& p, void* stream);
 int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream);
 int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,
                  int v_dim, uint16_t* out, float* lse, void* stream);
+int launch_merge_balanced(const DecodeParams& p, void* stream);
 int launch_gather(const uint16_t* cache, int64_t num_blocks, const int32_t* block_table,
                   const int32_t* seq_lens, int batch, int max_blocks, int dst_max_tokens,
                   uint16_t* dst, int32_t* status, void* stream);

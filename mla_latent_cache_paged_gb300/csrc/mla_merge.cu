@@ -69,7 +69,133 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(
     }
 }
 
+// Merge of the page-balanced schedule: CTA (b, y) handles request b, heads
+// 8y..8y+7, one warp per head. The request's page offset and the batch's page
+// total come from a block reduction over seq_lens, which gives the CTA pairs
+// whose ranges touch the request (the same cut as the decode kernel's). A
+// request inside one range was written by the decode kernel; a request
+// without pages gets O = 0 and LSE = -inf; the others combine one partial per
+// range, slot 2c or 2c + 1, with the LSE-weighted sum of merge_attn_states.
+constexpr int kBalMergeWarps = 8;
+
+__global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel(const DecodeParams p) {
+    __shared__ int64_t red_before[kBalMergeWarps], red_total[kBalMergeWarps];
+    __shared__ float weights[kBalMergeWarps][kMaxBalancedPairs];
+    __shared__ int slots[kMaxBalancedPairs];
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int N = p.num_heads;
+    const int h = blockIdx.y * kBalMergeWarps + warp;
+    auto pages_checked = [&](int i) {
+        const int L = p.seq_lens[i];
+        return (L < 0 || int64_t(L) > int64_t(p.max_blocks) * kPageSize) ? 0 : pages_of(L);
+    };
+    int64_t before = 0, total = 0;
+    for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
+        const int pg = pages_checked(i);
+        total += pg;
+        if (i < b) before += pg;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        total += __shfl_xor_sync(0xffffffffu, total, o);
+    }
+    if (lane == 0) {
+        red_before[warp] = before;
+        red_total[warp] = total;
+    }
+    __syncthreads();
+    before = 0;
+    total = 0;
+    for (int w = 0; w < kBalMergeWarps; ++w) {
+        before += red_before[w];
+        total += red_total[w];
+    }
+    const int64_t pb = before, pe = before + pages_checked(b);
+    const int C = p.sched_pairs;
+
+    if (pe == pb) {
+        // No pages: O = 0, LSE = -inf.
+        if (h < N) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t(b) * N + h) * kLkv);
+            for (int i = lane; i < kLkv / 8; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+            if (lane == 0 && p.lse != nullptr) p.lse[size_t(b) * N + h] = -INFINITY;
+        }
+        return;
+    }
+    const int c_lo = pair_of_page(pb, C, total);
+    const int c_hi = pair_of_page(pe - 1, C, total);
+    if (c_lo == c_hi) return;   // inside one range: written by the decode kernel
+    const int pieces = c_hi - c_lo + 1;
+    for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
+        const int c = c_lo + i;
+        slots[i] = pair_begin(c, C, total) >= pb ? 2 * c : 2 * c + 1;
+    }
+    __syncthreads();
+    if (h >= N) return;
+
+    float* w = weights[warp];
+    float m = -INFINITY;
+    for (int i = lane; i < pieces; i += 32) m = fmaxf(m, p.lse_part[size_t(slots[i]) * N + h]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float lse_h = -INFINITY;
+    if (m != -INFINITY) {
+        float z = 0.f;
+        for (int i = lane; i < pieces; i += 32) z += expf(p.lse_part[size_t(slots[i]) * N + h] - m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        lse_h = m + logf(z);
+        for (int i = lane; i < pieces; i += 32)
+            w[i] = expf(p.lse_part[size_t(slots[i]) * N + h] - lse_h);
+    } else {
+        for (int i = lane; i < pieces; i += 32) w[i] = 0.f;
+    }
+    __syncwarp();
+    if (lane == 0 && p.lse != nullptr) p.lse[size_t(b) * N + h] = lse_h;
+    // Lane l owns columns 4l + 128k (k = 0..3): four independent 16-byte
+    // loads per piece in flight.
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < pieces; ++i) {
+        const float wi = w[i];
+        if (wi == 0.f) continue;
+        const float* src = p.o_part + (size_t(slots[i]) * N + h) * kLkv + lane * 4;
+        float4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = __ldg(reinterpret_cast<const float4*>(src + 128 * k));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc[k].x = fmaf(wi, v[k].x, acc[k].x);
+            acc[k].y = fmaf(wi, v[k].y, acc[k].y);
+            acc[k].z = fmaf(wi, v[k].z, acc[k].z);
+            acc[k].w = fmaf(wi, v[k].w, acc[k].w);
+        }
+    }
+    uint16_t* dst = p.out + (size_t(b) * N + h) * kLkv + lane * 4;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint2 packed;
+        packed.x = uint32_t(f32_to_bf16_bits_rn(acc[k].x)) |
+                   (uint32_t(f32_to_bf16_bits_rn(acc[k].y)) << 16);
+        packed.y = uint32_t(f32_to_bf16_bits_rn(acc[k].z)) |
+                   (uint32_t(f32_to_bf16_bits_rn(acc[k].w)) << 16);
+        *reinterpret_cast<uint2*>(dst + 128 * k) = packed;
+    }
+}
+
 }  // namespace
+
+int launch_merge_balanced(const DecodeParams& p, void* stream) {
+    if (p.batch == 0) return 0;
+    if (p.sched_pairs < 1 || p.sched_pairs > kMaxBalancedPairs) return int(cudaErrorInvalidValue);
+    const dim3 grid(unsigned(p.batch), unsigned((p.num_heads + kBalMergeWarps - 1) / kBalMergeWarps));
+    mla_merge_balanced_kernel<<<grid, kBalMergeWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return int(cudaGetLastError());
+}
 
 int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,
                  int v_dim, uint16_t* out, float* lse, void* stream) {

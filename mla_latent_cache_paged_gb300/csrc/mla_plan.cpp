@@ -33,6 +33,32 @@ double list_schedule(const std::vector<double>& costs, int machines) {
 
 int heads_per_simt_cta() { return 16; }
 
+// Fixed cost of one work item (or one segment of the balanced schedule) of the
+// tensor-core kernel, in pages: q staging, pipeline fill and the epilogue.
+constexpr double kTcItemPages = 4.0;
+
+// Workspace layout for a plan: status header, then the fp32 partial rows and
+// their LSEs. Split schedule: [B, N, S, Lkv] and [B, N, S] (S > 1 only);
+// balanced schedule: [2 * pairs, N, Lkv] and [2 * pairs, N].
+void workspace_layout(int batch, int num_heads, int S, int pairs, uint64_t* part_off,
+                      uint64_t* lse_off, uint64_t* bytes) {
+    uint64_t rows = 0;
+    if (pairs > 0)
+        rows = uint64_t(2) * pairs * num_heads;
+    else if (S > 1)
+        rows = uint64_t(batch) * num_heads * S;
+    uint64_t off = kStatusBytes;
+    *part_off = 0;
+    *lse_off = 0;
+    if (rows > 0) {
+        *part_off = off;
+        off = align_up(off + rows * kLkv * sizeof(float), 256);
+        *lse_off = off;
+        off = align_up(off + rows * sizeof(float), 256);
+    }
+    *bytes = off;
+}
+
 // Estimated run time, in units of "one page through one worker", of a split
 // count S. Each (request, split) is one work item; partial results cost
 // their write + read through HBM, spread over all workers.
@@ -47,13 +73,14 @@ double estimate(int kernel, int S, int batch, int num_heads, const std::vector<i
         workers = std::max(1, num_sms * 2);          // two SIMT CTAs per SM
         items_per_split = (num_heads + heads_per_simt_cta() - 1) / heads_per_simt_cta();
     }
+    const double item = kernel == MLA_KERNEL_TC ? kTcItemPages : 0.15;
     std::vector<double> costs;
     costs.reserve(size_t(batch) * S * items_per_split);
     for (int b = 0; b < batch; ++b) {
         int per_split = (pages[b] + S - 1) / S;
         for (int s = 0; s < S; ++s) {
             int here = std::max(0, std::min(per_split, pages[b] - s * per_split));
-            for (int i = 0; i < items_per_split; ++i) costs.push_back(0.15 + here);
+            for (int i = 0; i < items_per_split; ++i) costs.push_back(item + here);
         }
     }
     double t = list_schedule(costs, workers);
@@ -63,6 +90,21 @@ double estimate(int kernel, int S, int batch, int num_heads, const std::vector<i
         double per_round = page_bytes * (kernel == MLA_KERNEL_TC ? workers : workers / 2.0);
         t += partial / per_round + 4.0;  // + the merge launch
     }
+    return t;
+}
+
+// Estimated run time, same units, of the page-balanced schedule over `pairs`
+// CTA pairs: an equal share of the pages, one item cost per request a pair
+// touches, and the partial rows of the requests that cross range boundaries
+// (at most two per pair) written and read once.
+double estimate_balanced(int pairs, int batch, int num_heads, const std::vector<int>& pages) {
+    double total = 0.0;
+    for (int pg : pages) total += pg;
+    const double segments = 1.0 + double(batch) / pairs;
+    double t = total / pairs + kTcItemPages * segments;
+    const double page_bytes = double(kPageSize) * kD * 2.0;
+    const double partial = 2.0 * pairs * num_heads * (kLkv * 4.0 + 4.0) * 2.0;
+    t += partial / (page_bytes * pairs) + 4.0;   // + the merge launch
     return t;
 }
 
@@ -78,6 +120,26 @@ int validate_plan(const mla_decode_plan_t* p) {
         return MLA_ERR_INVALID_ARG;
     if (p->kernel != MLA_KERNEL_SIMT && p->kernel != MLA_KERNEL_TC) return MLA_ERR_INVALID_ARG;
     if (p->kernel == MLA_KERNEL_TC && !tc_kernel_built()) return MLA_ERR_UNSUPPORTED;
+    if (p->sched_pairs < 0 || p->sched_pairs > kMaxBalancedPairs) return MLA_ERR_INVALID_ARG;
+    if (p->sched_pairs > 0 && (p->kernel != MLA_KERNEL_TC || p->num_kv_splits != 1 ||
+                               p->batch > kMaxBalancedBatch))
+        return MLA_ERR_INVALID_ARG;
+    // The launch shape and the workspace layout follow from the sizes; a plan
+    // that disagrees was not made by mla_decode_plan (or was edited).
+    int64_t grid;
+    if (p->kernel == MLA_KERNEL_TC)
+        grid = p->sched_pairs > 0 ? 2 * int64_t(p->sched_pairs)
+                                  : 2 * int64_t(p->batch) * p->num_kv_splits;
+    else
+        grid = int64_t((p->num_heads + heads_per_simt_cta() - 1) / heads_per_simt_cta()) *
+               p->batch * p->num_kv_splits;
+    if (grid != p->grid_ctas) return MLA_ERR_INVALID_ARG;
+    uint64_t part_off, lse_off, bytes;
+    workspace_layout(p->batch, p->num_heads, p->num_kv_splits, p->sched_pairs, &part_off, &lse_off,
+                     &bytes);
+    if (p->partial_offset != part_off || p->lse_partial_offset != lse_off ||
+        p->workspace_bytes != bytes)
+        return MLA_ERR_INVALID_ARG;
     return MLA_OK;
 }
 
@@ -119,10 +181,12 @@ extern "C" int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int r
         kernel = MLA_KERNEL_SIMT;
 
     int S = num_kv_splits;
+    int pairs = 0;
     if (S == 0) {
         S = 1;
+        double best = 0.0;
         if (batch > 0 && max_pages > 1) {
-            double best = estimate(kernel, 1, batch, num_heads, pages, num_sms);
+            best = estimate(kernel, 1, batch, num_heads, pages, num_sms);
             int cap = std::min(max_pages, 64);
             for (int s = 2; s <= cap; ++s) {
                 double t = estimate(kernel, s, batch, num_heads, pages, num_sms);
@@ -131,6 +195,20 @@ extern "C" int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int r
                     S = s;
                 }
             }
+        }
+        // The page-balanced schedule: every co-resident CTA pair gets an
+        // equal share of the batch's pages (tensor-core kernel only).
+        int64_t total_pages = 0;
+        for (int pg : pages) total_pages += pg;
+        const int c = int(std::min<int64_t>({int64_t(num_sms / 2), int64_t(kMaxBalancedPairs),
+                                             total_pages}));
+        if (kernel == MLA_KERNEL_TC && !(flags & MLA_PLAN_SPLIT_ONLY) && batch > 0 &&
+            batch <= kMaxBalancedBatch && c >= 1 &&
+            int64_t(batch) * max_blocks_per_seq < (int64_t(1) << 31) &&
+            ((flags & MLA_PLAN_FORCE_BALANCED) ||
+             (best > 0.0 && estimate_balanced(c, batch, num_heads, pages) < best * 0.98))) {
+            pairs = c;
+            S = 1;
         }
     }
 
@@ -143,22 +221,17 @@ extern "C" int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int r
     plan->max_blocks_per_seq = max_blocks_per_seq;
     plan->max_seq_len = max_seq_len;
     plan->num_kv_splits = S;
+    plan->sched_pairs = pairs;
     plan->kernel = kernel;
     plan->num_sms = num_sms;
     plan->flags = flags;
     if (kernel == MLA_KERNEL_TC)
-        plan->grid_ctas = 2 * batch * S;
+        plan->grid_ctas = pairs > 0 ? 2 * pairs : 2 * batch * S;
     else
         plan->grid_ctas = ((num_heads + heads_per_simt_cta() - 1) / heads_per_simt_cta()) * batch * S;
 
-    uint64_t off = kStatusBytes;
-    if (S > 1) {
-        plan->partial_offset = off;
-        off = align_up(off + uint64_t(batch) * num_heads * S * kLkv * sizeof(float), 256);
-        plan->lse_partial_offset = off;
-        off = align_up(off + uint64_t(batch) * num_heads * S * sizeof(float), 256);
-    }
-    plan->workspace_bytes = off;
+    workspace_layout(batch, num_heads, S, pairs, &plan->partial_offset, &plan->lse_partial_offset,
+                     &plan->workspace_bytes);
     return MLA_OK;
 }
 

@@ -77,12 +77,14 @@ def assert_lse_close(got, ref, what=""):
     return float(err.max()) if err.size else 0.0
 
 
-def run_decode(w, num_kv_splits=None, force_simt=False, device="cuda"):
+def run_decode(w, num_kv_splits=None, force_simt=False, device="cuda", schedule="auto",
+               num_sms=None):
     """Run the CUDA path on workload `w`; returns (out_f64, lse, plan, tensors)."""
     import torch
     q, cache, table, lens = to_torch(w, device)
     splits = w.num_kv_splits if num_kv_splits is None else num_kv_splits
-    plan = binding.make_plan(w.batch, w.num_heads, w.max_blocks_per_seq,
+    plan = binding.make_plan(w.batch, w.num_heads, w.max_blocks_per_seq, schedule=schedule,
+                             num_sms=num_sms,
                              seq_lens_host=w.seq_lens, max_seq_len=max(w.max_seq_len, 0),
                              num_kv_splits=splits, force_simt=force_simt)
     ws = binding.new_workspace(plan, device)

@@ -32,16 +32,18 @@ def test_every_declared_function_is_exported(lib):
     for name in names:
         assert hasattr(lib, name), name
     assert set(names) == set(binding.EXPORTED_SYMBOLS)
-    assert lib.mla_abi_version() == 1
+    version = int(re.search(r"#define MLA_DECODE_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert lib.mla_abi_version() == version
 
 
 def test_plan_struct_layout_matches_the_header(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "mla_decode.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(mla_decode_plan_t),"
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(mla_decode_plan_t),"
         " offsetof(mla_decode_plan_t, flags), offsetof(mla_decode_plan_t, workspace_bytes),"
-        " offsetof(mla_decode_plan_t, lse_partial_offset), offsetof(mla_decode_plan_t, reserved));"
+        " offsetof(mla_decode_plan_t, lse_partial_offset), offsetof(mla_decode_plan_t, sched_pairs),"
+        " offsetof(mla_decode_plan_t, reserved));"
         "return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o",
@@ -50,7 +52,7 @@ def test_plan_struct_layout_matches_the_header(tmp_path):
                                           check=True).stdout.split()]
     P = binding.MlaDecodePlan
     want = [ctypes.sizeof(P), P.flags.offset, P.workspace_bytes.offset,
-            P.lse_partial_offset.offset, P.reserved.offset]
+            P.lse_partial_offset.offset, P.sched_pairs.offset, P.reserved.offset]
     assert got == want
 
 
@@ -172,3 +174,42 @@ def test_status_strings(lib):
 def test_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(RuntimeError):
         binding.load_library(str(tmp_path / "missing.so"))
+
+
+def test_plan_balanced_schedule(lib):
+    # Headline shape: 128 requests of 128 pages on 152 SMs -> 76 CTA pairs.
+    rc, plan = _plan(lib, batch=128, max_blocks=128, max_seq=8192, lens=[8192] * 128)
+    assert rc == 0
+    assert (plan.sched_pairs, plan.grid_ctas, plan.num_kv_splits) == (76, 152, 1)
+    rows = 2 * 76 * 128
+    assert plan.partial_offset == 256
+    assert plan.lse_partial_offset == 256 + rows * 512 * 4
+    assert plan.workspace_bytes == plan.lse_partial_offset + rows * 4
+    # The split-only flag, the CUDA-core kernel and an explicit S keep the split schedule.
+    for kw in (dict(flags=binding.MLA_PLAN_SPLIT_ONLY), dict(flags=binding.MLA_PLAN_FORCE_SIMT),
+               dict(splits=2)):
+        rc, p2 = _plan(lib, batch=128, max_blocks=128, max_seq=8192, lens=[8192] * 128, **kw)
+        assert rc == 0 and p2.sched_pairs == 0, kw
+    # More requests than the offsets table holds: split schedule.
+    rc, p3 = _plan(lib, batch=600, max_blocks=4, max_seq=256, lens=[256] * 600,
+                   flags=binding.MLA_PLAN_FORCE_BALANCED)
+    assert rc == 0 and p3.sched_pairs == 0
+    # Forced: at most one pair per page.
+    rc, p4 = _plan(lib, batch=2, max_blocks=4, max_seq=256, lens=[100, 30],
+                   flags=binding.MLA_PLAN_FORCE_BALANCED)
+    assert rc == 0 and p4.sched_pairs == 3 and p4.grid_ctas == 6
+
+
+def test_decode_rejects_a_plan_that_does_not_follow_from_its_sizes(lib):
+    rc, plan = _plan(lib, batch=128, max_blocks=128, max_seq=8192, lens=[8192] * 128)
+    assert rc == 0
+    dummy = ctypes.c_void_p(1 << 20)
+    for field, value in (("grid_ctas", plan.grid_ctas + 2), ("sched_pairs", 300),
+                         ("workspace_bytes", plan.workspace_bytes - 256),
+                         ("num_kv_splits", 2)):
+        bad = binding.MlaDecodePlan.from_buffer_copy(plan)
+        setattr(bad, field, value)
+        rc = lib.mla_decode(ctypes.byref(bad), dummy, dummy, 16, dummy, dummy,
+                            ctypes.c_float(0.1), dummy, None, dummy,
+                            ctypes.c_size_t(1 << 40), None)
+        assert rc == binding.MLA_ERR_INVALID_ARG, field
