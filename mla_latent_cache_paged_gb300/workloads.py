@@ -170,6 +170,13 @@ def _c3(with_data=True):
                          num_kv_splits=0, with_data=with_data)
 
 
+def _c3_small(with_data=True):
+    # The headline shape at 16 requests (151 MB of cache, still larger than
+    # L2): the small case for full-section profiles of the same kernel.
+    return make_workload("b16_n128_l8192", 16, 128, [8192] * 16, seed=20260006,
+                         num_kv_splits=0, with_data=with_data)
+
+
 def _c4(length):
     def build(with_data=True):
         return make_workload(f"b4_n128_l{length // 1024}k_s64", 4, 128, [length] * 4,
@@ -191,6 +198,7 @@ WORKLOADS = {
     "b1_n16_l256_pool8": _c1,
     "b32_n128_l1k-4k": _c2,
     "b128_n128_l8192": _c3,
+    "b16_n128_l8192": _c3_small,
     "b4_n128_l32k_s64": _c4(32768),
     "b4_n128_l64k_s64": _c4(65536),
     "b4_n128_l96k_s64": _c4(98304),

@@ -160,6 +160,7 @@ def test_bad_seq_len_is_reported(kernel):
     ("b1_n16_l256_pool8", None),
     ("b32_n128_l1k-4k", None),
     ("b128_n128_l8192", [0, 17, 63, 64, 101, 127]),
+    ("b16_n128_l8192", [0, 7, 15]),
     ("b4_n128_l32k_s64", None),
     ("b4_n128_l64k_s64", [0, 3]),
     ("b4_n128_l96k_s64", [1]),
