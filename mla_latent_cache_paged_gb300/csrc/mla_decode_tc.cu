@@ -92,6 +92,8 @@ struct TcBars {
     uint64_t s_full[2];   // score MMAs of the page complete
     uint64_t p_free[2];   // P.V MMA complete: score buffer free, O current
     uint64_t q_ready;     // q staged (128 arrivals)
+    uint64_t q_staged;    // q dims 0..255 copied to the staging area (128 arrivals)
+    uint64_t q_read;      // staging area read into TMEM (128 arrivals)
     uint64_t final_qk;    // drain of the score warp's MMAs
     uint64_t final_sm[4]; // drain of each softmax warp's P.V MMAs
     uint32_t p_count[2];  // softmax warps done with the pages of each parity
@@ -403,6 +405,8 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
     const uint32_t b_sfull = ptx::smem_addr(&bars->s_full[0]);
     const uint32_t b_pfree = ptx::smem_addr(&bars->p_free[0]);
     const uint32_t b_qready = ptx::smem_addr(&bars->q_ready);
+    const uint32_t b_qstaged = ptx::smem_addr(&bars->q_staged);
+    const uint32_t b_qread = ptx::smem_addr(&bars->q_read);
     const uint32_t b_final_qk = ptx::smem_addr(&bars->final_qk);
     const uint32_t b_final_sm = ptx::smem_addr(&bars->final_sm[0]);
     const uint32_t a_pcount = ptx::smem_addr(&bars->p_count[0]);
@@ -420,6 +424,8 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 bars->p_count[i] = 0;
             }
             ptx::mbar_init(b_qready, 128);
+            ptx::mbar_init(b_qstaged, 128);
+            ptx::mbar_init(b_qread, 128);
             ptx::mbar_init(b_final_qk, 1);
             for (int i = 0; i < 4; ++i) ptx::mbar_init(b_final_sm + 8 * i, 1);
             bars->abort = 0;
@@ -491,12 +497,31 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                         reinterpret_cast<const unsigned char*>(p.cache) + size_t(blk) * kPageBytes;
                     ptx::prefetch_l2(page + rank * (kPageBytes / 2), kPageBytes / 2);
                 };
+                // q of the next segment's request into L2 (half per CTA) a
+                // few pages before this segment ends (earlier, the page
+                // stream would evict it), so that staging it is short.
+                int q_next = -1;
+                if (k_ring) {
+                    SegmentWalk peek = walk;
+                    Segment nx;
+                    if (walk_next(p, pfx, pair, peek, nx)) q_next = nx.b;
+                }
+                auto prefetch_q = [&]() {
+                    if (q_next < 0) return;
+                    const uint32_t qbytes = uint32_t(N) * kD * 2;   // a multiple of 16
+                    const unsigned char* qb =
+                        reinterpret_cast<const unsigned char*>(p.q + size_t(q_next) * N * kD);
+                    const uint32_t half = (qbytes / 2) & ~15u;
+                    ptx::prefetch_l2(qb + rank * half, rank == 0 ? half : qbytes - half);
+                };
+                if (ntiles <= kPrefetchAhead) prefetch_q();
                 for (int j = 0; j < kPrefetchAhead; ++j) prefetch(j);
                 int next = ntiles > 0 ? table[page0] : 0;
                 for (int j = 0; j < ntiles; ++j, ++jg) {
                     const int blk = next;
                     if (j + 1 < ntiles) next = table[page0 + j + 1];
                     prefetch(j + kPrefetchAhead);
+                    if (j + kPrefetchAhead == ntiles) prefetch_q();
                     int32_t y;
                     if (blk >= 0 && int64_t(blk) < p.num_blocks) {
                         y = blk * kTile;
@@ -545,55 +570,72 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
         const bool live_head = h < N;
         bool issued_pv = false;
         bool ok = true;
-        SegmentWalk walk = walk_begin(p, pfx, pair);
-        Segment sg;
-        int jg = 0;   // pages done so far, across segments
-        while (ok && walk_next(p, pfx, pair, walk, sg)) {
-            const int ntiles = seg_pages(sg);
-            if (ntiles > 0) {
-                // q of this request: dims 256..575 -> shared memory (cp.async;
-                // padded heads zero-filled), dims 0..255 -> TMEM, two 64-dim
-                // blocks per round of loads. The previous segment's score MMAs
-                // (the only readers of q) are complete: this warp saw their
-                // last s_full.
-                const uint16_t* qrow = p.q + (size_t(sg.b) * N + (live_head ? h : 0)) * kD;
-#pragma unroll
-                for (int kb = 0; kb < 5; ++kb)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        ptx::cp_async16(
-                            sbase + uint32_t(kOffQS + kb * 16384 + h * 128 + ((c ^ (h & 7)) * 16)),
-                            qrow + 64 * (kQTmemBlocks + kb) + 8 * c, live_head ? 16u : 0u);
-#pragma unroll 1
-                for (int c2 = 0; c2 < kQTmemBlocks; c2 += 2) {
-                    uint32_t r0[32], r1[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r0[i] = r1[i] = 0u;
-                    if (live_head) {
-                        const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * c2);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const uint4 v = __ldg(src + i);
-                            const uint4 w = __ldg(src + 8 + i);
-                            r0[4 * i + 0] = v.x;
-                            r0[4 * i + 1] = v.y;
-                            r0[4 * i + 2] = v.z;
-                            r0[4 * i + 3] = v.w;
-                            r1[4 * i + 0] = w.x;
-                            r1[4 * i + 1] = w.y;
-                            r1[4 * i + 2] = w.z;
-                            r1[4 * i + 3] = w.w;
-                        }
-                    }
-                    ptx::tmem_st32(trow + kTmemQ + uint32_t(c2 * 32), r0);
-                    ptx::tmem_st32(trow + kTmemQ + uint32_t(c2 * 32 + 32), r1);
-                }
-                ptx::cp_async_wait_all();
-                ptx::fence_proxy_async_smem();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(b_qready);
+        // q of request qb, copied with coalesced 16-byte cp.async (a warp
+        // copies whole rows): dims 0..255 first into the q area as a staging
+        // copy (row r at 512 r, chunk c at (c ^ r % 32) * 16: conflict-free
+        // row reads), from which each thread moves its own row to TMEM; then
+        // dims 256..575 into the q area in the score MMAs' SW128 layout. Rows
+        // of padded heads are zero-filled. Called once every score MMA that
+        // read the previous q has completed. Returns false if a wait expired.
+        int nstage = 0;
+        auto stage_q = [&](int qb) -> bool {
+            const uint16_t* qbase = p.q + size_t(qb) * N * kD;
+            const uint32_t ph = uint32_t(nstage++) & 1u;
+            const int t = tid - 64;   // 0..127 over the four softmax warps
+#pragma unroll 4
+            for (int k = 0; k < 32; ++k) {
+                const int i = t + 128 * k;   // 128 rows x 32 chunks
+                const int r = i >> 5, c = i & 31;
+                const bool live = r < N;
+                ptx::cp_async16(sbase + uint32_t(kOffQS + r * 512 + ((c ^ (r & 31)) * 16)),
+                                qbase + (live ? size_t(r) * kD + 8 * c : 0), live ? 16u : 0u);
             }
-
+            ptx::cp_async_wait_all();
+            ptx::mbar_arrive(b_qstaged);
+            if (!wait_phase(b_qstaged, ph, bars, p.status, kSiteQReady)) return false;
+#pragma unroll 1
+            for (int blk = 0; blk < kQTmemBlocks; ++blk) {
+                uint32_t r32[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = 8 * blk + i;
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        smem + kOffQS + h * 512 + ((c ^ (h & 31)) * 16));
+                    r32[4 * i + 0] = v.x;
+                    r32[4 * i + 1] = v.y;
+                    r32[4 * i + 2] = v.z;
+                    r32[4 * i + 3] = v.w;
+                }
+                ptx::tmem_st32(trow + kTmemQ + uint32_t(blk * 32), r32);
+            }
+            ptx::mbar_arrive(b_qread);
+            if (!wait_phase(b_qread, ph, bars, p.status, kSiteQReady)) return false;
+#pragma unroll 4
+            for (int k = 0; k < 40; ++k) {
+                const int i = t + 128 * k;   // 128 rows x 40 chunks (dims 256..575)
+                const int r = i / 40, c = i - 40 * (i / 40);
+                const int kb = c >> 3, cc = c & 7;
+                const bool live = r < N;
+                ptx::cp_async16(
+                    sbase + uint32_t(kOffQS + kb * 16384 + r * 128 + ((cc ^ (r & 7)) * 16)),
+                    qbase + (live ? size_t(r) * kD + 256 + 8 * c : 0), live ? 16u : 0u);
+            }
+            ptx::cp_async_wait_all();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(b_qready);
+            return true;
+        };
+        SegmentWalk walk = walk_begin(p, pfx, pair);
+        Segment sg, nx;
+        bool have = walk_next(p, pfx, pair, walk, sg);
+        if (have && seg_pages(sg) > 0) ok = __all_sync(0xffffffffu, stage_q(sg.b));
+        int jg = 0;   // pages done so far, across segments
+        while (ok && have) {
+            const int ntiles = seg_pages(sg);
+            // The next segment, looked up now so that its global loads are
+            // done by the time this segment ends.
+            const bool have_next = walk_next(p, pfx, pair, walk, nx);
             float m_ref = -INFINITY;   // log2 units
             float l_sum = 0.f;         // sum of fp32 weights (for the LSE)
             float l_bf = 0.f;          // sum of the bf16 weights the MMA used (for O)
@@ -709,6 +751,15 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             }
             if (!ok) break;
 
+            // q of the next segment goes in now, ahead of this epilogue: the
+            // score MMAs of this segment (the only readers of q) are complete
+            // (this warp saw their last s_full), and the score warp can start
+            // the next segment while the output is written.
+            if (have_next && seg_pages(nx) > 0) {
+                ok = __all_sync(0xffffffffu, stage_q(nx.b));
+                if (!ok) break;
+            }
+
             // Epilogue: O / l -> bf16 output, or the fp32 partial row.
             if (ntiles > 0) {
                 // The commit after the segment's last P.V covers every
@@ -771,6 +822,8 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             // The next segment's first P.V overwrites O: every softmax warp
             // has read it by then, since that P.V waits for all four warps
             // to finish the segment's first page, which comes after this.
+            sg = nx;
+            have = have_next;
         }
         // Every P.V MMA this warp issued completes before TMEM is freed.
         if (issued_pv) warp_drain(b_final_sm + 8 * quarter, margs);
