@@ -88,13 +88,15 @@ extern "C" {
  *
  * Page-balanced schedule (sched_pairs = C > 0, MLA_KERNEL_TC, B <= 512,
  * num_kv_splits = 1). This is a work-partitioning choice of this library; the
- * papers' split-KV has no counterpart of it. The pages of the batch, request
- * after request, are cut into C contiguous ranges of near-equal length (range
- * c = pages [floor(c*P/C), floor((c+1)*P/C)) of the P pages, taken from the
- * device seq_lens at run time), one per CTA pair. A request inside one range
- * is written directly; one that crosses range boundaries leaves fp32 partial
- * rows ([2C,N,Lkv] / [2C,N] in the workspace: slot 2c for the first request
- * of range c, slot 2c+1 for its last) that a second kernel combines with the
+ * papers' split-KV has no counterpart of it. In work units, a request with
+ * p > 0 pages is 3 units of fixed cost followed by its p pages (an empty
+ * request is nothing); the batch's units, request after request (taken from
+ * the device seq_lens at run time, T in total), are cut into C contiguous
+ * ranges, range c = units [floor(c*T/C), floor((c+1)*T/C)), one per CTA
+ * pair. A request whose pages lie inside one range is written directly; one
+ * whose pages cross range boundaries leaves fp32 partial rows ([2C,N,Lkv] /
+ * [2C,N] in the workspace: slot 2c for the first request with pages in range
+ * c, slot 2c+1 for its last) that a second kernel combines with the
  * LSE-weighted merge. Results agree with the split schedule up to rounding.
  */
 typedef struct mla_decode_plan {

@@ -78,6 +78,7 @@ constexpr uint64_t kTimeoutNs = 1000000000ull;   // 1 s per wait
 // A waiting thread sleeps in mbarrier.try_wait until the phase completes (or
 // this long), so waiting warps take no issue slots from the working ones.
 constexpr uint32_t kSuspendNs = 20000;
+constexpr int kSoftmaxSpin = 256;   // polls of s_full before the softmax warps sleep
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
@@ -165,12 +166,13 @@ struct Segment {
 
 struct SegmentWalk {
     int next_b;        // balanced: next request to look at; split: 1 once done
-    int64_t g0, g1;    // balanced: the pair's page range
+    int64_t g0, g1;    // balanced: the pair's unit range
+    bool first;        // balanced: no segment returned yet
 };
 
 __device__ __forceinline__ SegmentWalk walk_begin(const DecodeParams& p, const int32_t* pfx,
                                                   int pair) {
-    SegmentWalk w{0, 0, 0};
+    SegmentWalk w{0, 0, 0, true};
     if (p.sched_pairs > 0) {
         const int64_t total = pfx[p.batch];
         if (total > 0) {
@@ -206,15 +208,18 @@ __device__ __forceinline__ bool walk_next(const DecodeParams& p, const int32_t* 
     }
     while (w.next_b < p.batch && pfx[w.next_b] < w.g1) {
         const int b = w.next_b++;
-        const int64_t pb = pfx[b], pe = pfx[b + 1];
-        if (pe == pb) continue;   // no pages: the merge writes this request
+        if (pfx[b + 1] == pfx[b]) continue;   // no pages: the merge writes this request
+        // The request's pages occupy units [pb, pe), after its fixed cost.
+        const int64_t pb = pfx[b] + kSegmentCostPages, pe = pfx[b + 1];
         const int64_t lo = pb > w.g0 ? pb : w.g0;
         const int64_t hi = pe < w.g1 ? pe : w.g1;
+        if (lo >= hi) continue;   // only the fixed cost falls in this range
         s.b = b;
         s.t_lo = int(lo - pb) * kPageSize;
         s.t_hi = min(p.seq_lens[b], int(hi - pb) * kPageSize);
-        s.prow0 = (lo == pb && hi == pe) ? -1 : (lo == w.g0 ? 2 * pair : 2 * pair + 1) * p.num_heads;
+        s.prow0 = (lo == pb && hi == pe) ? -1 : (w.first ? 2 * pair : 2 * pair + 1) * p.num_heads;
         s.prow_stride = 1;
+        w.first = false;
         return true;
     }
     return false;
@@ -432,7 +437,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
         if (p.sched_pairs > 0) {
-            // Page offsets of the balanced schedule: pfx[b] = pages of
+            // Unit offsets of the balanced schedule: pfx[b] = work units of
             // requests 0..b-1 (a request with an invalid length has none).
             int carry = 0;
             for (int base = 0; base < p.batch; base += 128) {
@@ -440,7 +445,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int i = base + 32 * k + lane;
-                    pg[k] = i < p.batch ? pages_of(checked_seq_len(p, i)) : 0;
+                    pg[k] = i < p.batch ? work_units(pages_of(checked_seq_len(p, i))) : 0;
                 }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -642,8 +647,15 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             const int jg0 = jg;
             for (int j = 0; j < ntiles; ++j, ++jg) {
                 const int sl = jg & 1;
-                ok = wait_phase(b_sfull + 8 * sl, uint32_t(jg >> 1) & 1u, bars, p.status,
-                                kSiteSFull);
+                // Poll briefly before sleeping: the scores are usually a few
+                // hundred cycles away and a poll wakes sooner than a
+                // suspended thread.
+                ok = false;
+                for (int sp = 0; sp < kSoftmaxSpin && !ok; ++sp)
+                    ok = ptx::mbar_test_wait(b_sfull + 8 * sl, uint32_t(jg >> 1) & 1u);
+                if (!ok)
+                    ok = wait_phase(b_sfull + 8 * sl, uint32_t(jg >> 1) & 1u, bars, p.status,
+                                    kSiteSFull);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 ptx::tc_fence_after();
                 // The page's 64 scores of this head, scaled to log2 units.

@@ -47,14 +47,20 @@ __device__ __forceinline__ int checked_seq_len(const DecodeParams& p, int b) {
 }
 
 // ------------------------------------------------------ page-balanced schedule
-// The pages of the batch, request after request, are cut into `pairs`
-// contiguous ranges of near-equal length; CTA pair c works through pages
-// [pair_begin(c), pair_begin(c + 1)). A request that lies inside one range is
-// written directly; one that crosses a range boundary leaves a partial result
-// in each range it touches, and the merge combines them. A range holds at
-// most two partial pieces: that of its first request (slot 2c; the range
-// starts inside that request or at its first page) and that of its last
-// request (slot 2c + 1; the range ends inside it).
+// Work units: a request with p > 0 pages is kSegmentCostPages units of fixed
+// cost followed by its p pages; an empty request is nothing. The batch's
+// units, request after request (prefix pfx[b] = units of requests 0..b-1,
+// total T), are cut into `pairs` contiguous ranges of near-equal length; CTA
+// pair c works through the pages that fall in units
+// [pair_begin(c), pair_begin(c + 1)). A request whose pages lie inside one
+// range is written directly; one whose pages cross a range boundary leaves a
+// partial result in each range it touches, and the merge combines them. A
+// range holds at most two partial pieces: that of its first request with
+// pages in the range (slot 2c) and that of its last (slot 2c + 1).
+__device__ __forceinline__ int work_units(int pages) {
+    return pages > 0 ? pages + kSegmentCostPages : 0;
+}
+
 __device__ __forceinline__ int64_t pair_begin(int c, int pairs, int64_t total_pages) {
     return int64_t(c) * total_pages / pairs;
 }

@@ -17,6 +17,10 @@ constexpr size_t kStatusBytes = 256;   // status header at the start of the work
 constexpr int kMaxMergeSplits = 1024;
 constexpr int kMaxBalancedBatch = 512;   // the page-balanced schedule keeps B+1 offsets in smem
 constexpr int kMaxBalancedPairs = 256;   // pieces one merged row can have
+// Page-balanced schedule: a request with pages counts as its pages plus this
+// many pages of work for the cut (q staging and the epilogue a CTA pair pays
+// for each request it touches).
+constexpr int kSegmentCostPages = 3;
 
 // Layout of the status header (int32 words).
 //   [0] first MLA_ERR_* recorded by a kernel (0 = none)

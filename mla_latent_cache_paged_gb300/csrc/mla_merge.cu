@@ -91,9 +91,9 @@ __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel
         const int L = p.seq_lens[i];
         return (L < 0 || int64_t(L) > int64_t(p.max_blocks) * kPageSize) ? 0 : pages_of(L);
     };
-    int64_t before = 0, total = 0;
+    int64_t before = 0, total = 0;   // work units
     for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
-        const int pg = pages_checked(i);
+        const int pg = work_units(pages_checked(i));
         total += pg;
         if (i < b) before += pg;
     }
@@ -113,10 +113,12 @@ __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel
         before += red_before[w];
         total += red_total[w];
     }
-    const int64_t pb = before, pe = before + pages_checked(b);
+    const int pages_b = pages_checked(b);
+    // The request's pages occupy units [pb, pe), after its fixed cost.
+    const int64_t pb = before + kSegmentCostPages, pe = before + work_units(pages_b);
     const int C = p.sched_pairs;
 
-    if (pe == pb) {
+    if (pages_b == 0) {
         // No pages: O = 0, LSE = -inf.
         if (h < N) {
             uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t(b) * N + h) * kLkv);
@@ -131,7 +133,9 @@ __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel
     const int pieces = c_hi - c_lo + 1;
     for (int i = threadIdx.x; i < pieces; i += blockDim.x) {
         const int c = c_lo + i;
-        slots[i] = pair_begin(c, C, total) >= pb ? 2 * c : 2 * c + 1;
+        // b is the first request with pages in range c unless an earlier
+        // request's pages reach into it (its range starts before b's units).
+        slots[i] = pair_begin(c, C, total) >= before ? 2 * c : 2 * c + 1;
     }
     __syncthreads();
     if (h >= N) return;

@@ -19,19 +19,23 @@ pytestmark = pytest.mark.gpu
 PS = 64
 
 
+SEG_COST = 3   # units of fixed cost per request with pages (the header's cut rule)
+
+
 def balanced_pieces(lens, pairs):
     """Host restatement of the cut: {request: [(slot, t_lo, t_hi), ...]} for the
-    requests that cross a range boundary, and the set of requests written
-    whole by one pair."""
+    requests whose pages cross a range boundary, and the set of requests whose
+    pages lie inside one range."""
     pages = [-(-int(L) // PS) for L in lens]
-    pfx = np.concatenate([[0], np.cumsum(pages)]).astype(np.int64)
+    units = [pg + SEG_COST if pg > 0 else 0 for pg in pages]
+    pfx = np.concatenate([[0], np.cumsum(units)]).astype(np.int64)
     total = int(pfx[-1])
     begin = [c * total // pairs for c in range(pairs + 1)]
     pieces, whole = {}, set()
     for b, L in enumerate(lens):
-        pb, pe = int(pfx[b]), int(pfx[b + 1])
-        if pe == pb:
+        if pages[b] == 0:
             continue
+        pb, pe = int(pfx[b]) + SEG_COST, int(pfx[b + 1])   # units holding the pages
         cs = [c for c in range(pairs) if begin[c] < pe and begin[c + 1] > pb]
         if len(cs) == 1:
             whole.add(b)
@@ -39,7 +43,7 @@ def balanced_pieces(lens, pairs):
         pieces[b] = []
         for c in cs:
             lo, hi = max(begin[c], pb), min(begin[c + 1], pe)
-            slot = 2 * c if begin[c] >= pb else 2 * c + 1
+            slot = 2 * c if begin[c] >= int(pfx[b]) else 2 * c + 1
             pieces[b].append((slot, (lo - pb) * PS, min(int(L), (hi - pb) * PS)))
     return pieces, whole
 
