@@ -288,21 +288,34 @@ __device__ __forceinline__ uint64_t desc_vmn(uint32_t addr) {
 }
 
 // Four score MMAs (K = 64 dims) of dim block KB against the 64 x 64 block at
-// shared-memory address bblk. Called by one elected lane.
+// shared-memory address bblk. Called by one elected lane. The first MMA also
+// probes the mbarrier phase (bar, parity) without blocking (bar = 0: no
+// probe); returns the probe's answer.
 template <int KB>
-__device__ __forceinline__ void score_block(uint32_t d, uint32_t tmem, uint32_t qs, uint32_t bblk,
-                                            bool first) {
+__device__ __forceinline__ uint32_t score_block(uint32_t d, uint32_t tmem, uint32_t qs,
+                                                uint32_t bblk, bool first, uint32_t bar = 0,
+                                                uint32_t parity = 0) {
     constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(kTile, false);
+    uint32_t done = 1;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
         const uint64_t bdesc = desc_kmajor(bblk + uint32_t(kk * 32));
         const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-        if (KB < kQTmemBlocks)
-            ptx::mma_ts(d, tmem + kTmemQ + uint32_t(KB * 32 + kk * 8), bdesc, idesc_qk, acc);
-        else
-            ptx::mma_ss(d, desc_kmajor(qs + uint32_t((KB - kQTmemBlocks) * 16384 + kk * 32)),
-                        bdesc, idesc_qk, acc);
+        if (KB < kQTmemBlocks) {
+            const uint32_t at = tmem + kTmemQ + uint32_t(KB * 32 + kk * 8);
+            if (kk == 0 && bar != 0)
+                done = ptx::mma_ts_probe(d, at, bdesc, idesc_qk, acc, bar, parity);
+            else
+                ptx::mma_ts(d, at, bdesc, idesc_qk, acc);
+        } else {
+            const uint64_t ad = desc_kmajor(qs + uint32_t((KB - kQTmemBlocks) * 16384 + kk * 32));
+            if (kk == 0 && bar != 0)
+                done = ptx::mma_ss_probe(d, ad, bdesc, idesc_qk, acc, bar, parity);
+            else
+                ptx::mma_ss(d, ad, bdesc, idesc_qk, acc);
+        }
     }
+    return done;
 }
 
 // S = Q K^T for every page: the five K-ring blocks, then the four value
@@ -327,44 +340,56 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
         const int ntiles = seg_pages(sg);
         if (ntiles == 0) continue;
         ok = warp_wait(b_qready, uint32_t(nseg++) & 1u, a, kSiteQReady);
-        for (int j = 0; ok && j < ntiles; ++j, ++jg) {
-            const int sl = jg & 1;
-            const uint32_t ph = uint32_t(jg >> 1) & 1u;
-            // The score buffer is free once the P.V MMA of page jg-2 has read P.
-            if (jg >= 2 && !warp_wait(b_pfree + 8 * sl, ph ^ 1u, a, kSiteSFree)) {
-                ok = false;
-                break;
-            }
-            if (!warp_wait(b_kfull + 8 * sl, ph, a, kSiteKFull)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t d = tmem + kTmemS + uint32_t(sl * 64);
-            const uint32_t kslot = a.sbase + uint32_t(kOffK + sl * kKBytes);
-            const uint32_t vslot = a.sbase + uint32_t(kOffV + sl * kVBytes);
-            if (ptx::elect_one()) {
+        if (!ok) break;
+        // One elected lane issues the whole segment. Each barrier it needs
+        // is first probed inside an earlier MMA (the probe's latency passes
+        // while the lane waits for the pipe), and it only waits when the
+        // probe found the phase still pending.
+        const int jg0 = jg;
+        if (ptx::elect_one()) {
+            bool ready = false;   // this page's score buffer and K-ring blocks
+            for (int j = 0; j < ntiles; ++j) {
+                const int jc = jg0 + j;
+                const int sl = jc & 1;
+                const uint32_t ph = uint32_t(jc >> 1) & 1u;
+                if (!ready) {
+                    // The score buffer is free once the P.V MMA of page jc-2 has read P.
+                    if (jc >= 2 && !wait_phase(b_pfree + 8 * sl, ph ^ 1u, a.bars, a.status,
+                                               kSiteSFree))
+                        break;
+                    if (!wait_phase(b_kfull + 8 * sl, ph, a.bars, a.status, kSiteKFull)) break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d = tmem + kTmemS + uint32_t(sl * 64);
+                const uint32_t kslot = a.sbase + uint32_t(kOffK + sl * kKBytes);
+                const uint32_t vslot = a.sbase + uint32_t(kOffV + sl * kVBytes);
+                const uint32_t b_vf = b_vfull + 8 * sl;
                 score_block<k_block(RANK, 0)>(d, tmem, qs, kslot + 0 * kBlockBytes, true);
                 score_block<k_block(RANK, 1)>(d, tmem, qs, kslot + 1 * kBlockBytes, false);
                 score_block<k_block(RANK, 2)>(d, tmem, qs, kslot + 2 * kBlockBytes, false);
-                score_block<k_block(RANK, 3)>(d, tmem, qs, kslot + 3 * kBlockBytes, false);
+                const uint32_t vr = score_block<k_block(RANK, 3)>(
+                    d, tmem, qs, kslot + 3 * kBlockBytes, false, b_vf, ph);
                 score_block<k_block(RANK, 4)>(d, tmem, qs, kslot + 4 * kBlockBytes, false);
                 ptx::mma_commit(b_kempty + 8 * sl);
-            }
-            __syncwarp();
-            if (!warp_wait(b_vfull + 8 * sl, ph, a, kSiteVFull)) {
-                ok = false;
-                break;
-            }
-            if (ptx::elect_one()) {
+                if (!vr && !wait_phase(b_vf, ph, a.bars, a.status, kSiteVFull)) break;
+                // The next page's buffer and blocks are probed here (page jn
+                // may lie in the next segment or not exist: then the answers
+                // are not used).
+                const int jn = jc + 1;
+                const uint32_t phn = uint32_t(jn >> 1) & 1u;
                 score_block<4 * RANK + 0>(d, tmem, qs, vslot + 0 * kBlockBytes, false);
                 score_block<4 * RANK + 1>(d, tmem, qs, vslot + 1 * kBlockBytes, false);
-                score_block<4 * RANK + 2>(d, tmem, qs, vslot + 2 * kBlockBytes, false);
-                score_block<4 * RANK + 3>(d, tmem, qs, vslot + 3 * kBlockBytes, false);
+                const uint32_t nf = score_block<4 * RANK + 2>(
+                    d, tmem, qs, vslot + 2 * kBlockBytes, false, b_pfree + 8 * (jn & 1), phn ^ 1u);
+                const uint32_t nk = score_block<4 * RANK + 3>(
+                    d, tmem, qs, vslot + 3 * kBlockBytes, false, b_kfull + 8 * (jn & 1), phn);
                 ptx::mma_commit(b_sfull + 8 * sl);
+                ready = j + 1 < ntiles && (jn < 2 || nf != 0) && nk != 0;
             }
-            __syncwarp();
         }
+        __syncwarp();
+        jg = jg0 + ntiles;
+        if (aborting(a.bars)) ok = false;
     }
     warp_drain(b_final, a);
 }

@@ -254,6 +254,40 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// The same two MMAs, each also testing an mbarrier phase without blocking:
+// the test is issued before the MMA and its answer is read after it, so its
+// latency passes while the issuing thread waits for the pipe to take the MMA.
+// Returns 1 if the phase with `parity` has completed.
+__device__ __forceinline__ uint32_t mma_ss_probe(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate, uint32_t bar,
+                                                 uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p, q;\n mbarrier.test_wait.parity.shared::cta.b64 q, [%6], %7;\n"
+        " setp.ne.b32 p, %5, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(done)
+        : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar), "r"(parity)
+        : "memory");
+    return done;
+}
+
+__device__ __forceinline__ uint32_t mma_ts_probe(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate, uint32_t bar,
+                                                 uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p, q;\n mbarrier.test_wait.parity.shared::cta.b64 q, [%6], %7;\n"
+        " setp.ne.b32 p, %5, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(done)
+        : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar), "r"(parity)
+        : "memory");
+    return done;
+}
+
 // Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
 // when every prior tcgen05 op of this thread completes.
 __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
