@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MLA_DECODE_ABI_VERSION 2
+#define MLA_DECODE_ABI_VERSION 3
 
 /* Status codes. */
 #define MLA_OK                 0
@@ -145,8 +145,12 @@ int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int rope_dim,
 
 /*
  * mla_workspace_init -- zero the status header of a fresh workspace
- * (cudaMemsetAsync of its first 256 bytes on `stream`). Call once per
- * workspace allocation before its first mla_decode.
+ * (cudaMemsetAsync of its first 8192 bytes on `stream`: the status word and
+ * the per-request counters through which the page-balanced merge learns that
+ * a request's partial rows are complete; every call leaves the counters at
+ * zero). Call once per workspace allocation before its first mla_decode, and
+ * again after a call that reported MLA_ERR_TIMEOUT (an abandoned call may
+ * leave counters behind).
  */
 int mla_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
@@ -260,7 +264,9 @@ int mla_abi_version(void);
  * [0, num_blocks) are recorded in the workspace status word and their rows
  * are left untouched. This is the semantics of vLLM's gather_cache /
  * cp_gather_cache (mla_attention API docs, _compute_prefill_context), used
- * here only to check the indexing bit for bit.
+ * here only to check the indexing bit for bit. `workspace` is a status
+ * header: device, >= 8192 bytes, 256-byte aligned, zeroed by
+ * mla_workspace_init.
  */
 int mla_debug_gather_pages(const void* latent_cache, int64_t num_blocks,
                            const int32_t* block_table, const int32_t* seq_lens,

@@ -33,7 +33,7 @@ KV_LORA_RANK = 512
 ROPE_DIM = 64
 HEAD_DIM = KV_LORA_RANK + ROPE_DIM
 PAGE_SIZE = 64
-STATUS_BYTES = 256
+STATUS_BYTES = 8192
 
 EXPORTED_SYMBOLS = (
     "mla_decode_plan", "mla_workspace_init", "mla_decode", "mla_merge_splits",

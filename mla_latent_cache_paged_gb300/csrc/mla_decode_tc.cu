@@ -417,6 +417,10 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
     TcBars* bars = reinterpret_cast<TcBars*>(smem + kOffBar);
     int32_t* pfx = reinterpret_cast<int32_t*>(smem + kOffPfx);
     const uint32_t sbase = ptx::smem_addr(smem);
+    // The page-balanced merge is launched as a programmatic dependent of this
+    // kernel: it may start on SMs this grid has left, and waits for each
+    // request's partial rows through counters (never for the whole grid).
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -855,6 +859,14 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 } else {
                     p.lse_part[prow] = lse;
                 }
+            }
+            if (p.sched_pairs > 0 && sg.prow0 >= 0) {
+                // This warp's part of a partial row set is written: count it
+                // for the merge, which may already be running on SMs that
+                // other CTAs have left (it waits for kPieceArrivals per piece).
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(p.status + kReadyWord + sg.b, 1);
             }
             // The next segment's first P.V overwrites O: every softmax warp
             // has read it by then, since that P.V waits for all four warps

@@ -13,7 +13,7 @@ constexpr int kRope = 64;          // RoPE width
 constexpr int kD = kLkv + kRope;   // one cache entry = absorbed q/k head dim
 constexpr int kPageSize = 64;      // tokens per block
 constexpr int kMaxHeads = 128;
-constexpr size_t kStatusBytes = 256;   // status header at the start of the workspace
+constexpr size_t kStatusBytes = 8192;  // status header at the start of the workspace
 constexpr int kMaxMergeSplits = 1024;
 constexpr int kMaxBalancedBatch = 512;   // the page-balanced schedule keeps B+1 offsets in smem
 constexpr int kMaxBalancedPairs = 256;   // pieces one merged row can have
@@ -21,10 +21,19 @@ constexpr int kMaxBalancedPairs = 256;   // pieces one merged row can have
 // many pages of work for the cut (q staging and the epilogue a CTA pair pays
 // for each request it touches).
 constexpr int kSegmentCostPages = 3;
+constexpr int kReadyWord = 64;
+constexpr int kDoneWord = kReadyWord + kMaxBalancedBatch;
+constexpr int kPieceArrivals = 8;   // increments of kReadyWord + b per partial row set
+static_assert((kDoneWord + kMaxBalancedBatch) * 4 <= int(kStatusBytes), "status header too small");
 
 // Layout of the status header (int32 words).
 //   [0] first MLA_ERR_* recorded by a kernel (0 = none)
 //   [1] detail: the offending block id / seq_len / wait site
+//   [kReadyWord + b]  page-balanced schedule: softmax warps (4 per CTA, both
+//                     CTAs of a pair) that wrote their part of a partial row
+//                     set of request b in this call
+//   [kDoneWord + b]   merge warps done with request b; the last one resets
+//                     both words to 0 for the next call
 struct StatusWords {
     int32_t code;
     int32_t detail;

@@ -77,11 +77,19 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(
 // without pages gets O = 0 and LSE = -inf; the others combine one partial per
 // range, slot 2c or 2c + 1, with the LSE-weighted sum of merge_attn_states.
 constexpr int kBalMergeWarps = 8;
+constexpr int32_t kMergeWaitSite = 20;   // detail of MLA_ERR_TIMEOUT: the merge's wait for pieces
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel(const DecodeParams p) {
     __shared__ int64_t red_before[kBalMergeWarps], red_total[kBalMergeWarps];
     __shared__ float weights[kBalMergeWarps][kMaxBalancedPairs];
     __shared__ int slots[kMaxBalancedPairs];
+    __shared__ int pieces_ready;
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -137,57 +145,91 @@ __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel
         // request's pages reach into it (its range starts before b's units).
         slots[i] = pair_begin(c, C, total) >= before ? 2 * c : 2 * c + 1;
     }
-    __syncthreads();
-    if (h >= N) return;
-
-    float* w = weights[warp];
-    float m = -INFINITY;
-    for (int i = lane; i < pieces; i += 32) m = fmaxf(m, p.lse_part[size_t(slots[i]) * N + h]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float lse_h = -INFINITY;
-    if (m != -INFINITY) {
-        float z = 0.f;
-        for (int i = lane; i < pieces; i += 32) z += expf(p.lse_part[size_t(slots[i]) * N + h] - m);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        lse_h = m + logf(z);
-        for (int i = lane; i < pieces; i += 32)
-            w[i] = expf(p.lse_part[size_t(slots[i]) * N + h] - lse_h);
-    } else {
-        for (int i = lane; i < pieces; i += 32) w[i] = 0.f;
+    // This kernel may run while the decode grid is still working on other
+    // requests: wait until every piece of request b is written (each piece
+    // counts kPieceArrivals softmax warps). Bounded: 4 s, then
+    // MLA_ERR_TIMEOUT and no output for the request.
+    int32_t* ready = p.status + kReadyWord + b;
+    if (threadIdx.x == 0) {
+        const int target = kPieceArrivals * pieces;
+        const uint64_t t0 = globaltimer_ns();
+        int ok = 1;
+        while (*reinterpret_cast<volatile int32_t*>(ready) < target) {
+            if (globaltimer_ns() - t0 > 4000000000ull) {
+                record_error(p.status, MLA_ERR_TIMEOUT, kMergeWaitSite);
+                ok = 0;
+                break;
+            }
+            __nanosleep(200);
+        }
+        pieces_ready = ok;
     }
-    __syncwarp();
-    if (lane == 0 && p.lse != nullptr) p.lse[size_t(b) * N + h] = lse_h;
-    // Lane l owns columns 4l + 128k (k = 0..3): four independent 16-byte
-    // loads per piece in flight.
-    float4 acc[4];
+    __syncthreads();
+    __threadfence();
+    const bool go = pieces_ready != 0;
+    if (go && h < N) {
+        float* w = weights[warp];
+        float m = -INFINITY;
+        for (int i = lane; i < pieces; i += 32)
+            m = fmaxf(m, __ldcg(p.lse_part + size_t(slots[i]) * N + h));
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < pieces; ++i) {
-        const float wi = w[i];
-        if (wi == 0.f) continue;
-        const float* src = p.o_part + (size_t(slots[i]) * N + h) * kLkv + lane * 4;
-        float4 v[4];
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float lse_h = -INFINITY;
+        if (m != -INFINITY) {
+            float z = 0.f;
+            for (int i = lane; i < pieces; i += 32)
+                z += expf(__ldcg(p.lse_part + size_t(slots[i]) * N + h) - m);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = __ldg(reinterpret_cast<const float4*>(src + 128 * k));
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            lse_h = m + logf(z);
+            for (int i = lane; i < pieces; i += 32)
+                w[i] = expf(__ldcg(p.lse_part + size_t(slots[i]) * N + h) - lse_h);
+        } else {
+            for (int i = lane; i < pieces; i += 32) w[i] = 0.f;
+        }
+        __syncwarp();
+        if (lane == 0 && p.lse != nullptr) p.lse[size_t(b) * N + h] = lse_h;
+        // Lane l owns columns 4l + 128k (k = 0..3): four independent 16-byte
+        // loads per piece in flight (L2 only: the rows were written by
+        // another grid that may still be running).
+        float4 acc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < pieces; ++i) {
+            const float wi = w[i];
+            if (wi == 0.f) continue;
+            const float* src = p.o_part + (size_t(slots[i]) * N + h) * kLkv + lane * 4;
+            float4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = __ldcg(reinterpret_cast<const float4*>(src + 128 * k));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc[k].x = fmaf(wi, v[k].x, acc[k].x);
+                acc[k].y = fmaf(wi, v[k].y, acc[k].y);
+                acc[k].z = fmaf(wi, v[k].z, acc[k].z);
+                acc[k].w = fmaf(wi, v[k].w, acc[k].w);
+            }
+        }
+        uint16_t* dst = p.out + (size_t(b) * N + h) * kLkv + lane * 4;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            acc[k].x = fmaf(wi, v[k].x, acc[k].x);
-            acc[k].y = fmaf(wi, v[k].y, acc[k].y);
-            acc[k].z = fmaf(wi, v[k].z, acc[k].z);
-            acc[k].w = fmaf(wi, v[k].w, acc[k].w);
+            uint2 packed;
+            packed.x = uint32_t(f32_to_bf16_bits_rn(acc[k].x)) |
+                       (uint32_t(f32_to_bf16_bits_rn(acc[k].y)) << 16);
+            packed.y = uint32_t(f32_to_bf16_bits_rn(acc[k].z)) |
+                       (uint32_t(f32_to_bf16_bits_rn(acc[k].w)) << 16);
+            *reinterpret_cast<uint2*>(dst + 128 * k) = packed;
         }
     }
-    uint16_t* dst = p.out + (size_t(b) * N + h) * kLkv + lane * 4;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        uint2 packed;
-        packed.x = uint32_t(f32_to_bf16_bits_rn(acc[k].x)) |
-                   (uint32_t(f32_to_bf16_bits_rn(acc[k].y)) << 16);
-        packed.y = uint32_t(f32_to_bf16_bits_rn(acc[k].z)) |
-                   (uint32_t(f32_to_bf16_bits_rn(acc[k].w)) << 16);
-        *reinterpret_cast<uint2*>(dst + 128 * k) = packed;
+    // Every warp of the request's CTAs counts itself once its CTA has seen
+    // the pieces; the last one resets both counters for the next call.
+    __syncwarp();
+    if (lane == 0 && go) {
+        int32_t* done = p.status + kDoneWord + b;
+        if (atomicAdd(done, 1) == int(gridDim.y) * kBalMergeWarps - 1) {
+            *reinterpret_cast<volatile int32_t*>(ready) = 0;
+            *reinterpret_cast<volatile int32_t*>(done) = 0;
+        }
     }
 }
 
@@ -197,8 +239,20 @@ int launch_merge_balanced(const DecodeParams& p, void* stream) {
     if (p.batch == 0) return 0;
     if (p.sched_pairs < 1 || p.sched_pairs > kMaxBalancedPairs) return int(cudaErrorInvalidValue);
     const dim3 grid(unsigned(p.batch), unsigned((p.num_heads + kBalMergeWarps - 1) / kBalMergeWarps));
-    mla_merge_balanced_kernel<<<grid, kBalMergeWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(p);
-    return int(cudaGetLastError());
+    // A programmatic dependent of the decode kernel: its CTAs (about 9 KB of
+    // shared memory each, so none fits beside a decode CTA) start on SMs the
+    // decode grid has left and wait for their requests' pieces themselves.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBalMergeWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return int(cudaLaunchKernelEx(&cfg, mla_merge_balanced_kernel, p));
 }
 
 int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,

@@ -72,12 +72,12 @@ def _plan(lib, batch=4, heads=128, max_blocks=32, max_seq=2048, lens=None, split
 def test_plan_fixed_splits_and_workspace_layout(lib):
     rc, p = _plan(lib, batch=4, heads=128, splits=64)
     assert rc == 0 and p.num_kv_splits == 64
-    assert p.partial_offset == 256
+    assert p.partial_offset == binding.STATUS_BYTES   # status header, then the partials
     assert p.lse_partial_offset >= p.partial_offset + 4 * 128 * 64 * 512 * 4
     assert p.workspace_bytes >= p.lse_partial_offset + 4 * 128 * 64 * 4
     assert p.workspace_bytes % 256 == 0
     rc, p1 = _plan(lib, splits=1)
-    assert rc == 0 and p1.num_kv_splits == 1 and p1.workspace_bytes == 256
+    assert rc == 0 and p1.num_kv_splits == 1 and p1.workspace_bytes == binding.STATUS_BYTES
 
 
 def test_planner_choice_is_bounded_and_deterministic(lib):
@@ -182,8 +182,8 @@ def test_plan_balanced_schedule(lib):
     assert rc == 0
     assert (plan.sched_pairs, plan.grid_ctas, plan.num_kv_splits) == (76, 152, 1)
     rows = 2 * 76 * 128
-    assert plan.partial_offset == 256
-    assert plan.lse_partial_offset == 256 + rows * 512 * 4
+    assert plan.partial_offset == binding.STATUS_BYTES
+    assert plan.lse_partial_offset == binding.STATUS_BYTES + rows * 512 * 4
     assert plan.workspace_bytes == plan.lse_partial_offset + rows * 4
     # The split-only flag, the CUDA-core kernel and an explicit S keep the split schedule.
     for kw in (dict(flags=binding.MLA_PLAN_SPLIT_ONLY), dict(flags=binding.MLA_PLAN_FORCE_SIMT),

@@ -101,3 +101,26 @@ def test_balanced_partials_cover_their_ranges():
             err = np.abs(o_part[slot] - ref_o[0]).max()
             assert err < 2e-2, (b, slot, err)
 
+
+
+def test_balanced_merge_counters_return_to_zero():
+    """The merge of the balanced schedule waits on per-request counters in the
+    workspace's status header; every call must leave them at zero, so that the
+    same workspace serves the next call (bit-identical results)."""
+    import torch
+    from mla_latent_cache_paged_gb300 import binding
+    lens = [1000, 1, 2000, 0, 129, 640, 3000, 77]
+    w = make_workload("bal_ctr", len(lens), 128, lens, seed=91, extra_blocks=2, num_kv_splits=0)
+    _, _, plan, t = run_decode(w, schedule="balanced", num_sms=10)
+    ws = t["ws"]
+    words = ws[:binding.STATUS_BYTES].view(torch.int32).cpu().numpy()
+    assert not words[2:].any(), np.nonzero(words[2:])
+    first_out, first_lse = t["out"].clone(), t["lse"].clone()
+    for _ in range(3):
+        out, lse = binding.mla_decode(t["q"], t["cache"], t["table"], t["lens"], w.softmax_scale,
+                                      plan=plan, workspace=ws)
+        torch.cuda.synchronize()
+        assert binding.read_error(ws) == 0
+        assert torch.equal(out, first_out) and torch.equal(lse, first_lse)
+    words = ws[:binding.STATUS_BYTES].view(torch.int32).cpu().numpy()
+    assert not words[2:].any(), np.nonzero(words[2:])

@@ -19,7 +19,7 @@ def test_gather_pages_bit_exact(lens):
     T = max(max(lens), 1) + 3
     dst = torch.full((w.batch, T, 576), SENTINEL, dtype=torch.int16, device="cuda")
     dst = dst.view(torch.bfloat16)
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(binding.STATUS_BYTES, dtype=torch.uint8, device="cuda")
     binding.debug_gather_pages(cache, table, seq, dst, ws)
     torch.cuda.synchronize()
     assert binding.read_error(ws) == 0
@@ -37,6 +37,6 @@ def test_gather_reports_bad_block_ids():
     _, cache, table, seq = to_torch(w)
     table[0, 1] = w.num_blocks
     dst = torch.zeros((2, 128, 576), dtype=torch.bfloat16, device="cuda")
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(binding.STATUS_BYTES, dtype=torch.uint8, device="cuda")
     binding.debug_gather_pages(cache, table, seq, dst, ws)
     assert binding.read_error(ws) == binding.MLA_ERR_BAD_BLOCK_ID
