@@ -84,7 +84,11 @@ extern "C" {
  * C_b = page_size * ceil(ceil(L_b/page_size)/S); empty splits contribute
  * nothing. With S = 1 the decode kernel writes `out` and `lse` itself; with
  * S > 1 it writes fp32 partials [B,N,S,Lkv] / [B,N,S] into the workspace and
- * mla_merge_splits combines them.
+ * mla_merge_splits combines them (an empty split writes only its LSE, -inf:
+ * its weight is 0 and its row is never read). The tensor-core kernel runs
+ * min(B*S, num_sms/2) CTA pairs, each over a contiguous run of the B*S
+ * (request, split) items in request-major order, and stages a request's q
+ * once for the consecutive splits it takes.
  *
  * Page-balanced schedule (sched_pairs = C > 0, MLA_KERNEL_TC, B <= 512,
  * num_kv_splits = 1). This is a work-partitioning choice of this library; the

@@ -154,9 +154,10 @@ __host__ __device__ constexpr int k_block(int rank, int pos) {
 
 // ------------------------------------------------------------ work segments
 // A CTA pair works through one or more segments: tokens [t_lo, t_hi) of a
-// request. The split schedule gives pair `pair` = (b, split) one segment; the
-// page-balanced schedule gives it the requests its page range touches (the
-// page offsets pfx[b] = pages of requests 0..b-1 are in shared memory).
+// request. In the split schedule the B*S items (b, split), b-major, are cut
+// into one contiguous run per CTA pair and each item is a segment; the
+// page-balanced schedule gives a pair the requests its page range touches
+// (the page offsets pfx[b] = pages of requests 0..b-1 are in shared memory).
 struct Segment {
     int b;
     int t_lo, t_hi;
@@ -165,15 +166,20 @@ struct Segment {
 };
 
 struct SegmentWalk {
-    int next_b;        // balanced: next request to look at; split: 1 once done
-    int64_t g0, g1;    // balanced: the pair's unit range
+    int next_b;        // balanced: next request to look at
+    int64_t g0, g1;    // balanced: the pair's unit range; split: its item range
     bool first;        // balanced: no segment returned yet
 };
 
 __device__ __forceinline__ SegmentWalk walk_begin(const DecodeParams& p, const int32_t* pfx,
                                                   int pair) {
     SegmentWalk w{0, 0, 0, true};
-    if (p.sched_pairs > 0) {
+    if (p.sched_pairs == 0) {
+        const int64_t items = int64_t(p.batch) * p.num_splits;
+        const int64_t pairs = int64_t(gridDim.x >> 1);
+        w.g0 = pair * items / pairs;
+        w.g1 = (pair + 1) * items / pairs;
+    } else {
         const int64_t total = pfx[p.batch];
         if (total > 0) {
             w.g0 = pair_begin(pair, p.sched_pairs, total);
@@ -196,11 +202,11 @@ __device__ __forceinline__ SegmentWalk walk_begin(const DecodeParams& p, const i
 __device__ __forceinline__ bool walk_next(const DecodeParams& p, const int32_t* pfx, int pair,
                                           SegmentWalk& w, Segment& s) {
     if (p.sched_pairs == 0) {
-        if (w.next_b != 0) return false;
-        w.next_b = 1;
+        if (w.g0 >= w.g1) return false;
         const int S = p.num_splits;
-        const int split = pair % S;
-        s.b = pair / S;
+        const int64_t item = w.g0++;
+        const int split = int(item % S);
+        s.b = int(item / S);
         split_range(checked_seq_len(p, s.b), S, split, &s.t_lo, &s.t_hi);
         s.prow0 = S == 1 ? -1 : s.b * p.num_heads * S + split;
         s.prow_stride = S;
@@ -334,13 +340,18 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
     SegmentWalk walk = walk_begin(p, pfx, pair);
     Segment sg;
     int jg = 0;
-    int nseg = 0;   // segments with pages so far (one q_ready phase each)
+    int nseg = 0;   // q stagings waited for so far (one q_ready phase each)
+    int q_b = -1;   // request whose q is staged
     bool ok = true;
     while (ok && walk_next(p, pfx, pair, walk, sg)) {
         const int ntiles = seg_pages(sg);
         if (ntiles == 0) continue;
-        ok = warp_wait(b_qready, uint32_t(nseg++) & 1u, a, kSiteQReady);
-        if (!ok) break;
+        // A new request's q (consecutive splits of one request share it).
+        if (sg.b != q_b) {
+            ok = warp_wait(b_qready, uint32_t(nseg++) & 1u, a, kSiteQReady);
+            if (!ok) break;
+            q_b = sg.b;
+        }
         // One elected lane issues the whole segment. Each barrier it needs
         // is first probed inside an earlier MMA (the probe's latency passes
         // while the lane waits for the pipe), and it only waits when the
@@ -663,7 +674,11 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
         SegmentWalk walk = walk_begin(p, pfx, pair);
         Segment sg, nx;
         bool have = walk_next(p, pfx, pair, walk, sg);
-        if (have && seg_pages(sg) > 0) ok = __all_sync(0xffffffffu, stage_q(sg.b));
+        int staged_b = -1;   // request whose q is staged
+        if (have && seg_pages(sg) > 0) {
+            ok = __all_sync(0xffffffffu, stage_q(sg.b));
+            staged_b = sg.b;
+        }
         int jg = 0;   // pages done so far, across segments
         while (ok && have) {
             const int ntiles = seg_pages(sg);
@@ -796,9 +811,10 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             // score MMAs of this segment (the only readers of q) are complete
             // (this warp saw their last s_full), and the score warp can start
             // the next segment while the output is written.
-            if (have_next && seg_pages(nx) > 0) {
+            if (have_next && seg_pages(nx) > 0 && nx.b != staged_b) {
                 ok = __all_sync(0xffffffffu, stage_q(nx.b));
                 if (!ok) break;
+                staged_b = nx.b;
             }
 
             // Epilogue: O / l -> bf16 output, or the fp32 partial row.
@@ -816,8 +832,11 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
             const size_t row = size_t(sg.b) * N + h;
             const size_t prow = size_t(sg.prow0) + size_t(h) * sg.prow_stride;
+            // An empty split's partial row is never read (its LSE of -inf
+            // gives it weight 0 in the merge): only its LSE is written.
+            const int cend = (ntiles == 0 && sg.prow0 >= 0) ? 0 : 256;
 #pragma unroll 1
-            for (int c = 0; c < 256; c += 32) {
+            for (int c = 0; c < cend; c += 32) {
                 uint32_t o[32];
                 if (ntiles > 0) {
                     ptx::tmem_ld32(trow + kTmemO + uint32_t(c), o);

@@ -59,6 +59,13 @@ void workspace_layout(int batch, int num_heads, int S, int pairs, uint64_t* part
     *bytes = off;
 }
 
+// CTA pairs of the tensor-core kernel's split schedule: one per SM pair, at
+// most one per (request, split) item; each walks a contiguous run of items.
+int64_t tc_split_pairs(int batch, int S, int num_sms) {
+    const int64_t items = int64_t(batch) * S;
+    return std::min<int64_t>(items, std::max(1, num_sms / 2));
+}
+
 // Estimated run time, in units of "one page through one worker", of a split
 // count S. Each (request, split) is one work item; partial results cost
 // their write + read through HBM, spread over all workers.
@@ -129,7 +136,7 @@ int validate_plan(const mla_decode_plan_t* p) {
     int64_t grid;
     if (p->kernel == MLA_KERNEL_TC)
         grid = p->sched_pairs > 0 ? 2 * int64_t(p->sched_pairs)
-                                  : 2 * int64_t(p->batch) * p->num_kv_splits;
+                                  : 2 * tc_split_pairs(p->batch, p->num_kv_splits, p->num_sms);
     else
         grid = int64_t((p->num_heads + heads_per_simt_cta() - 1) / heads_per_simt_cta()) *
                p->batch * p->num_kv_splits;
@@ -228,7 +235,7 @@ extern "C" int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int r
     plan->num_sms = num_sms;
     plan->flags = flags;
     if (kernel == MLA_KERNEL_TC)
-        plan->grid_ctas = pairs > 0 ? 2 * pairs : 2 * batch * S;
+        plan->grid_ctas = pairs > 0 ? 2 * pairs : int(2 * tc_split_pairs(batch, S, num_sms));
     else
         plan->grid_ctas = ((num_heads + heads_per_simt_cta() - 1) / heads_per_simt_cta()) * batch * S;
 

@@ -99,8 +99,12 @@ def test_split_partials_follow_the_page_aligned_partition(kernel):
     assert_lse_close(l_part, ref_l, "lse partials")
     # fp32 partials: the tensor-core kernel rounds P to bf16 for the P.V MMA
     # (relative 2^-9 per weight, so up to ~2^-9 * max|V| ~ 0.01 here); the
-    # bound is the one the bf16 output is held to.
-    err = np.abs(o_part - ref_o).max()
+    # bound is the one the bf16 output is held to. An empty split's row is
+    # only defined by its LSE of -inf (the merge gives it weight 0 and never
+    # reads the row), so the rows are compared where the split has tokens.
+    live = ~np.isneginf(ref_l)
+    assert live.any() and (~live).any()
+    err = np.abs(o_part - ref_o)[live].max()
     assert err < 2e-2, err
 
 
