@@ -831,6 +831,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             const float inv = l_bf > 0.f ? 1.f / l_bf : 0.f;
             const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
             const size_t row = size_t(sg.b) * N + h;
+            const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0u;
             const size_t prow = size_t(sg.prow0) + size_t(h) * sg.prow_stride;
             // An empty split's partial row is never read (its LSE of -inf
             // gives it weight 0 in the merge): only its LSE is written.
@@ -848,28 +849,33 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 if (!live_head) {
                     // padded head row: nothing to write
                 } else if (sg.prow0 < 0) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * kLkv + col);
+                    // bf16 row: 32-byte stores when `out` allows them.
+                    uint16_t* dst = p.out + row * kLkv + col;
+                    uint32_t v[16];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv,
-                                          __uint_as_float(o[8 * i + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv,
-                                          __uint_as_float(o[8 * i + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv,
-                                          __uint_as_float(o[8 * i + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv,
-                                          __uint_as_float(o[8 * i + 7]) * inv);
-                        dst[i] = v;
+                    for (int i = 0; i < 16; ++i)
+                        v[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv,
+                                           __uint_as_float(o[2 * i + 1]) * inv);
+                    if (out32) {
+                        ptx::st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(v));
+                        ptx::st_global_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(v + 8));
+                    } else {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            d4[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     }
                 } else {
-                    float4* dst = reinterpret_cast<float4*>(p.o_part + prow * kLkv + col);
+                    // fp32 partial row (workspace: 256-byte aligned rows).
+                    float* dst = p.o_part + prow * kLkv + col;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
-                                             __uint_as_float(o[4 * i + 1]) * inv,
-                                             __uint_as_float(o[4 * i + 2]) * inv,
-                                             __uint_as_float(o[4 * i + 3]) * inv);
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t v[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            v[k] = __float_as_uint(__uint_as_float(o[8 * i + k]) * inv);
+                        ptx::st_global_v8(dst + 8 * i, v);
+                    }
                 }
             }
             if (rank == 0 && live_head) {

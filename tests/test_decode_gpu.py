@@ -189,3 +189,19 @@ def test_full_size_configs(name, sample):
     e_lse = assert_lse_close(lse[reqs], ref_lse, name)
     print(f"{name}: kernel={plan.kernel} S={plan.num_kv_splits} "
           f"max|out err|={strict:.3g} max|lse err|={e_lse:.3g}")
+
+
+def test_output_at_a_16_byte_offset_matches_aligned_output():
+    """`out` need only be 16-byte aligned (the header's rule); the kernels'
+    wider stores must fall back to 16-byte ones there, bit for bit."""
+    import torch
+    w = make_workload("align16", 3, 128, [700, 64, 1], seed=41, extra_blocks=2, num_kv_splits=1)
+    ref, ref_lse, plan, t = run_decode(w)
+    buf = torch.empty(w.batch * w.num_heads * 512 + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(w.batch, w.num_heads, 512)
+    assert out.data_ptr() % 32 == 16
+    got, lse = binding.mla_decode(t["q"], t["cache"], t["table"], t["lens"], w.softmax_scale,
+                                  plan=plan, workspace=t["ws"], out=out)
+    torch.cuda.synchronize()
+    assert binding.read_error(t["ws"]) == 0
+    assert torch.equal(got, t["out"]) and torch.equal(lse, t["lse"])
