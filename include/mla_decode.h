@@ -93,7 +93,7 @@ extern "C" {
  * Page-balanced schedule (sched_pairs = C > 0, MLA_KERNEL_TC, B <= 512,
  * num_kv_splits = 1). This is a work-partitioning choice of this library; the
  * papers' split-KV has no counterpart of it. In work units, a request with
- * p > 0 pages is 3 units of fixed cost followed by its p pages (an empty
+ * p > 0 pages is 5 units of fixed cost followed by its p pages (an empty
  * request is nothing); the batch's units, request after request (taken from
  * the device seq_lens at run time, T in total), are cut into C contiguous
  * ranges, range c = units [floor(c*T/C), floor((c+1)*T/C)), one per CTA

@@ -20,7 +20,7 @@ constexpr int kMaxBalancedPairs = 256;   // pieces one merged row can have
 // Page-balanced schedule: a request with pages counts as its pages plus this
 // many pages of work for the cut (q staging and the epilogue a CTA pair pays
 // for each request it touches).
-constexpr int kSegmentCostPages = 3;
+constexpr int kSegmentCostPages = 5;
 constexpr int kReadyWord = 64;
 constexpr int kDoneWord = kReadyWord + kMaxBalancedBatch;
 constexpr int kPieceArrivals = 8;   // increments of kReadyWord + b per partial row set

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 PS = 64
 
 
-SEG_COST = 3   # units of fixed cost per request with pages (the header's cut rule)
+SEG_COST = 5   # units of fixed cost per request with pages (the header's cut rule)
 
 
 def balanced_pieces(lens, pairs):
