@@ -294,34 +294,39 @@ __device__ __forceinline__ uint64_t desc_vmn(uint32_t addr) {
 }
 
 // Four score MMAs (K = 64 dims) of dim block KB against the 64 x 64 block at
-// shared-memory address bblk. Called by one elected lane. The first MMA also
-// probes the mbarrier phase (bar, parity) without blocking (bar = 0: no
-// probe); returns the probe's answer.
+// shared-memory address bblk. Called by one elected lane. With bar != 0 the
+// block also tests the mbarrier phase (bar, parity) without blocking, before
+// its first MMA, and reads the answer after its fourth (returned).
 template <int KB>
 __device__ __forceinline__ uint32_t score_block(uint32_t d, uint32_t tmem, uint32_t qs,
                                                 uint32_t bblk, bool first, uint32_t bar = 0,
                                                 uint32_t parity = 0) {
     constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(kTile, false);
-    uint32_t done = 1;
+    const uint32_t acc0 = first ? 0u : 1u;
+    uint64_t bd[4];
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t bdesc = desc_kmajor(bblk + uint32_t(kk * 32));
-        const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-        if (KB < kQTmemBlocks) {
-            const uint32_t at = tmem + kTmemQ + uint32_t(KB * 32 + kk * 8);
-            if (kk == 0 && bar != 0)
-                done = ptx::mma_ts_probe(d, at, bdesc, idesc_qk, acc, bar, parity);
-            else
-                ptx::mma_ts(d, at, bdesc, idesc_qk, acc);
-        } else {
-            const uint64_t ad = desc_kmajor(qs + uint32_t((KB - kQTmemBlocks) * 16384 + kk * 32));
-            if (kk == 0 && bar != 0)
-                done = ptx::mma_ss_probe(d, ad, bdesc, idesc_qk, acc, bar, parity);
-            else
-                ptx::mma_ss(d, ad, bdesc, idesc_qk, acc);
-        }
+    for (int kk = 0; kk < 4; ++kk) bd[kk] = desc_kmajor(bblk + uint32_t(kk * 32));
+    if (KB < kQTmemBlocks) {
+        const uint32_t at = tmem + kTmemQ + uint32_t(KB * 32);
+        if (bar != 0)
+            return ptx::mma4_ts_probe(d, at, at + 8, at + 16, at + 24, bd[0], bd[1], bd[2], bd[3],
+                                      idesc_qk, acc0, bar, parity);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_ts(d, at + uint32_t(kk * 8), bd[kk], idesc_qk, kk == 0 ? acc0 : 1u);
+    } else {
+        const uint32_t qa = qs + uint32_t((KB - kQTmemBlocks) * 16384);
+        uint64_t ad[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) ad[kk] = desc_kmajor(qa + uint32_t(kk * 32));
+        if (bar != 0)
+            return ptx::mma4_ss_probe(d, ad[0], ad[1], ad[2], ad[3], bd[0], bd[1], bd[2], bd[3],
+                                      idesc_qk, acc0, bar, parity);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_ss(d, ad[kk], bd[kk], idesc_qk, kk == 0 ? acc0 : 1u);
     }
-    return done;
+    return 1u;
 }
 
 // S = Q K^T for every page: the five K-ring blocks, then the four value
@@ -358,44 +363,48 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
         // probe found the phase still pending.
         const int jg0 = jg;
         if (ptx::elect_one()) {
-            bool ready = false;   // this page's score buffer and K-ring blocks
+            // This page's score buffer and K-ring blocks, found free / landed
+            // by probes during the previous page.
+            bool pf_ready = false, kf_ready = false;
             for (int j = 0; j < ntiles; ++j) {
                 const int jc = jg0 + j;
                 const int sl = jc & 1;
                 const uint32_t ph = uint32_t(jc >> 1) & 1u;
-                if (!ready) {
-                    // The score buffer is free once the P.V MMA of page jc-2 has read P.
-                    if (jc >= 2 && !wait_phase(b_pfree + 8 * sl, ph ^ 1u, a.bars, a.status,
-                                               kSiteSFree))
-                        break;
-                    if (!wait_phase(b_kfull + 8 * sl, ph, a.bars, a.status, kSiteKFull)) break;
-                }
+                // The score buffer is free once the P.V MMA of page jc-2 has read P.
+                if (jc >= 2 && !pf_ready &&
+                    !wait_phase(b_pfree + 8 * sl, ph ^ 1u, a.bars, a.status, kSiteSFree))
+                    break;
+                if (!kf_ready && !wait_phase(b_kfull + 8 * sl, ph, a.bars, a.status, kSiteKFull))
+                    break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + kTmemS + uint32_t(sl * 64);
                 const uint32_t kslot = a.sbase + uint32_t(kOffK + sl * kKBytes);
                 const uint32_t vslot = a.sbase + uint32_t(kOffV + sl * kVBytes);
                 const uint32_t b_vf = b_vfull + 8 * sl;
+                // Page jn (the next one; it may lie in the next segment or not
+                // exist, and then the answers are not used): its K-ring blocks
+                // are probed early (they landed long ago), its score buffer as
+                // late as possible (the P.V of page jc-1 finishes about now).
+                const int jn = jc + 1;
+                const uint32_t phn = uint32_t(jn >> 1) & 1u;
                 score_block<k_block(RANK, 0)>(d, tmem, qs, kslot + 0 * kBlockBytes, true);
-                score_block<k_block(RANK, 1)>(d, tmem, qs, kslot + 1 * kBlockBytes, false);
+                const uint32_t nk = score_block<k_block(RANK, 1)>(
+                    d, tmem, qs, kslot + 1 * kBlockBytes, false, b_kfull + 8 * (jn & 1), phn);
                 score_block<k_block(RANK, 2)>(d, tmem, qs, kslot + 2 * kBlockBytes, false);
                 const uint32_t vr = score_block<k_block(RANK, 3)>(
                     d, tmem, qs, kslot + 3 * kBlockBytes, false, b_vf, ph);
                 score_block<k_block(RANK, 4)>(d, tmem, qs, kslot + 4 * kBlockBytes, false);
                 ptx::mma_commit(b_kempty + 8 * sl);
                 if (!vr && !wait_phase(b_vf, ph, a.bars, a.status, kSiteVFull)) break;
-                // The next page's buffer and blocks are probed here (page jn
-                // may lie in the next segment or not exist: then the answers
-                // are not used).
-                const int jn = jc + 1;
-                const uint32_t phn = uint32_t(jn >> 1) & 1u;
                 score_block<4 * RANK + 0>(d, tmem, qs, vslot + 0 * kBlockBytes, false);
                 score_block<4 * RANK + 1>(d, tmem, qs, vslot + 1 * kBlockBytes, false);
-                const uint32_t nf = score_block<4 * RANK + 2>(
-                    d, tmem, qs, vslot + 2 * kBlockBytes, false, b_pfree + 8 * (jn & 1), phn ^ 1u);
-                const uint32_t nk = score_block<4 * RANK + 3>(
-                    d, tmem, qs, vslot + 3 * kBlockBytes, false, b_kfull + 8 * (jn & 1), phn);
+                score_block<4 * RANK + 2>(d, tmem, qs, vslot + 2 * kBlockBytes, false);
+                const uint32_t nf = score_block<4 * RANK + 3>(
+                    d, tmem, qs, vslot + 3 * kBlockBytes, false, b_pfree + 8 * (jn & 1), phn ^ 1u);
                 ptx::mma_commit(b_sfull + 8 * sl);
-                ready = j + 1 < ntiles && (jn < 2 || nf != 0) && nk != 0;
+                const bool more = j + 1 < ntiles;
+                pf_ready = more && nf != 0;
+                kf_ready = more && nk != 0;
             }
         }
         __syncwarp();

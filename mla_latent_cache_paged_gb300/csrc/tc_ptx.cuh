@@ -295,6 +295,56 @@ __device__ __forceinline__ uint32_t mma_ts_probe(uint32_t d_tmem, uint32_t a_tme
     return done;
 }
 
+// Four MMAs into one accumulator (A from TMEM at a0..a3, or from shared
+// memory through descriptors a0..a3; B descriptors b0..b3), the first with
+// accumulate flag acc0, the others accumulating; an mbarrier phase is tested
+// before the first and the answer read after the fourth, so the test's
+// latency passes while the MMAs issue. Returns 1 if the phase with `parity`
+// has completed.
+__device__ __forceinline__ uint32_t mma4_ts_probe(uint32_t d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
+                                                  uint64_t b3, uint32_t idesc, uint32_t acc0,
+                                                  uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p, q;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 q, [%11], %12;\n"
+        " setp.ne.b32 p, %10, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %6, %9, p;\n"
+        " setp.eq.b32 p, %10, %10;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [%3], %7, %9, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [%4], %8, %9, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [%5], %13, %9, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(done)
+        : "r"(d), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b0), "l"(b1), "l"(b2), "r"(idesc),
+          "r"(acc0), "r"(bar), "r"(parity), "l"(b3)
+        : "memory");
+    return done;
+}
+
+__device__ __forceinline__ uint32_t mma4_ss_probe(uint32_t d, uint64_t a0, uint64_t a1, uint64_t a2,
+                                                  uint64_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
+                                                  uint64_t b3, uint32_t idesc, uint32_t acc0,
+                                                  uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p, q;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 q, [%11], %12;\n"
+        " setp.ne.b32 p, %10, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %6, %9, p;\n"
+        " setp.eq.b32 p, %10, %10;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], %3, %7, %9, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], %4, %8, %9, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], %5, %13, %9, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(done)
+        : "r"(d), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "r"(idesc),
+          "r"(acc0), "r"(bar), "r"(parity), "l"(b3)
+        : "memory");
+    return done;
+}
+
 // Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
 // when every prior tcgen05 op of this thread completes.
 __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
