@@ -3,6 +3,7 @@
 // goes onto the caller's stream without any host synchronisation.
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 
@@ -54,6 +55,10 @@ extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const vo
     p.num_heads = plan->num_heads;
     p.num_splits = S;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    // A zero scale weighs every token 1; the smallest normal scale does the
+    // same in fp32 (every scaled score rounds 2^x to 1) and keeps the
+    // tensor-core kernel's scaled masking sentinel at -inf.
+    if (p.scale_log2 == 0.f) p.scale_log2 = FLT_MIN;
     p.out = static_cast<uint16_t*>(out);
     p.lse = lse;
     p.status = reinterpret_cast<int32_t*>(ws);

@@ -711,32 +711,40 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                                     kSiteSFull);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 ptx::tc_fence_after();
-                // The page's 64 scores of this head, scaled to log2 units.
+                // The page's 64 raw scores of this head. The scale (log2
+                // units) is applied inside the weights' FMA below, so the
+                // page maximum of the scaled scores is the scale times the
+                // raw maximum (the raw minimum for a negative scale; the host
+                // never passes 0). Tokens past the sequence end get the raw
+                // score that scales to -inf.
                 const uint32_t sbuf = trow + kTmemS + uint32_t(sl * 64);
                 const int valid = min(kTile, sg.t_hi - (sg.t_lo + j * kTile));
-                const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
+                const float sc = p.scale_log2;
                 float x[64];
                 {
                     uint32_t r[64];
                     ptx::tmem_ld64(sbuf, r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float2 v = __fmul2_rn(
-                            make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
-                            scale2);
-                        x[2 * i] = v.x;
-                        x[2 * i + 1] = v.y;
-                    }
+                    for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(r[i]);
                 }
                 if (valid < kTile) {
+                    const float masked = sc > 0.f ? -INFINITY : INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) x[i] = i < valid ? x[i] : -INFINITY;
+                    for (int i = 0; i < 64; ++i) x[i] = i < valid ? x[i] : masked;
                 }
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                float mx;
+                if (sc > 0.f) {
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                const float m_new = fmaxf(m_ref, mx);
+                    for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+                    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                } else {
+                    float m4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) m4[i & 3] = fminf(m4[i & 3], x[i]);
+                    mx = fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
+                }
+                const float m_new = fmaxf(m_ref, mx * sc);
                 const bool rescale = m_new > m_ref + kRescaleThreshold;
                 float alpha = 1.f;
                 if (rescale) {
@@ -751,10 +759,11 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 float2 lb2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 {
                     const float2 negm2 = make_float2(-m_ref, -m_ref);
+                    const float2 sc2 = make_float2(sc, sc);
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float2 d = __fadd2_rn(make_float2(x[2 * i], x[2 * i + 1]), negm2);
+                        const float2 d = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), sc2, negm2);
                         const float a = ptx::ex2(d.x);
                         const float c = ptx::ex2(d.y);
                         pk[i] = pack_bf16x2(a, c);

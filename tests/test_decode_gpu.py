@@ -205,3 +205,17 @@ def test_output_at_a_16_byte_offset_matches_aligned_output():
     torch.cuda.synchronize()
     assert binding.read_error(t["ws"]) == 0
     assert torch.equal(got, t["out"]) and torch.equal(lse, t["lse"])
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("scale", [0.0, -0.05, 0.3])
+def test_zero_negative_and_large_scales(kernel, scale):
+    """softmax_scale is any finite number: 0 weighs every token alike, a
+    negative scale favours the lowest scores; partial last pages must still
+    mask their tail tokens."""
+    w = make_workload("scales", 3, 128, [700, 65, 1], seed=57, extra_blocks=2, num_kv_splits=1)
+    w.softmax_scale = scale
+    got, lse, _, _ = run_decode(w, force_simt=_force(kernel))
+    ref_out, ref_lse = oracle_rows(w, range(w.batch))
+    assert_out_close(got, ref_out, f"scale {scale}", value_abs_max(w, range(w.batch)))
+    assert_lse_close(lse, ref_lse, f"scale {scale} lse")
