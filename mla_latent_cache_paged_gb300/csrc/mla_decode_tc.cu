@@ -736,13 +736,15 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 if (sc > 0.f) {
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
-                    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    for (int i = 0; i < 64; i += 2)
+                        m4[(i >> 1) & 3] = ptx::fmax3(m4[(i >> 1) & 3], x[i], x[i + 1]);
+                    mx = ptx::fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
                 } else {
                     float m4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) m4[i & 3] = fminf(m4[i & 3], x[i]);
-                    mx = fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
+                    for (int i = 0; i < 64; i += 2)
+                        m4[(i >> 1) & 3] = ptx::fmin3(m4[(i >> 1) & 3], x[i], x[i + 1]);
+                    mx = ptx::fmin3(m4[0], m4[1], fminf(m4[2], m4[3]));
                 }
                 const float m_new = fmaxf(m_ref, mx * sc);
                 const bool rescale = m_new > m_ref + kRescaleThreshold;
