@@ -219,3 +219,18 @@ def test_zero_negative_and_large_scales(kernel, scale):
     ref_out, ref_lse = oracle_rows(w, range(w.batch))
     assert_out_close(got, ref_out, f"scale {scale}", value_abs_max(w, range(w.batch)))
     assert_lse_close(lse, ref_lse, f"scale {scale} lse")
+
+
+@pytest.mark.parametrize("num_sms,splits", [(4, 5), (6, 3), (2, 8)])
+def test_split_walk_over_many_items(num_sms, splits):
+    """Few CTA pairs walk long runs of (request, split) items: runs change
+    request mid-way, consecutive splits of one request share its staged q,
+    and short requests leave empty splits behind (LSE -inf only)."""
+    lens = [1, 700, 64, 2000, 65, 0, 300, 129]
+    w = make_workload("walk", len(lens), 128, lens, seed=61 + num_sms, extra_blocks=2,
+                      num_kv_splits=splits)
+    got, lse, plan, _ = run_decode(w, num_kv_splits=splits, num_sms=num_sms)
+    assert plan.grid_ctas == 2 * min(len(lens) * splits, num_sms // 2)
+    ref_out, ref_lse = oracle_rows(w, range(w.batch))
+    assert_out_close(got, ref_out, "split walk", value_abs_max(w, range(w.batch)))
+    assert_lse_close(lse, ref_lse, "split walk lse")
