@@ -66,7 +66,15 @@ constexpr int kOffV = 5 * 16384;               // V ring: 2 pages
 constexpr int kOffK = kOffV + 2 * kVBytes;     // K ring: 2 pages
 constexpr int kOffBar = kOffK + 2 * kKBytes;   // 229,376
 constexpr int kOffPfx = kOffBar + 256;         // page offsets of the balanced schedule
-constexpr int kSmemBytes = kOffPfx + (kMaxBalancedBatch + 4) * 4;   // base is 1 KB aligned
+// UMMA descriptors of every score-MMA operand, built once by the score warp:
+// q's five shared-memory blocks (4 K-steps each), then per ring slot the
+// five K-ring and four value blocks (4 K-steps each).
+constexpr int kDescA = 5 * 4;
+constexpr int kDescSlot = 9 * 4;
+constexpr int kOffDesc = kOffPfx + (kMaxBalancedBatch + 4) * 4;
+constexpr int kSmemBytes = kOffDesc + (kDescA + 2 * kDescSlot) * 8;   // base is 1 KB aligned
+static_assert(kOffDesc % 16 == 0, "descriptor table alignment");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemQ = 0;     // 128 columns: q dims 0..255 as bf16 pairs (A operand)
@@ -246,6 +254,7 @@ struct MmaWarpArgs {
     uint32_t tmem, sbase;
     TcBars* bars;
     int32_t* status;
+    unsigned char* smem;
 };
 
 // Slow path of warp_wait, out of line. Called by the whole warp; returns
@@ -293,19 +302,20 @@ __device__ __forceinline__ uint64_t desc_vmn(uint32_t addr) {
     return ptx::desc_sw128(addr, kBlockBytes, 1024);   // MN-major: 64-col blocks, 8-token groups
 }
 
-// Four score MMAs (K = 64 dims) of dim block KB against the 64 x 64 block at
-// shared-memory address bblk. Called by one elected lane. With bar != 0 the
+// Four score MMAs (K = 64 dims) of dim block KB against the 64 x 64 block
+// whose four K-step descriptors are at bdesc (q's shared-memory blocks' at
+// desc). Called by one elected lane. With bar != 0 the
 // block also tests the mbarrier phase (bar, parity) without blocking, before
 // its first MMA, and reads the answer after its fourth (returned).
 template <int KB>
-__device__ __forceinline__ uint32_t score_block(uint32_t d, uint32_t tmem, uint32_t qs,
-                                                uint32_t bblk, bool first, uint32_t bar = 0,
-                                                uint32_t parity = 0) {
+__device__ __forceinline__ uint32_t score_block(uint32_t d, uint32_t tmem, const uint64_t* desc,
+                                                const uint64_t* bdesc, bool first,
+                                                uint32_t bar = 0, uint32_t parity = 0) {
     constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(kTile, false);
     const uint32_t acc0 = first ? 0u : 1u;
-    uint64_t bd[4];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) bd[kk] = desc_kmajor(bblk + uint32_t(kk * 32));
+    const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(bdesc);
+    const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(bdesc + 2);
+    const uint64_t bd[4] = {b01.x, b01.y, b23.x, b23.y};
     if (KB < kQTmemBlocks) {
         const uint32_t at = tmem + kTmemQ + uint32_t(KB * 32);
         if (bar != 0)
@@ -315,10 +325,10 @@ __device__ __forceinline__ uint32_t score_block(uint32_t d, uint32_t tmem, uint3
         for (int kk = 0; kk < 4; ++kk)
             ptx::mma_ts(d, at + uint32_t(kk * 8), bd[kk], idesc_qk, kk == 0 ? acc0 : 1u);
     } else {
-        const uint32_t qa = qs + uint32_t((KB - kQTmemBlocks) * 16384);
-        uint64_t ad[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) ad[kk] = desc_kmajor(qa + uint32_t(kk * 32));
+        const uint64_t* ad4 = desc + (KB - kQTmemBlocks) * 4;
+        const ulonglong2 a01 = *reinterpret_cast<const ulonglong2*>(ad4);
+        const ulonglong2 a23 = *reinterpret_cast<const ulonglong2*>(ad4 + 2);
+        const uint64_t ad[4] = {a01.x, a01.y, a23.x, a23.y};
         if (bar != 0)
             return ptx::mma4_ss_probe(d, ad[0], ad[1], ad[2], ad[3], bd[0], bd[1], bd[2], bd[3],
                                       idesc_qk, acc0, bar, parity);
@@ -341,7 +351,23 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
     const uint32_t b_kfull = b[0], b_kempty = b[1], b_vfull = b[2], b_sfull = b[3],
                    b_pfree = b[4], b_qready = b[5], b_final = b[6];
     const uint32_t tmem = a.tmem;
-    const uint32_t qs = a.sbase + uint32_t(kOffQS);
+    // The descriptor table (the operands' shared-memory addresses never
+    // change): lanes fill it, the elected lane reads it after __syncwarp.
+    uint64_t* desc = reinterpret_cast<uint64_t*>(a.smem + kOffDesc);
+    for (int i = int(threadIdx.x & 31); i < kDescA + 2 * kDescSlot; i += 32) {
+        uint32_t off;
+        if (i < kDescA) {
+            off = uint32_t(kOffQS + (i >> 2) * 16384 + (i & 3) * 32);
+        } else {
+            const int e = i - kDescA, sl = e / kDescSlot, r = e % kDescSlot;
+            const int pos = r >> 2, kk = r & 3;
+            off = pos < kKPerPage
+                      ? uint32_t(kOffK + sl * kKBytes + pos * kBlockBytes + kk * 32)
+                      : uint32_t(kOffV + sl * kVBytes + (pos - kKPerPage) * kBlockBytes + kk * 32);
+        }
+        desc[i] = desc_kmajor(a.sbase + off);
+    }
+    __syncwarp();
     SegmentWalk walk = walk_begin(p, pfx, pair);
     Segment sg;
     int jg = 0;
@@ -378,8 +404,8 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
                     break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + kTmemS + uint32_t(sl * 64);
-                const uint32_t kslot = a.sbase + uint32_t(kOffK + sl * kKBytes);
-                const uint32_t vslot = a.sbase + uint32_t(kOffV + sl * kVBytes);
+                const uint64_t* bk = desc + kDescA + sl * kDescSlot;   // K-ring blocks
+                const uint64_t* bv = bk + kKPerPage * 4;               // value blocks
                 const uint32_t b_vf = b_vfull + 8 * sl;
                 // Page jn (the next one; it may lie in the next segment or not
                 // exist, and then the answers are not used): its K-ring blocks
@@ -387,20 +413,20 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
                 // late as possible (the P.V of page jc-1 finishes about now).
                 const int jn = jc + 1;
                 const uint32_t phn = uint32_t(jn >> 1) & 1u;
-                score_block<k_block(RANK, 0)>(d, tmem, qs, kslot + 0 * kBlockBytes, true);
+                score_block<k_block(RANK, 0)>(d, tmem, desc, bk + 0, true);
                 const uint32_t nk = score_block<k_block(RANK, 1)>(
-                    d, tmem, qs, kslot + 1 * kBlockBytes, false, b_kfull + 8 * (jn & 1), phn);
-                score_block<k_block(RANK, 2)>(d, tmem, qs, kslot + 2 * kBlockBytes, false);
+                    d, tmem, desc, bk + 4, false, b_kfull + 8 * (jn & 1), phn);
+                score_block<k_block(RANK, 2)>(d, tmem, desc, bk + 8, false);
                 const uint32_t vr = score_block<k_block(RANK, 3)>(
-                    d, tmem, qs, kslot + 3 * kBlockBytes, false, b_vf, ph);
-                score_block<k_block(RANK, 4)>(d, tmem, qs, kslot + 4 * kBlockBytes, false);
+                    d, tmem, desc, bk + 12, false, b_vf, ph);
+                score_block<k_block(RANK, 4)>(d, tmem, desc, bk + 16, false);
                 ptx::mma_commit(b_kempty + 8 * sl);
                 if (!vr && !wait_phase(b_vf, ph, a.bars, a.status, kSiteVFull)) break;
-                score_block<4 * RANK + 0>(d, tmem, qs, vslot + 0 * kBlockBytes, false);
-                score_block<4 * RANK + 1>(d, tmem, qs, vslot + 1 * kBlockBytes, false);
-                score_block<4 * RANK + 2>(d, tmem, qs, vslot + 2 * kBlockBytes, false);
+                score_block<4 * RANK + 0>(d, tmem, desc, bv + 0, false);
+                score_block<4 * RANK + 1>(d, tmem, desc, bv + 4, false);
+                score_block<4 * RANK + 2>(d, tmem, desc, bv + 8, false);
                 const uint32_t nf = score_block<4 * RANK + 3>(
-                    d, tmem, qs, vslot + 3 * kBlockBytes, false, b_pfree + 8 * (jn & 1), phn ^ 1u);
+                    d, tmem, desc, bv + 12, false, b_pfree + 8 * (jn & 1), phn ^ 1u);
                 ptx::mma_commit(b_sfull + 8 * sl);
                 const bool more = j + 1 < ntiles;
                 pf_ready = more && nf != 0;
@@ -520,7 +546,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const MmaWarpArgs margs{tmem, sbase, bars, p.status};
+    const MmaWarpArgs margs{tmem, sbase, bars, p.status, smem};
 
     if (!aligned_ok) {
         // nothing runs; the error is recorded
