@@ -321,9 +321,7 @@ __device__ __forceinline__ uint32_t score_block(uint32_t d, uint32_t tmem, const
         if (bar != 0)
             return ptx::mma4_ts_probe(d, at, at + 8, at + 16, at + 24, bd[0], bd[1], bd[2], bd[3],
                                       idesc_qk, acc0, bar, parity);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_ts(d, at + uint32_t(kk * 8), bd[kk], idesc_qk, kk == 0 ? acc0 : 1u);
+        ptx::mma4_ts(d, at, at + 8, at + 16, at + 24, bd[0], bd[1], bd[2], bd[3], idesc_qk, acc0);
     } else {
         const uint64_t* ad4 = desc + (KB - kQTmemBlocks) * 4;
         const ulonglong2 a01 = *reinterpret_cast<const ulonglong2*>(ad4);
@@ -332,9 +330,7 @@ __device__ __forceinline__ uint32_t score_block(uint32_t d, uint32_t tmem, const
         if (bar != 0)
             return ptx::mma4_ss_probe(d, ad[0], ad[1], ad[2], ad[3], bd[0], bd[1], bd[2], bd[3],
                                       idesc_qk, acc0, bar, parity);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_ss(d, ad[kk], bd[kk], idesc_qk, kk == 0 ? acc0 : 1u);
+        ptx::mma4_ss(d, ad[0], ad[1], ad[2], ad[3], bd[0], bd[1], bd[2], bd[3], idesc_qk, acc0);
     }
     return 1u;
 }

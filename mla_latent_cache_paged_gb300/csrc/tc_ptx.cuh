@@ -295,6 +295,41 @@ __device__ __forceinline__ uint32_t mma_ts_probe(uint32_t d_tmem, uint32_t a_tme
     return done;
 }
 
+// Four MMAs into one accumulator, the first with accumulate flag acc0 and
+// the others accumulating (A from TMEM at a0..a3, or from shared memory
+// through descriptors a0..a3; B descriptors b0..b3).
+__device__ __forceinline__ void mma4_ts(uint32_t d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
+                                        uint64_t b3, uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " setp.ne.b32 p, %9, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %8, p;\n"
+        " setp.eq.b32 p, %9, %9;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %8, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %8, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %10, %8, p;\n}\n"
+        ::"r"(d), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b0), "l"(b1), "l"(b2), "r"(idesc),
+          "r"(acc0), "l"(b3)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma4_ss(uint32_t d, uint64_t a0, uint64_t a1, uint64_t a2,
+                                        uint64_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
+                                        uint64_t b3, uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " setp.ne.b32 p, %9, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %8, p;\n"
+        " setp.eq.b32 p, %9, %9;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %8, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %8, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %10, %8, p;\n}\n"
+        ::"r"(d), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "r"(idesc),
+          "r"(acc0), "l"(b3)
+        : "memory");
+}
+
 // Four MMAs into one accumulator (A from TMEM at a0..a3, or from shared
 // memory through descriptors a0..a3; B descriptors b0..b3), the first with
 // accumulate flag acc0, the others accumulating; an mbarrier phase is tested
