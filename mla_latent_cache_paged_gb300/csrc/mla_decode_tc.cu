@@ -7,35 +7,43 @@
 // attends to every token with K = the 576-wide latent entry and V = its first
 // 512 columns. The design is this file's own.
 //
-// Work item = (request, split), handled by two CTAs launched as a cluster so
-// that they run side by side. CTA c owns the value columns [256c, 256c+256)
-// of O; everything else it does on its own, with no traffic between the two:
+// Work is cut into segments (tokens [t_lo, t_hi) of one request): a CTA
+// pair, two CTAs launched as a cluster so that they run side by side, walks
+// its segments in order (the page-balanced schedule: the requests its range
+// of work units touches; the split schedule: a contiguous run of (request,
+// split) items). CTA c owns the value columns [256c, 256c+256) of O;
+// everything else it does on its own, with no traffic between the two:
 //   * Scores: the full tile S = Q K^T for all (up to) 128 heads and the 64
 //     tokens of a page, tcgen05.mma M=128, N=64, K=16 (36 steps). An MMA with
 //     N <= 64 costs the tensor pipe about as much as one with N = 64, so the
-//     score tile is computed in both CTAs at no extra pipe time; that keeps
-//     the softmax local. q's dims 0..255 are the A operand in TMEM, dims
-//     256..575 in shared memory.
+//     score tile is computed in both CTAs; that keeps the softmax local. q's
+//     dims 0..255 are the A operand in TMEM, dims 256..575 in shared memory.
 //   * Each page is TMA-loaded by both CTAs (the second read of a page is
 //     served from L2; each CTA also pulls half of a page four pages ahead
 //     into L2). Its 64-column blocks go to two page rings: this CTA's four
 //     value blocks to a V ring (kept until the P.V MMA of the page), the five
 //     other blocks to a K ring (released once the page's score MMAs finish).
 //   * Softmax: 128 threads, one per head (= TMEM lane), fp32, base 2 with the
-//     scale folded in; the reference max moves only when a page raises it by
-//     more than 8 (log2), so the O rescale (a TMEM read-modify-write) is rare.
-//     The bf16 weights P overwrite the page's scores in TMEM; O is normalised
-//     by the sum of those rounded weights and the LSE keeps the fp32 sum.
+//     scale folded into the weights' FMA; the reference max moves only when a
+//     page raises it by more than 8 (log2), so the O rescale (a TMEM
+//     read-modify-write) is rare. The bf16 weights P overwrite the page's
+//     scores in TMEM; O is normalised by the sum of those rounded weights and
+//     the LSE keeps the fp32 sum.
 //   * O_c[128 x 256] += P[128 x 64] V_c[64 x 256]: P the A operand in TMEM,
 //     V read MN-major from the V ring.
 // Two score buffers in TMEM let the score MMAs of the next page run while the
 // softmax works on the current one.
 //
 // Warp roles: 0 = K-ring loads (and L2 prefetch), 6 = V-ring loads,
-// 1 = score MMAs, 2-5 = softmax, P.V MMAs, O correction and epilogue. The
-// two rings have their own producers, so a page's K blocks never wait behind
-// the previous page's V slot; the softmax warp that finishes a page last
-// issues its P.V MMAs, with no hand-off to another warp. Every wait is bounded: on expiry the kernel
+// 1 = score MMAs (one elected lane per segment), 2-5 = softmax, P.V MMAs, O
+// correction and epilogue. The two rings have their own producers, so a
+// page's K blocks never wait behind the previous page's V slot; the softmax
+// warp that finishes a page last issues its P.V MMAs, with no hand-off to
+// another warp. An issuing thread blocks until the tensor pipe takes each
+// MMA, so the score lane keeps its own instructions few (operand descriptors
+// come from a table built once; four MMAs per asm statement) and tests the
+// barriers it will need inside those statements, waiting only when a test
+// found the phase pending. Every wait is bounded: on expiry the kernel
 // records MLA_ERR_TIMEOUT, lets each role leave its loop, waits (bounded) for
 // its own loads and MMAs, frees TMEM and returns. A block id outside the pool
 // is recorded and loaded from negative rows, which TMA fills with zeros.

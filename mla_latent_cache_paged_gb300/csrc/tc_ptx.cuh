@@ -71,10 +71,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void fence_mbarrier_init_cluster() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -84,29 +80,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// Arrive on a barrier in another CTA of the cluster (address from mapa),
-// releasing this thread's prior writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-                 : "memory");
-}
-
 // Non-blocking test of a phase.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -128,37 +106,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
-// Same, with acquire at cluster scope (the arrivals came from the peer CTA).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// ---------------------------------------------------------------- cluster
-
-__device__ __forceinline__ uint32_t mapa(uint32_t local_smem, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y,
@@ -170,46 +117,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
-// Same load, delivered to the same offset of every CTA in `cta_mask` (their
-// mbarriers at `bar`'s offset receive the byte count).
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, int32_t x,
-                                               int32_t y, uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
-// cluster shared-memory address; completes bytes on a (possibly remote) mbarrier.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
-                                                     uint32_t bytes, uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
-        " [%0], [%1], %2, [%3];" ::"r"(dst_cluster),
-        "r"(src), "r"(bytes), "r"(bar_cluster)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until every committed bulk copy of this thread has read its source.
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 // 32-byte global store (the address must be 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&v)[8]) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(v[0]),
                  "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                  : "memory");
-}
-
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -241,16 +153,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // D[tmem] (+)= A[tmem] * B[smem desc]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -259,40 +161,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
-}
-
-// The same two MMAs, each also testing an mbarrier phase without blocking:
-// the test is issued before the MMA and its answer is read after it, so its
-// latency passes while the issuing thread waits for the pipe to take the MMA.
-// Returns 1 if the phase with `parity` has completed.
-__device__ __forceinline__ uint32_t mma_ss_probe(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate, uint32_t bar,
-                                                 uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p, q;\n mbarrier.test_wait.parity.shared::cta.b64 q, [%6], %7;\n"
-        " setp.ne.b32 p, %5, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, p;\n"
-        " selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(done)
-        : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar), "r"(parity)
-        : "memory");
-    return done;
-}
-
-__device__ __forceinline__ uint32_t mma_ts_probe(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate, uint32_t bar,
-                                                 uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p, q;\n mbarrier.test_wait.parity.shared::cta.b64 q, [%6], %7;\n"
-        " setp.ne.b32 p, %5, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p;\n"
-        " selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(done)
-        : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar), "r"(parity)
-        : "memory");
-    return done;
 }
 
 // Four MMAs into one accumulator, the first with accumulate flag acc0 and
@@ -380,16 +248,6 @@ __device__ __forceinline__ uint32_t mma4_ss_probe(uint32_t d, uint64_t a0, uint6
     return done;
 }
 
-// Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
-// when every prior tcgen05 op of this thread completes.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // Arrive once on a local mbarrier when every prior tcgen05 op of this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -438,18 +296,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
         : "memory");
 }
 
-// 32 lanes x 16 consecutive 32-bit columns; waits for the store.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-        "%13,%14,%15,%16};\n"
-        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15])
-        : "memory");
-}
-
 // Maximum / minimum of three floats in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
@@ -470,33 +316,18 @@ __device__ __forceinline__ float ex2(float x) {
 
 // ------------------------------------------------------- UMMA descriptors
 
-// Shared-memory matrix descriptor (version 1) for a swizzled layout.
-//   K-major operand: 8-row groups of swizzle-width rows, `sbo` bytes apart.
+// Shared-memory matrix descriptor (version 1) for a 128-byte-swizzled layout.
+//   K-major operand: 8-row groups of 128-byte rows, `sbo` bytes apart.
 //   MN-major operand: `lbo` = byte stride between 64-element column blocks,
 //                     `sbo` = byte stride between 8-row groups along K.
-// layout: 2 = 128-byte swizzle, 4 = 64-byte swizzle.
-__device__ __forceinline__ uint64_t desc_swz(uint32_t saddr, uint32_t lbo, uint32_t sbo,
-                                             uint32_t layout) {
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
     d |= uint64_t((saddr & 0x3FFFFu) >> 4);
     d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
     d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
     d |= uint64_t(1) << 46;
-    d |= uint64_t(layout & 7u) << 61;
+    d |= uint64_t(2) << 61;   // 128-byte swizzle
     return d;
-}
-
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return desc_swz(saddr, lbo, sbo, 2);
-}
-
-__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr, uint32_t sbo) {
-    return desc_swz(saddr, 16, sbo, 4);
-}
-
-// Exact 2^k for an integer k; 0 below the normal range.
-__device__ __forceinline__ float pow2i(int k) {
-    return k < -126 ? 0.f : __int_as_float((127 + min(k, 127)) << 23);
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, M = 128.
