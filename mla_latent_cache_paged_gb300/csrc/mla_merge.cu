@@ -1,9 +1,10 @@
 // LSE-weighted merge of split partials (mla_merge_splits).
 //
-// One warp per (request, head) row. The S log-sum-exps are reduced first
-// (max, then the sum of exponentials), giving the merged LSE and one weight
-// per split; the warp then streams the S partial rows of v_dim fp32 values,
-// 16 bytes per lane per load, and writes the weighted sum rounded to bf16.
+// One warp per (request, head) row, or per row and 128-column group when the
+// rows are few. The S log-sum-exps are reduced first (max, then the sum of
+// exponentials), giving the merged LSE and one weight per split; the warp then
+// streams the S partial rows of fp32 values, 16 bytes per lane per load, and
+// writes the weighted sum rounded to bf16.
 // Formula: the merge the vLLM pages call merge_attn_states (mla_attention API
 // docs, "Chunked Prefill"); a zero partial with -inf LSE is the neutral
 // element (neutralize_empty_context_partials).
@@ -19,6 +20,16 @@ namespace {
 constexpr int kMergeThreads = 256;
 constexpr int kRowsPerCta = kMergeThreads / 32;
 
+// Few rows (a small batch with many splits) leave most SMs idle with one warp
+// per row, so the value columns are then cut into 128-wide groups, one per
+// CTA row of the grid: CTA (x, y) covers rows 8x..8x+7 and columns
+// 128y..128y+127, and each warp keeps four partials' loads in flight.
+// Otherwise CTA x covers rows 8x..8x+7 and each warp walks its whole row.
+// Every warp first forms its row's LSE and the S weights; a partial with
+// weight 0 (an empty split) is never read.
+constexpr int kChunkedMergeRows = 2048;   // below this many rows: column groups
+
+template <bool kColumnGroups>
 __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(
         const float* __restrict__ o_part, const float* __restrict__ lse_part, int rows,
         int S, int v_dim, uint16_t* __restrict__ out, float* __restrict__ lse) {
@@ -47,25 +58,58 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(
         for (int s = lane; s < S; s += 32) w[s] = 0.f;
     }
     __syncwarp();
-    if (lane == 0 && lse != nullptr) lse[row] = total;
+    if (lane == 0 && lse != nullptr && blockIdx.y == 0) lse[row] = total;
 
     const float* base = o_part + size_t(row) * S * v_dim;
     uint16_t* dst = out + size_t(row) * v_dim;
-    for (int d = lane * 4; d < v_dim; d += 128) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < S; ++s) {
-            const float ws = w[s];
-            if (ws == 0.f) continue;   // neutral partials (also skips their contents)
-            const float4 v = __ldg(reinterpret_cast<const float4*>(base + size_t(s) * v_dim + d));
-            acc.x = fmaf(ws, v.x, acc.x);
-            acc.y = fmaf(ws, v.y, acc.y);
-            acc.z = fmaf(ws, v.z, acc.z);
-            acc.w = fmaf(ws, v.w, acc.w);
-        }
+    auto store4 = [&](int d, float4 r) {
         uint2 packed;
-        packed.x = uint32_t(f32_to_bf16_bits_rn(acc.x)) | (uint32_t(f32_to_bf16_bits_rn(acc.y)) << 16);
-        packed.y = uint32_t(f32_to_bf16_bits_rn(acc.z)) | (uint32_t(f32_to_bf16_bits_rn(acc.w)) << 16);
+        packed.x = uint32_t(f32_to_bf16_bits_rn(r.x)) | (uint32_t(f32_to_bf16_bits_rn(r.y)) << 16);
+        packed.y = uint32_t(f32_to_bf16_bits_rn(r.z)) | (uint32_t(f32_to_bf16_bits_rn(r.w)) << 16);
         *reinterpret_cast<uint2*>(dst + d) = packed;
+    };
+    if constexpr (kColumnGroups) {
+        const int d = int(blockIdx.y) * 128 + lane * 4;
+        float4 acc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < S; s0 += 4) {
+            float4 v[4];
+            float ws[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int s = s0 + k;
+                ws[k] = s < S ? w[s] : 0.f;
+                v[k] = ws[k] != 0.f
+                           ? __ldg(reinterpret_cast<const float4*>(base + size_t(s) * v_dim + d))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc[k].x = fmaf(ws[k], v[k].x, acc[k].x);
+                acc[k].y = fmaf(ws[k], v[k].y, acc[k].y);
+                acc[k].z = fmaf(ws[k], v[k].z, acc[k].z);
+                acc[k].w = fmaf(ws[k], v[k].w, acc[k].w);
+            }
+        }
+        store4(d, make_float4((acc[0].x + acc[1].x) + (acc[2].x + acc[3].x),
+                              (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y),
+                              (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z),
+                              (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w)));
+    } else {
+        for (int d = lane * 4; d < v_dim; d += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < S; ++s) {
+                const float ws = w[s];
+                if (ws == 0.f) continue;
+                const float4 v = __ldg(reinterpret_cast<const float4*>(base + size_t(s) * v_dim + d));
+                acc.x = fmaf(ws, v.x, acc.x);
+                acc.y = fmaf(ws, v.y, acc.y);
+                acc.z = fmaf(ws, v.z, acc.z);
+                acc.w = fmaf(ws, v.w, acc.w);
+            }
+            store4(d, acc);
+        }
     }
 }
 
@@ -258,9 +302,15 @@ int launch_merge_balanced(const DecodeParams& p, void* stream) {
 int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,
                  int v_dim, uint16_t* out, float* lse, void* stream) {
     if (rows == 0) return 0;
-    dim3 grid((rows + kRowsPerCta - 1) / kRowsPerCta);
-    mla_merge_kernel<<<grid, kMergeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        o_part, lse_part, rows, num_splits, v_dim, out, lse);
+    if (v_dim % 128 != 0) return int(cudaErrorInvalidValue);
+    const dim3 rows_grid((rows + kRowsPerCta - 1) / kRowsPerCta);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (rows < kChunkedMergeRows)
+        mla_merge_kernel<true><<<dim3(rows_grid.x, v_dim / 128), kMergeThreads, 0, st>>>(
+                o_part, lse_part, rows, num_splits, v_dim, out, lse);
+    else
+        mla_merge_kernel<false><<<rows_grid, kMergeThreads, 0, st>>>(
+                o_part, lse_part, rows, num_splits, v_dim, out, lse);
     return int(cudaGetLastError());
 }
 
