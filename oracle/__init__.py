@@ -7,6 +7,10 @@ CUDA library never calls into it and shares no code with it.
 
 from .mla_oracle import (  # noqa: F401
     absorb_query,
+    dcp_combine,
+    dcp_decode_partials,
+    dcp_local_seq_lens,
+    dcp_owner,
     gather_request_latent,
     merge_partials,
     mha_compute_friendly,

@@ -22,6 +22,11 @@ Pins (see ``tests/test_oracle.py``):
   * ``gather_request_latent`` -- golden page-table fixture and permutation.
   * ``mha_compute_friendly`` / ``absorb_query`` / ``up_project`` -- the
     identity between the two computing approaches, plus torch SDPA.
+  * ``dcp_owner`` / ``dcp_local_seq_lens`` -- a hand-worked placement, the
+    per-rank bound the pages print for a shard's length, conservation of
+    tokens; ``dcp_decode_partials`` + ``dcp_combine`` -- equal to the unsplit
+    definition for every world size and interleave tried, and world 1 is the
+    unsplit result itself.
 No function here is "parity unpinned".
 """
 
@@ -229,3 +234,72 @@ def mha_compute_friendly(q_nope, q_pe, kv_c, k_pe, w_uk, w_uv, softmax_scale):
         lse[h] = m + math.log(e.sum())
         out[h] = (e / e.sum()) @ v[:, h, :]
     return out, lse
+
+
+# Decode context parallelism (DCP): every rank holds a shard of every
+# request's tokens, attends over its shard, and the ranks' (out, lse) pairs are
+# combined with the same LSE merge as split-KV (vLLM ``mla_attention`` API
+# docs, ``MLAAttention.forward``: ``forward_mqa`` per rank, then
+# ``dcp_manager.combine`` with the per-rank ``lse``).
+
+def dcp_owner(t, world, interleave):
+    """Rank that holds token ``t`` and the token's index in that rank's shard.
+
+    vLLM ``mla_attention`` API docs, ``MLACommonMetadataBuilder.__init__`` and
+    ``build``: tokens are dealt to the ``world`` ranks in runs of
+    ``cp_kv_cache_interleave_size`` (the local block), so one virtual block of
+    ``interleave * world`` tokens holds one local block per rank. The pages do
+    not print the placement; the reading used is the plain round-robin one:
+    run ``t // interleave`` goes to rank ``run % world`` and lands after the
+    ``run // world`` runs that rank already holds.
+    """
+    run = t // interleave
+    return run % world, (run // world) * interleave + t % interleave
+
+
+def dcp_local_seq_lens(seq_lens, world, interleave):
+    """Tokens of each request on each rank, ``[world, B]``, by counting owners.
+
+    Brute force over every token: ``counts[r, b]`` is the number of
+    ``t < seq_lens[b]`` with ``dcp_owner(t)[0] == r``.
+    """
+    counts = np.zeros((world, len(seq_lens)), dtype=np.int64)
+    for b, seq_len in enumerate(seq_lens):
+        for t in range(int(seq_len)):
+            counts[dcp_owner(t, world, interleave)[0], b] += 1
+    return counts
+
+
+def dcp_decode_partials(q, cache, block_table, seq_lens, softmax_scale, world,
+                        interleave, kv_lora_rank=512):
+    """Per-rank results of DCP decode: ``out [world, B, N, Lkv]`` (each
+    normalised over the rank's own tokens) and ``lse [world, B, N]``.
+
+    Rank ``r`` attends over the tokens ``dcp_owner`` gives it, in the order of
+    their local indices; a rank without tokens of a request gives the merge's
+    neutral element (zero output, ``-inf`` LSE).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    page_size = np.asarray(cache).shape[1]
+    batch, n_heads, _ = q.shape
+    out = np.zeros((world, batch, n_heads, kv_lora_rank), dtype=np.float64)
+    lse = np.full((world, batch, n_heads), -np.inf, dtype=np.float64)
+    for b in range(batch):
+        k_all = gather_request_latent(cache, block_table[b], seq_lens[b], page_size)
+        shards = [[] for _ in range(world)]
+        for t in range(int(seq_lens[b])):
+            r, j = dcp_owner(t, world, interleave)
+            assert j == len(shards[r])
+            shards[r].append(t)
+        for r in range(world):
+            out[r, b], lse[r, b] = _attend_one(q[b], k_all[shards[r]], softmax_scale,
+                                               kv_lora_rank)
+    return out, lse
+
+
+def dcp_combine(out_parts, lse_parts):
+    """Combine the ranks' results: ``out [world, B, N, V]``, ``lse [world, B, N]``
+    -> ``out [B, N, V]``, ``lse [B, N]``; the ``merge_partials`` identity taken
+    over the rank axis."""
+    return merge_partials(np.moveaxis(np.asarray(out_parts), 0, -2),
+                          np.moveaxis(np.asarray(lse_parts), 0, -1))

@@ -12,8 +12,9 @@ import os
 import numpy as np
 import pytest
 
-from oracle import (absorb_query, gather_request_latent, merge_partials,
-                    mha_compute_friendly, mla_decode_reference,
+from oracle import (absorb_query, dcp_combine, dcp_decode_partials,
+                    dcp_local_seq_lens, dcp_owner, gather_request_latent,
+                    merge_partials, mha_compute_friendly, mla_decode_reference,
                     mla_decode_split_partials, split_token_ranges, up_project)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -295,3 +296,80 @@ def test_rope_columns_enter_scores_but_not_values():
     np.testing.assert_array_equal(o3, o4)
     np.testing.assert_array_equal(l3, l4)
     assert o1.shape[-1] == 512
+
+
+# ------------------------------------------------ decode context parallelism
+
+def test_dcp_placement_hand_worked():
+    """Runs of `interleave` tokens dealt round-robin (worked by hand)."""
+    # world 2, interleave 2, 10 tokens: runs 0..4 -> ranks 0,1,0,1,0.
+    got = [dcp_owner(t, 2, 2) for t in range(10)]
+    assert got == [(0, 0), (0, 1), (1, 0), (1, 1), (0, 2), (0, 3),
+                   (1, 2), (1, 3), (0, 4), (0, 5)]
+    # world 3, interleave 1 (one token per run), 7 tokens.
+    got = [dcp_owner(t, 3, 1) for t in range(7)]
+    assert got == [(0, 0), (1, 0), (2, 0), (0, 1), (1, 1), (2, 1), (0, 2)]
+    # world 1 keeps every token where it was.
+    assert all(dcp_owner(t, 1, 4) == (0, t) for t in range(9))
+    np.testing.assert_array_equal(dcp_local_seq_lens([10, 7, 0], 2, 2),
+                                  [[6, 4, 0], [4, 3, 0]])
+
+
+def test_dcp_local_lengths_bound_and_conservation():
+    """Every token is on exactly one rank, local indices are dense, and no
+    shard is longer than the bound the pages print for it: ceil(L / (R * I)) * I
+    (vLLM mla_attention API docs, MLACommonMetadataBuilder.build); rank 0
+    reaches it whenever the last virtual block gives it a whole run."""
+    for world in [1, 2, 3, 4, 8]:
+        for interleave in [1, 2, 16, 64]:
+            lens = [0, 1, 5, 63, 64, 65, 129, 1000, 1031]
+            counts = dcp_local_seq_lens(lens, world, interleave)
+            np.testing.assert_array_equal(counts.sum(axis=0), lens)
+            for b, L in enumerate(lens):
+                bound = -(-L // (world * interleave)) * interleave
+                assert counts[:, b].max() <= bound
+                if L % (world * interleave) == 0 or L % (world * interleave) >= interleave:
+                    assert counts[0, b] == bound
+                seen = [set() for _ in range(world)]
+                for t in range(L):
+                    r, j = dcp_owner(t, world, interleave)
+                    seen[r].add(j)
+                for r in range(world):
+                    assert seen[r] == set(range(counts[r, b]))
+
+
+@pytest.mark.parametrize("world,interleave", [(1, 1), (2, 1), (2, 64), (3, 2), (4, 16)])
+def test_dcp_combine_equals_unsplit(world, interleave):
+    rng = np.random.default_rng(200 + 7 * world + interleave)
+    lens = [1, 3, 64, 65, 300]
+    dense = [rng.standard_normal((L, 576)) for L in lens]
+    cache, table = _paged_from_dense(rng, dense, 64)
+    q = rng.standard_normal((len(lens), 4, 576))
+    scale = 1 / math.sqrt(192)
+    ref_out, ref_lse = mla_decode_reference(q, cache, table, lens, scale)
+    o_r, l_r = dcp_decode_partials(q, cache, table, lens, scale, world, interleave)
+    assert o_r.shape == (world, len(lens), 4, 512) and l_r.shape == (world, len(lens), 4)
+    if world > 1:
+        assert np.isneginf(l_r[:, 0]).any(), "a 1-token request leaves ranks empty"
+    out, lse = dcp_combine(o_r, l_r)
+    if world == 1:
+        np.testing.assert_array_equal(out, ref_out)
+        np.testing.assert_array_equal(lse, ref_lse)
+    np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+
+
+def test_dcp_rank_result_is_attention_over_its_own_tokens():
+    """Rank r's result equals the definition applied to the dense rows it holds."""
+    rng = np.random.default_rng(210)
+    L = 37
+    rows = rng.standard_normal((L, 576))
+    cache, table = _paged_from_dense(rng, [rows], 8)
+    q = rng.standard_normal((1, 3, 576))
+    o_r, l_r = dcp_decode_partials(q, cache, table, [L], 0.1, 3, 2)
+    for r in range(3):
+        mine = [t for t in range(L) if (t // 2) % 3 == r]
+        c1, t1 = _paged_from_dense(rng, [rows[mine]], 8)
+        o, l = mla_decode_reference(q, c1, t1, [len(mine)], 0.1)
+        np.testing.assert_allclose(o_r[r], o, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(l_r[r], l, rtol=1e-13, atol=1e-13)
