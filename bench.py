@@ -239,6 +239,32 @@ def run_reference(args, w, rank):
     }
 
 
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values (the slowest rank's time); x itself at
+    world 1. Every rank must call it."""
+    if world == 1:
+        return x
+    import torch
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def agree_on_steps(steps, world, device):
+    """Rank 0's step count on every rank."""
+    if world == 1:
+        return steps
+    import torch
+    t = torch.tensor([steps], device=device, dtype=torch.int64)
+    torch.distributed.broadcast(t, 0)
+    return int(t.item())
+
+
+def whole_job_rate(units_per_rank_step, world, steps, elapsed_ms):
+    """Units every rank processed, per second of the slowest rank's time."""
+    return units_per_rank_step * world * steps / (elapsed_ms / 1e3)
+
+
 def run_ours(args, w, rank, world):
     import torch
     from mla_latent_cache_paged_gb300 import binding, build
@@ -281,11 +307,7 @@ def run_ours(args, w, rank, world):
             step()
         torch.cuda.synchronize()
         per = (time.perf_counter() - t0) / 5
-        steps = int(min(20000, max(20, 3.0 / max(per, 1e-6))))
-        if world > 1:
-            t = torch.tensor([steps], device=dev)
-            torch.distributed.broadcast(t, 0)
-            steps = int(t.item())
+        steps = agree_on_steps(int(min(20000, max(20, 3.0 / max(per, 1e-6)))), world, dev)
 
     sampler = ClockSampler(dev.index) if rank == 0 else None
     barrier()
@@ -301,10 +323,7 @@ def run_ours(args, w, rank, world):
     barrier()
     elapsed_ms = start.elapsed_time(end)
     clocks = sampler.stop() if sampler else None
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     status = binding.read_error(ws)
     if status != 0:
         raise RuntimeError(f"device status after timing: {binding.status_string(status)}")
@@ -361,17 +380,14 @@ def run_ours(args, w, rank, world):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     if rank != 0:
         return None
 
     units = w.total_tokens * w.num_heads
     ms_per_step = elapsed_ms / steps
-    value = units * world * steps / (elapsed_ms / 1e3)
+    value = whole_job_rate(units, world, steps, elapsed_ms)
     nbytes, flops = algorithmic_work(w)
     peaks, peak_kind = load_peaks()
     t_s = ms_per_step / 1e3
@@ -412,7 +428,7 @@ def run_ours(args, w, rank, world):
         },
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks,
-        "e2e": {"value": units * world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+        "e2e": {"value": whole_job_rate(units, world, e2e_steps, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": q.numel() * 2 + table.numel() * 4 + lens.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
                 "ms_per_step": e2e_ms / e2e_steps,

@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MLA_DECODE_ABI_VERSION 3
+#define MLA_DECODE_ABI_VERSION 4
 
 /* Status codes. */
 #define MLA_OK                 0
@@ -242,6 +242,46 @@ int mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q, const void*
  */
 int mla_merge_splits(const float* o_part, const float* lse_part, int batch, int num_heads,
                      int num_splits, int v_dim, void* out, float* lse, void* stream);
+
+/*
+ * Decode context parallelism (DCP): each of `world` ranks holds a shard of
+ * every request's cached tokens, runs mla_decode over its shard (with its own
+ * block table and the shard lengths below as seq_lens), and the ranks'
+ * (out, lse) pairs, once gathered, are combined. vLLM mla_attention API docs,
+ * MLAAttention.forward (forward_mqa per rank, then dcp_manager.combine with
+ * the returned lse) and MLACommonMetadataBuilder (cp_kv_cache_interleave_size
+ * as the local block, dcp_local_seq_lens as the rank's seq_lens).
+ *
+ * mla_dcp_local_seq_lens -- host only, no device work.
+ * Token t of a request belongs to rank (t / interleave) % world, at index
+ * (t / (interleave * world)) * interleave + t % interleave of that rank's
+ * shard (runs of `interleave` tokens dealt round-robin). Writes, for every
+ * request b, the number of its tokens that `rank` holds. Each shard length
+ * is at most ceil(L / (world * interleave)) * interleave.
+ *
+ *   seq_lens_host   host, int32 [batch], every entry >= 0.
+ *   world           >= 1; rank in [0, world); interleave >= 1.
+ *   local_lens_host host, int32 [batch], written.
+ * Returns MLA_ERR_INVALID_ARG for a null pointer, a negative length or
+ * batch, or world / rank / interleave out of range (nothing written).
+ */
+int mla_dcp_local_seq_lens(const int32_t* seq_lens_host, int batch, int world, int rank,
+                           int interleave, int32_t* local_lens_host);
+
+/*
+ * mla_dcp_combine -- combine the ranks' decode results, rank-major as an
+ * all-gather over ranks leaves them:
+ *     out_parts  device, bf16 [world, B, N, v_dim] (each rank's mla_decode out)
+ *     lse_parts  device, fp32 [world, B, N] (each rank's mla_decode lse)
+ * into out (bf16 [B, N, v_dim]) and lse (fp32 [B, N], or NULL) with the merge
+ * identity of mla_merge_splits taken over the rank axis. A rank without
+ * tokens of a request (out 0, lse -inf) carries no weight. Same argument
+ * rules as mla_merge_splits (1 <= world <= 1024, v_dim a multiple of 8 in
+ * [8, 2048]; out_parts and out 8-byte aligned); one kernel launch on
+ * `stream`, no synchronisation.
+ */
+int mla_dcp_combine(const void* out_parts, const float* lse_parts, int world, int batch,
+                    int num_heads, int v_dim, void* out, float* lse, void* stream);
 
 /*
  * mla_read_error -- synchronise `stream`, then read and clear the device

@@ -38,7 +38,7 @@ STATUS_BYTES = 8192
 EXPORTED_SYMBOLS = (
     "mla_decode_plan", "mla_workspace_init", "mla_decode", "mla_merge_splits",
     "mla_read_error", "mla_status_string", "mla_abi_version", "mla_debug_gather_pages",
-    "mla_decode_noalloc",
+    "mla_decode_noalloc", "mla_dcp_local_seq_lens", "mla_dcp_combine",
 )
 
 
@@ -100,6 +100,8 @@ def load_library(path=None):
     lib.mla_debug_gather_pages.argtypes = [vp, i64, vp, vp, i32, i32, i32, vp, vp, sz, vp]
     lib.mla_decode_noalloc.argtypes = [ctypes.POINTER(MlaDecodePlan), vp, vp, i64, vp, vp, f32, vp,
                                        vp, vp, vp]
+    lib.mla_dcp_local_seq_lens.argtypes = [vp, i32, i32, i32, i32, vp]
+    lib.mla_dcp_combine.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
     for name in EXPORTED_SYMBOLS:
         if name not in ("mla_status_string",):
             getattr(lib, name).restype = ctypes.c_int
@@ -243,6 +245,37 @@ def mla_merge_splits(o_part, lse_part, *, out=None, lse=None, return_lse=True, s
     rc = load_library().mla_merge_splits(_ptr(o_part), _ptr(lse_part), B, N, S, V, _ptr(out),
                                          _ptr(lse), _stream_ptr(stream))
     _check(rc, "mla_merge_splits")
+    return out, lse
+
+
+def dcp_local_seq_lens(seq_lens_host, world, rank, interleave):
+    """Tokens of each request on ``rank`` of ``world`` (runs of ``interleave``
+    tokens dealt round-robin): int32 numpy ``[B]``, computed on the host."""
+    import numpy as np
+    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    local = np.empty_like(lens)
+    rc = load_library().mla_dcp_local_seq_lens(
+        ctypes.c_void_p(lens.ctypes.data), int(lens.size), int(world), int(rank),
+        int(interleave), ctypes.c_void_p(local.ctypes.data))
+    _check(rc, "mla_dcp_local_seq_lens")
+    return local
+
+
+def mla_dcp_combine(out_parts, lse_parts, *, out=None, lse=None, return_lse=True, stream=None):
+    """Combine the ranks' results, bf16 ``[R,B,N,V]`` / fp32 ``[R,B,N]`` ->
+    bf16 ``[B,N,V]``, fp32 ``[B,N]``."""
+    import torch
+    R, B, N, V = out_parts.shape
+    _check_tensor(out_parts, "out_parts", torch.bfloat16)
+    _check_tensor(lse_parts, "lse_parts", torch.float32, (R, B, N))
+    if out is None:
+        out = torch.empty((B, N, V), dtype=torch.bfloat16, device=out_parts.device)
+    _check_tensor(out, "out", torch.bfloat16, (B, N, V))
+    if lse is None and return_lse:
+        lse = torch.empty((B, N), dtype=torch.float32, device=out_parts.device)
+    rc = load_library().mla_dcp_combine(_ptr(out_parts), _ptr(lse_parts), R, B, N, V, _ptr(out),
+                                        _ptr(lse), _stream_ptr(stream))
+    _check(rc, "mla_dcp_combine")
     return out, lse
 
 

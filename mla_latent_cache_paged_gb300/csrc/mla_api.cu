@@ -96,6 +96,22 @@ extern "C" int mla_merge_splits(const float* o_part, const float* lse_part, int 
                                     static_cast<uint16_t*>(out), lse, stream));
 }
 
+extern "C" int mla_dcp_combine(const void* out_parts, const float* lse_parts, int world,
+                               int batch, int num_heads, int v_dim, void* out, float* lse,
+                               void* stream) {
+    if (batch < 0 || num_heads < 0 || world < 1 || world > kMaxMergeSplits)
+        return MLA_ERR_INVALID_ARG;
+    if (v_dim < 8 || v_dim > 2048 || v_dim % 8 != 0) return MLA_ERR_UNSUPPORTED;
+    if (batch == 0 || num_heads == 0) return MLA_OK;
+    if (!out_parts || !lse_parts || !out) return MLA_ERR_INVALID_ARG;
+    if (!aligned(out_parts, 8) || !aligned(lse_parts, 4) || !aligned(out, 8) ||
+        (lse && !aligned(lse, 4)))
+        return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_rank_combine(static_cast<const uint16_t*>(out_parts), lse_parts,
+                                           world, batch * num_heads, v_dim,
+                                           static_cast<uint16_t*>(out), lse, stream));
+}
+
 extern "C" int mla_read_error(void* workspace, int* device_status, void* stream) {
     if (!workspace || !device_status) return MLA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

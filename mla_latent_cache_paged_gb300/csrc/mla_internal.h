@@ -65,6 +65,10 @@ int launch_decode_simt(const DecodeParams& p, void* stream);
 int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream);
 int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,
                  int v_dim, uint16_t* out, float* lse, void* stream);
+// Combine of per-rank results in rank-major layout: bf16 [world, rows, v_dim]
+// and fp32 [world, rows] -> bf16 [rows, v_dim], fp32 [rows].
+int launch_rank_combine(const uint16_t* out_parts, const float* lse_parts, int world, int rows,
+                        int v_dim, uint16_t* out, float* lse, void* stream);
 int launch_merge_balanced(const DecodeParams& p, void* stream);
 int launch_gather(const uint16_t* cache, int64_t num_blocks, const int32_t* block_table,
                   const int32_t* seq_lens, int batch, int max_blocks, int dst_max_tokens,

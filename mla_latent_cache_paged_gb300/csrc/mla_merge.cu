@@ -26,22 +26,52 @@ constexpr int kRowsPerCta = kMergeThreads / 32;
 // 128y..128y+127, and each warp keeps four partials' loads in flight.
 // Otherwise CTA x covers rows 8x..8x+7 and each warp walks its whole row.
 // Every warp first forms its row's LSE and the S weights; a partial with
-// weight 0 (an empty split) is never read.
+// weight 0 (an empty split, a rank without tokens) is never read.
+//
+// Partial s of row r starts at o_part + r * o_row + s * o_split (elements,
+// multiples of 4) and its LSE is lse_part[r * l_row + s * l_split]: the split
+// schedule's [rows, S, v_dim] and the context-parallel [S, rows, v_dim] are
+// both such layouts. The partials are fp32 or bf16 (TP = uint16_t).
 constexpr int kChunkedMergeRows = 2048;   // below this many rows: column groups
 
-template <bool kColumnGroups>
-__global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(
-        const float* __restrict__ o_part, const float* __restrict__ lse_part, int rows,
-        int S, int v_dim, uint16_t* __restrict__ out, float* __restrict__ lse) {
+struct MergeArgs {
+    const float* lse_part;
+    int rows, S, v_dim;
+    int64_t o_row, o_split, l_row, l_split;
+    uint16_t* out;
+    float* lse;
+};
+
+__device__ __forceinline__ float4 load_partial4(const float* p) {
+    return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+__device__ __forceinline__ float4 load_partial4(const uint16_t* p) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
+__device__ __forceinline__ void store_bf16x4(uint16_t* p, float4 r) {
+    uint2 packed;
+    packed.x = uint32_t(f32_to_bf16_bits_rn(r.x)) | (uint32_t(f32_to_bf16_bits_rn(r.y)) << 16);
+    packed.y = uint32_t(f32_to_bf16_bits_rn(r.z)) | (uint32_t(f32_to_bf16_bits_rn(r.w)) << 16);
+    *reinterpret_cast<uint2*>(p) = packed;
+}
+
+template <typename TP, bool kColumnGroups>
+__global__ void __launch_bounds__(kMergeThreads, 4) mla_merge_kernel(const TP* __restrict__ o_part,
+                                                                   const MergeArgs a) {
     __shared__ float weights[kRowsPerCta][kMaxMergeSplits];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * kRowsPerCta + warp;
-    if (row >= rows) return;
+    if (row >= a.rows) return;
+    const int S = a.S;
 
-    const float* ls = lse_part + size_t(row) * S;
+    const float* ls = a.lse_part + row * a.l_row;
     float m = -INFINITY;
-    for (int s = lane; s < S; s += 32) m = fmaxf(m, ls[s]);
+    for (int s = lane; s < S; s += 32) m = fmaxf(m, ls[s * a.l_split]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
 
@@ -49,27 +79,22 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(
     float total = -INFINITY;
     if (m != -INFINITY) {
         float z = 0.f;
-        for (int s = lane; s < S; s += 32) z += expf(ls[s] - m);
+        for (int s = lane; s < S; s += 32) z += expf(ls[s * a.l_split] - m);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         total = m + logf(z);
-        for (int s = lane; s < S; s += 32) w[s] = expf(ls[s] - total);
+        for (int s = lane; s < S; s += 32) w[s] = expf(ls[s * a.l_split] - total);
     } else {
         for (int s = lane; s < S; s += 32) w[s] = 0.f;
     }
     __syncwarp();
-    if (lane == 0 && lse != nullptr && blockIdx.y == 0) lse[row] = total;
+    if (lane == 0 && a.lse != nullptr && blockIdx.y == 0) a.lse[row] = total;
 
-    const float* base = o_part + size_t(row) * S * v_dim;
-    uint16_t* dst = out + size_t(row) * v_dim;
-    auto store4 = [&](int d, float4 r) {
-        uint2 packed;
-        packed.x = uint32_t(f32_to_bf16_bits_rn(r.x)) | (uint32_t(f32_to_bf16_bits_rn(r.y)) << 16);
-        packed.y = uint32_t(f32_to_bf16_bits_rn(r.z)) | (uint32_t(f32_to_bf16_bits_rn(r.w)) << 16);
-        *reinterpret_cast<uint2*>(dst + d) = packed;
-    };
+    const TP* base = o_part + row * a.o_row;
+    uint16_t* dst = a.out + size_t(row) * a.v_dim;
     if constexpr (kColumnGroups) {
         const int d = int(blockIdx.y) * 128 + lane * 4;
+        if (d >= a.v_dim) return;
         float4 acc[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -80,9 +105,8 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(
             for (int k = 0; k < 4; ++k) {
                 const int s = s0 + k;
                 ws[k] = s < S ? w[s] : 0.f;
-                v[k] = ws[k] != 0.f
-                           ? __ldg(reinterpret_cast<const float4*>(base + size_t(s) * v_dim + d))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[k] = ws[k] != 0.f ? load_partial4(base + s * a.o_split + d)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -92,25 +116,40 @@ __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(
                 acc[k].w = fmaf(ws[k], v[k].w, acc[k].w);
             }
         }
-        store4(d, make_float4((acc[0].x + acc[1].x) + (acc[2].x + acc[3].x),
+        store_bf16x4(dst + d, make_float4((acc[0].x + acc[1].x) + (acc[2].x + acc[3].x),
                               (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y),
                               (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z),
                               (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w)));
     } else {
-        for (int d = lane * 4; d < v_dim; d += 128) {
+        for (int d = lane * 4; d < a.v_dim; d += 128) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < S; ++s) {
+            const TP* p = base + d;
+            for (int s = 0; s < S; ++s, p += a.o_split) {
                 const float ws = w[s];
                 if (ws == 0.f) continue;
-                const float4 v = __ldg(reinterpret_cast<const float4*>(base + size_t(s) * v_dim + d));
+                const float4 v = load_partial4(p);
                 acc.x = fmaf(ws, v.x, acc.x);
                 acc.y = fmaf(ws, v.y, acc.y);
                 acc.z = fmaf(ws, v.z, acc.z);
                 acc.w = fmaf(ws, v.w, acc.w);
             }
-            store4(d, acc);
+            store_bf16x4(dst + d, acc);
         }
     }
+}
+
+template <typename TP>
+int launch_merge_strided(const TP* o_part, const MergeArgs& a, cudaStream_t st) {
+    if (a.rows == 0) return 0;
+    if (a.v_dim % 4 != 0 || a.o_row % 4 != 0 || a.o_split % 4 != 0)
+        return int(cudaErrorInvalidValue);
+    const dim3 rows_grid((a.rows + kRowsPerCta - 1) / kRowsPerCta);
+    if (a.rows < kChunkedMergeRows)
+        mla_merge_kernel<TP, true>
+                <<<dim3(rows_grid.x, (a.v_dim + 127) / 128), kMergeThreads, 0, st>>>(o_part, a);
+    else
+        mla_merge_kernel<TP, false><<<rows_grid, kMergeThreads, 0, st>>>(o_part, a);
+    return int(cudaGetLastError());
 }
 
 // Merge of the page-balanced schedule: CTA (b, y) handles request b, heads
@@ -301,17 +340,16 @@ int launch_merge_balanced(const DecodeParams& p, void* stream) {
 
 int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,
                  int v_dim, uint16_t* out, float* lse, void* stream) {
-    if (rows == 0) return 0;
-    if (v_dim % 128 != 0) return int(cudaErrorInvalidValue);
-    const dim3 rows_grid((rows + kRowsPerCta - 1) / kRowsPerCta);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (rows < kChunkedMergeRows)
-        mla_merge_kernel<true><<<dim3(rows_grid.x, v_dim / 128), kMergeThreads, 0, st>>>(
-                o_part, lse_part, rows, num_splits, v_dim, out, lse);
-    else
-        mla_merge_kernel<false><<<rows_grid, kMergeThreads, 0, st>>>(
-                o_part, lse_part, rows, num_splits, v_dim, out, lse);
-    return int(cudaGetLastError());
+    const MergeArgs a{lse_part, rows, num_splits, v_dim, int64_t(num_splits) * v_dim, v_dim,
+                      num_splits, 1, out, lse};
+    return launch_merge_strided(o_part, a, static_cast<cudaStream_t>(stream));
+}
+
+int launch_rank_combine(const uint16_t* out_parts, const float* lse_parts, int world, int rows,
+                        int v_dim, uint16_t* out, float* lse, void* stream) {
+    const MergeArgs a{lse_parts, rows, world, v_dim, v_dim, int64_t(rows) * v_dim,
+                      1, rows, out, lse};
+    return launch_merge_strided(out_parts, a, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace mla

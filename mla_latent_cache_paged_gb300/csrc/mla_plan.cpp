@@ -244,6 +244,25 @@ extern "C" int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int r
     return MLA_OK;
 }
 
+extern "C" int mla_dcp_local_seq_lens(const int32_t* seq_lens_host, int batch, int world,
+                                      int rank, int interleave, int32_t* local_lens_host) {
+    if (!seq_lens_host || !local_lens_host || batch < 0 || world < 1 || rank < 0 ||
+        rank >= world || interleave < 1)
+        return MLA_ERR_INVALID_ARG;
+    for (int b = 0; b < batch; ++b)
+        if (seq_lens_host[b] < 0) return MLA_ERR_INVALID_ARG;
+    const int64_t span = int64_t(world) * interleave;   // one virtual block
+    for (int b = 0; b < batch; ++b) {
+        const int64_t L = seq_lens_host[b];
+        // Whole virtual blocks give every rank `interleave` tokens; the last,
+        // partial one is dealt run by run from rank 0.
+        const int64_t tail = L % span - int64_t(rank) * interleave;
+        const int64_t extra = tail <= 0 ? 0 : (tail < interleave ? tail : interleave);
+        local_lens_host[b] = int32_t((L / span) * interleave + extra);
+    }
+    return MLA_OK;
+}
+
 extern "C" const char* mla_status_string(int status) {
     switch (status) {
         case MLA_OK: return "ok";

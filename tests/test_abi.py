@@ -165,6 +165,45 @@ def test_merge_and_gather_reject_bad_arguments(lib):
         binding.MLA_ERR_WORKSPACE
 
 
+def test_dcp_combine_rejects_bad_arguments(lib):
+    fake = ctypes.c_void_p(0x10000)
+    null = ctypes.c_void_p(0)
+    assert lib.mla_dcp_combine(fake, fake, 0, 1, 1, 512, fake, null, null) == \
+        binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_dcp_combine(fake, fake, 2, 1, 1, 500, fake, null, null) == \
+        binding.MLA_ERR_UNSUPPORTED
+    assert lib.mla_dcp_combine(null, fake, 2, 1, 1, 512, fake, null, null) == \
+        binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_dcp_combine(ctypes.c_void_p(0x10004), fake, 2, 1, 1, 512, fake, null,
+                               null) == binding.MLA_ERR_INVALID_ARG
+    assert lib.mla_dcp_combine(null, null, 2, 0, 1, 512, null, null, null) == binding.MLA_OK
+
+
+def test_dcp_local_seq_lens_match_the_oracle_placement():
+    """Host-side shard lengths, bit-exact against counting every token's owner."""
+    from oracle import dcp_local_seq_lens as oracle_counts
+    rng = np.random.default_rng(31)
+    lens = np.concatenate([[0, 1, 2, 63, 64, 65, 127, 128, 129, 4096, 4097],
+                           rng.integers(0, 5000, 20)]).astype(np.int32)
+    for world in [1, 2, 3, 4, 8]:
+        for interleave in [1, 2, 8, 64]:
+            want = oracle_counts(lens, world, interleave)
+            for rank in range(world):
+                got = binding.dcp_local_seq_lens(lens, world, rank, interleave)
+                np.testing.assert_array_equal(got, want[rank])
+
+
+@pytest.mark.parametrize("world,rank,interleave,lens", [
+    (0, 0, 1, [4]), (2, 2, 1, [4]), (2, -1, 1, [4]), (2, 0, 0, [4]), (2, 0, 1, [4, -1])])
+def test_dcp_local_seq_lens_rejects_bad_arguments(lib, world, rank, interleave, lens):
+    arr = np.asarray(lens, dtype=np.int32)
+    out = np.full(len(lens), 99, dtype=np.int32)
+    rc = lib.mla_dcp_local_seq_lens(ctypes.c_void_p(arr.ctypes.data), len(lens), world, rank,
+                                    interleave, ctypes.c_void_p(out.ctypes.data))
+    assert rc == binding.MLA_ERR_INVALID_ARG
+    assert (out == 99).all()
+
+
 def test_status_strings(lib):
     for code in range(-7, 1):
         assert lib.mla_status_string(code)
