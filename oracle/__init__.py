@@ -16,6 +16,8 @@ from .mla_oracle import (  # noqa: F401
     mha_compute_friendly,
     mla_decode_reference,
     mla_decode_split_partials,
+    q_absorb_concat_cache,
     split_token_ranges,
     up_project,
+    v_up_proj,
 )

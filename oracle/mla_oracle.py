@@ -27,6 +27,10 @@ Pins (see ``tests/test_oracle.py``):
     tokens; ``dcp_decode_partials`` + ``dcp_combine`` -- equal to the unsplit
     definition for every world size and interleave tried, and world 1 is the
     unsplit result itself.
+  * ``q_absorb_concat_cache`` / ``v_up_proj`` -- explicit sums over the
+    weights' printed layouts on tiny inputs, a hand-worked cache insert, and
+    the whole decode step (front end, decode, up-projection) equal to the
+    compute-friendly MHA over the cache plus the new token.
 No function here is "parity unpinned".
 """
 
@@ -303,3 +307,45 @@ def dcp_combine(out_parts, lse_parts):
     over the rank axis."""
     return merge_partials(np.moveaxis(np.asarray(out_parts), 0, -2),
                           np.moveaxis(np.asarray(lse_parts), 0, -1))
+
+
+# The steps on either side of the decode (vLLM ``mla_attention`` API docs,
+# ``MLAAttention.forward_impl`` and ``_v_up_proj``; raon-1-mini MLA page,
+# ``_decode_concat_cache`` and the weight preparation after loading).
+
+def q_absorb_concat_cache(q, w_uk_t, kv_c, k_pe, slot_mapping, cache,
+                          qk_nope_head_dim=128):
+    """Decode front end: ``mqa_q [B, N, Lkv + R]`` and the cache after the
+    new tokens' insert.
+
+    ``q [B, N, P + R]`` is split into ``q_nope`` (P) and ``q_pe`` (R);
+    ``ql_nope = bmm(q_nope (N, B, P), W_UK_T (N, P, Lkv))``, transposed back to
+    ``(B, N, Lkv)``, with ``W_UK_T = W_UK.permute(1, 2, 0)`` of the
+    ``(Lkv, N, P)`` weight; ``mqa_q = cat[ql_nope, q_pe]``. Each request's new
+    token ``[kv_c | k_pe]`` is written to row ``slot % page_size`` of block
+    ``slot // page_size`` (the page-to-token reading of the decode); the pages
+    print no rule for padded tokens, and the reading used is vLLM's padding
+    slot id: a negative slot writes nothing. Returns new arrays; the inputs are
+    not modified.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    w_uk = np.transpose(np.asarray(w_uk_t, dtype=np.float64), (2, 0, 1))   # (Lkv, N, P)
+    ql_nope = absorb_query(q[..., :qk_nope_head_dim], w_uk)
+    mqa_q = np.concatenate([ql_nope, q[..., qk_nope_head_dim:]], axis=-1)
+    new_cache = np.array(cache, dtype=np.float64, copy=True)
+    page_size = new_cache.shape[1]
+    kv_c = np.asarray(kv_c, dtype=np.float64)
+    k_pe = np.asarray(k_pe, dtype=np.float64)
+    lkv = kv_c.shape[-1]
+    for b, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        if slot < 0:
+            continue
+        new_cache[slot // page_size, slot % page_size, :lkv] = kv_c[b]
+        new_cache[slot // page_size, slot % page_size, lkv:] = k_pe[b]
+    return mqa_q, new_cache
+
+
+def v_up_proj(x, w_uv):
+    """``out [B, N, V] = bmm(x (N, B, Lkv), W_UV (N, Lkv, V))`` transposed back,
+    with ``W_UV`` the ``(Lkv, N, V)`` weight transposed to ``(N, Lkv, V)``."""
+    return up_project(x, np.transpose(np.asarray(w_uv, dtype=np.float64), (1, 0, 2)))

@@ -15,7 +15,8 @@ import pytest
 from oracle import (absorb_query, dcp_combine, dcp_decode_partials,
                     dcp_local_seq_lens, dcp_owner, gather_request_latent,
                     merge_partials, mha_compute_friendly, mla_decode_reference,
-                    mla_decode_split_partials, split_token_ranges, up_project)
+                    mla_decode_split_partials, q_absorb_concat_cache, split_token_ranges,
+                    up_project, v_up_proj)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -373,3 +374,84 @@ def test_dcp_rank_result_is_attention_over_its_own_tokens():
         o, l = mla_decode_reference(q, c1, t1, [len(mine)], 0.1)
         np.testing.assert_allclose(o_r[r], o, rtol=1e-13, atol=1e-13)
         np.testing.assert_allclose(l_r[r], l, rtol=1e-13, atol=1e-13)
+
+
+# -------------------------------------------- front end and up-projection
+
+def test_q_absorb_against_explicit_sums_over_the_printed_layout():
+    """ql_nope[b, n, l] = sum_p q_nope[b, n, p] * W_UK_T[n, p, l], with W_UK_T
+    (N, P, Lkv) as the page lays it out; q_pe lands after the Lkv columns."""
+    rng = np.random.default_rng(300)
+    B, N, P, R, L = 3, 2, 4, 2, 5
+    q = rng.standard_normal((B, N, P + R))
+    w_uk_t = rng.standard_normal((N, P, L))
+    mqa_q, _ = q_absorb_concat_cache(q, w_uk_t, np.zeros((B, L)), np.zeros((B, R)),
+                                     [-1] * B, np.zeros((1, 4, L + R)), qk_nope_head_dim=P)
+    assert mqa_q.shape == (B, N, L + R)
+    for b in range(B):
+        for n in range(N):
+            for l in range(L):
+                want = sum(q[b, n, p] * w_uk_t[n, p, l] for p in range(P))
+                assert abs(mqa_q[b, n, l] - want) < 1e-12
+            np.testing.assert_array_equal(mqa_q[b, n, L:], q[b, n, P:])
+
+
+def test_v_up_proj_against_explicit_sums_over_the_printed_layout():
+    """out[b, n, v] = sum_l x[b, n, l] * W_UV[n, l, v], W_UV laid out (N, Lkv, V)."""
+    rng = np.random.default_rng(301)
+    B, N, L, V = 2, 3, 5, 4
+    x = rng.standard_normal((B, N, L))
+    w_uv = rng.standard_normal((N, L, V))
+    out = v_up_proj(x, w_uv)
+    for b in range(B):
+        for n in range(N):
+            for v in range(V):
+                want = sum(x[b, n, l] * w_uv[n, l, v] for l in range(L))
+                assert abs(out[b, n, v] - want) < 1e-12
+
+
+def test_cache_insert_hand_worked():
+    """Slots 3, padding (-1) and 8 + 5 with 8-row pages: rows (0, 3) and
+    (1, 5) take [kv_c | k_pe]; every other row keeps its bits."""
+    rng = np.random.default_rng(302)
+    cache = rng.standard_normal((3, 8, 6))
+    kv_c = np.arange(12.0).reshape(3, 4)
+    k_pe = -np.arange(6.0).reshape(3, 2) - 1
+    q = rng.standard_normal((3, 1, 4 + 2))
+    _, new = q_absorb_concat_cache(q, rng.standard_normal((1, 4, 4)), kv_c, k_pe,
+                                   [3, -1, 13], cache, qk_nope_head_dim=4)
+    np.testing.assert_array_equal(new[0, 3], [0, 1, 2, 3, -1, -2])
+    np.testing.assert_array_equal(new[1, 5], [8, 9, 10, 11, -5, -6])
+    keep = np.ones(cache.shape[:2], dtype=bool)
+    keep[0, 3] = keep[1, 5] = False
+    np.testing.assert_array_equal(new[keep], cache[keep])
+    assert not np.array_equal(new, cache)
+
+
+def test_decode_step_with_front_end_equals_compute_friendly_mha():
+    """Front end (absorb, concat, insert of the new token) -> decode over the
+    cache, now holding the new token -> up-projection equals MHA over the
+    cached tokens plus the new one, with the weights in the layouts the page
+    prepares: W_UK_T = W_UK.permute(1, 2, 0), W_UV transposed to (N, Lkv, V)."""
+    rng = np.random.default_rng(303)
+    n, p, r, v, lkv, L, ps = 4, 16, 8, 16, 32, 21, 8
+    w_uk = rng.standard_normal((lkv, n, p)) / math.sqrt(lkv)
+    w_uv = rng.standard_normal((lkv, n, v)) / math.sqrt(lkv)
+    kv_c = rng.standard_normal((L + 1, lkv))          # the last row is the new token's
+    k_pe = rng.standard_normal((L + 1, r))
+    q = rng.standard_normal((1, n, p + r))
+    scale = (p + r) ** -0.5
+    ref_out, ref_lse = mha_compute_friendly(q[0, :, :p], q[0, :, p:], kv_c, k_pe, w_uk, w_uv,
+                                            scale)
+
+    cache, table = _paged_from_dense(rng, [np.concatenate([kv_c[:L], k_pe[:L]], axis=1)], ps,
+                                     extra_blocks=2)
+    # The new token goes to row L % ps of the request's last page (L = 21:
+    # page 2 of 3, which already holds rows 16..20).
+    slot = int(table[0, L // ps]) * ps + L % ps
+    mqa_q, cache2 = q_absorb_concat_cache(q, np.transpose(w_uk, (1, 2, 0)), kv_c[L:], k_pe[L:],
+                                          [slot], cache, qk_nope_head_dim=p)
+    lat, lse = mla_decode_reference(mqa_q, cache2, table, [L + 1], scale, kv_lora_rank=lkv)
+    out = v_up_proj(lat, np.transpose(w_uv, (1, 0, 2)))[0]
+    np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse[0], ref_lse, rtol=1e-12, atol=1e-13)
