@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--stage", choices=["decode"] + sorted(STAGES), default="decode",
+                    help="time one of the steps around the decode instead (at the workload's "
+                         "batch and head count)")
     return ap.parse_args()
 
 
@@ -236,6 +239,117 @@ def run_reference(args, w, rank):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{per_step_reqs} whole requests per step, numpy float64"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+STAGES = {
+    "front_end": "MLA decode front end (q absorption by W_UK_T, q_pe concat, latent cache "
+                 "insert), one launch",
+    "v_up_proj": "MLA up-projection of the decode output by W_UV, one launch",
+}
+
+
+def stage_work(stage, batch, heads):
+    """Algorithmic bytes and flops of one call of a step around the decode.
+
+    front end: W_UK_T (N*128*512 bf16) + q (B*N*192) + mqa_q written
+    (B*N*576) + the new tokens' kv_c and k_pe read and written to the cache
+    (2 * B * 576) + slot ids (8 B each). Up-projection: x (B*N*512) + W_UV
+    (N*512*128) + out (B*N*128). Both: 2 * B * N * 128 * 512 flops.
+    """
+    if stage == "front_end":
+        nbytes = 2 * (heads * 128 * 512 + batch * heads * 192 + batch * heads * 576 +
+                      2 * batch * 576) + 8 * batch
+    else:
+        nbytes = 2 * (batch * heads * 512 + heads * 512 * 128 + batch * heads * 128)
+    return nbytes, 2 * batch * heads * 128 * 512
+
+
+def run_stage(args, stage):
+    """Time one step around the decode through its C-ABI call, with the
+    inputs of several seeded sets rotated so that they exceed L2 twice over."""
+    import torch
+    from mla_latent_cache_paged_gb300 import binding, build
+    from mla_latent_cache_paged_gb300.workloads import HEADLINE, get_workload
+
+    build.build()
+    w = get_workload(args.workload or HEADLINE, with_data=False)
+    B, N = w.batch, w.num_heads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    nbytes, flops = stage_work(stage, B, N)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(2, -(-2 * l2 // nbytes) + 1)
+    gen = torch.Generator(device=dev).manual_seed(20260100)
+
+    def rnd(shape, scale=1.0):
+        return (torch.randn(shape, generator=gen, device=dev) * scale).to(torch.bfloat16)
+
+    ws = binding.new_status_workspace(dev)
+    sets = []
+    if stage == "front_end":
+        blocks = -(-B // 64)
+        cache = rnd((blocks * nsets, 64, 576))
+        for i in range(nsets):
+            slots = (torch.randperm(blocks * 64, generator=gen, device=dev)[:B] +
+                     i * blocks * 64).to(torch.int64)
+            sets.append(dict(q=rnd((B, N, 192)), w=rnd((N, 128, 512), 128 ** -0.5),
+                             kv_c=rnd((B, 512)), k_pe=rnd((B, 64)), slots=slots,
+                             out=torch.empty((B, N, 576), dtype=torch.bfloat16, device=dev)))
+
+        def call(i):
+            t = sets[i % nsets]
+            binding.mla_q_absorb_concat_cache(t["q"], t["w"], t["kv_c"], t["k_pe"], t["slots"],
+                                              cache, workspace=ws, out=t["out"])
+    else:
+        for i in range(nsets):
+            sets.append(dict(x=rnd((B, N, 512)), w=rnd((N, 512, 128), 512 ** -0.5),
+                             out=torch.empty((B, N, 128), dtype=torch.bfloat16, device=dev)))
+
+        def call(i):
+            t = sets[i % nsets]
+            binding.mla_v_up_proj(t["x"], t["w"], workspace=ws, out=t["out"])
+
+    for i in range(max(args.warmup, 3)):
+        call(i)
+    torch.cuda.synchronize()
+    if binding.read_error(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    steps = args.steps if args.steps > 0 else 2000
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if binding.read_error(ws) != 0:
+        raise RuntimeError("device status after timing")
+    ms = e0.elapsed_time(e1) / steps
+    peaks, peak_kind = load_peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {
+        "metric": STAGES[stage] + ": algorithmic bytes / time", "value": achieved,
+        "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{stage}_b{B}_n{N}", "batch": B, "heads": N,
+                   "l2": f"{nsets} input sets rotated ({nsets * nbytes / 1e6:.0f} MB, "
+                         f"more than twice L2), no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "tensor_achieved_tflops": flops / (ms / 1e3) / 1e12,
+                     "tensor_peak_tflops": peaks["bf16_tflops"]},
+        "gpu_launches": steps,
+        "clocks": clocks,
     }
 
 
@@ -447,6 +561,12 @@ def main():
 
     from mla_latent_cache_paged_gb300.workloads import HEADLINE, get_workload
     name = args.workload or HEADLINE
+
+    if args.stage != "decode":
+        if world > 1:
+            raise SystemExit("--stage runs on one GPU")
+        print(json.dumps(run_stage(args, args.stage)), flush=True)
+        return 0
 
     if args.impl == "reference":
         if rank != 0:

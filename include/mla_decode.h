@@ -284,6 +284,56 @@ int mla_dcp_combine(const void* out_parts, const float* lse_parts, int world, in
                     int num_heads, int v_dim, void* out, float* lse, void* stream);
 
 /*
+ * The steps on either side of the decode: per-head batched matmuls on the
+ * tensor cores (vLLM mla_attention API docs, MLAAttention.forward_impl and
+ * _v_up_proj; the weight layouts are the ones the raon-1-mini MLA page
+ * prepares after loading: W_UK_T = W_UK.permute(1, 2, 0), W_UV transposed to
+ * (N, Lkv, V)). Supported shapes: qk_nope_head_dim P = 128, RoPE width R = 64,
+ * kv_lora_rank 512, v_head_dim 128, 1 <= num_heads <= 128, any batch.
+ * Device-detected errors go to the status word of `workspace` (a status
+ * header: device, >= 8192 bytes, 256-byte aligned, zeroed by
+ * mla_workspace_init); read them with mla_read_error. One kernel launch on
+ * `stream` each, no synchronisation. Every device pointer 16-byte aligned
+ * (slot_mapping 8-byte aligned).
+ *
+ * mla_q_absorb_concat_cache -- the decode front end, in one launch
+ * (raon-1-mini page, _decode_concat_cache: query concat fused with the
+ * latent cache insert; RoPE is not applied here: q_pe and k_pe come in
+ * already rotated):
+ *     mqa_q[b, n, 0:512]   = sum_p q[b, n, p] * w_uk_t[n, p, 0:512]   (p < 128)
+ *     mqa_q[b, n, 512:576] = q[b, n, 128:192]
+ *     latent_cache row slot_mapping[b] = [kv_c[b, 0:512] | k_pe[b, 0:64]]
+ *
+ *   q             device, bf16 [B, N, 192] contiguous ([q_nope | q_pe]).
+ *   w_uk_t        device, bf16 [N, 128, 512] contiguous.
+ *   kv_c, k_pe    device, bf16 [B, 512] and [B, 64]: the new tokens' entries.
+ *   slot_mapping  device, int64 [B]: row slot % 64 of block slot / 64 of
+ *                 latent_cache (bf16 [num_blocks, 64, 576]); a negative slot
+ *                 writes nothing (padding); a slot >= num_blocks * 64 is
+ *                 recorded as MLA_ERR_BAD_BLOCK_ID (detail: slot / 64) and not
+ *                 written. Non-negative slots must be distinct. NULL: no
+ *                 insert (kv_c, k_pe, latent_cache unused).
+ *   mqa_q         device, bf16 [B, N, 576], written (the decode's q).
+ * Accumulation in fp32, one rounding to bf16 (nearest even).
+ */
+int mla_q_absorb_concat_cache(const void* q, const void* w_uk_t, const void* kv_c,
+                              const void* k_pe, const int64_t* slot_mapping, void* latent_cache,
+                              int64_t num_blocks, int batch, int num_heads, void* mqa_q,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_v_up_proj -- the up-projection after the decode:
+ *     out[b, n, 0:128] = sum_l x[b, n, l] * w_uv[n, l, 0:128]   (l < 512)
+ *
+ *   x     device, bf16 [B, N, 512] contiguous (mla_decode's out).
+ *   w_uv  device, bf16 [N, 512, 128] contiguous.
+ *   out   device, bf16 [B, N, 128] contiguous, written.
+ * Accumulation in fp32, one rounding to bf16 (nearest even).
+ */
+int mla_v_up_proj(const void* x, const void* w_uv, int batch, int num_heads, void* out,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mla_read_error -- synchronise `stream`, then read and clear the device
  * status word of `workspace`. *device_status receives MLA_OK or the first
  * MLA_ERR_* a kernel recorded since the last read. Returns MLA_ERR_CUDA if

@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "mla_decode_plan", "mla_workspace_init", "mla_decode", "mla_merge_splits",
     "mla_read_error", "mla_status_string", "mla_abi_version", "mla_debug_gather_pages",
     "mla_decode_noalloc", "mla_dcp_local_seq_lens", "mla_dcp_combine",
+    "mla_q_absorb_concat_cache", "mla_v_up_proj",
 )
 
 
@@ -102,6 +103,9 @@ def load_library(path=None):
                                        vp, vp, vp]
     lib.mla_dcp_local_seq_lens.argtypes = [vp, i32, i32, i32, i32, vp]
     lib.mla_dcp_combine.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
+    lib.mla_q_absorb_concat_cache.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp, sz,
+                                              vp]
+    lib.mla_v_up_proj.argtypes = [vp, vp, i32, i32, vp, vp, sz, vp]
     for name in EXPORTED_SYMBOLS:
         if name not in ("mla_status_string",):
             getattr(lib, name).restype = ctypes.c_int
@@ -277,6 +281,56 @@ def mla_dcp_combine(out_parts, lse_parts, *, out=None, lse=None, return_lse=True
                                         _ptr(lse), _stream_ptr(stream))
     _check(rc, "mla_dcp_combine")
     return out, lse
+
+
+def new_status_workspace(device=None, stream=None):
+    """A bare status header (for the calls that need no other workspace)."""
+    import torch
+    ws = torch.empty(STATUS_BYTES, dtype=torch.uint8, device=device or "cuda")
+    _check(load_library().mla_workspace_init(_ptr(ws), STATUS_BYTES, _stream_ptr(stream)),
+           "mla_workspace_init")
+    return ws
+
+
+def mla_q_absorb_concat_cache(q, w_uk_t, kv_c=None, k_pe=None, slot_mapping=None,
+                              latent_cache=None, *, workspace, out=None, stream=None):
+    """Decode front end: ``mqa_q [B, N, 576]`` from ``q [B, N, 192]`` and
+    ``W_UK_T [N, 128, 512]``; with ``slot_mapping`` (int64 ``[B]``) the new
+    tokens' ``[kv_c | k_pe]`` go into ``latent_cache`` in the same launch."""
+    import torch
+    B, N, _ = q.shape
+    _check_tensor(q, "q", torch.bfloat16, (B, N, 192))
+    _check_tensor(w_uk_t, "w_uk_t", torch.bfloat16, (N, 128, 512))
+    num_blocks = 0
+    if slot_mapping is not None:
+        _check_tensor(slot_mapping, "slot_mapping", torch.int64, (B,))
+        _check_tensor(kv_c, "kv_c", torch.bfloat16, (B, 512))
+        _check_tensor(k_pe, "k_pe", torch.bfloat16, (B, 64))
+        _check_tensor(latent_cache, "latent_cache", torch.bfloat16)
+        num_blocks = latent_cache.shape[0]
+    if out is None:
+        out = torch.empty((B, N, 576), dtype=torch.bfloat16, device=q.device)
+    _check_tensor(out, "out", torch.bfloat16, (B, N, 576))
+    rc = load_library().mla_q_absorb_concat_cache(
+        _ptr(q), _ptr(w_uk_t), _ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping), _ptr(latent_cache),
+        num_blocks, B, N, _ptr(out), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(rc, "mla_q_absorb_concat_cache")
+    return out
+
+
+def mla_v_up_proj(x, w_uv, *, workspace, out=None, stream=None):
+    """Up-projection: ``out [B, N, 128]`` from ``x [B, N, 512]`` and ``W_UV [N, 512, 128]``."""
+    import torch
+    B, N, _ = x.shape
+    _check_tensor(x, "x", torch.bfloat16, (B, N, 512))
+    _check_tensor(w_uv, "w_uv", torch.bfloat16, (N, 512, 128))
+    if out is None:
+        out = torch.empty((B, N, 128), dtype=torch.bfloat16, device=x.device)
+    _check_tensor(out, "out", torch.bfloat16, (B, N, 128))
+    rc = load_library().mla_v_up_proj(_ptr(x), _ptr(w_uv), B, N, _ptr(out), _ptr(workspace),
+                                      workspace.numel(), _stream_ptr(stream))
+    _check(rc, "mla_v_up_proj")
+    return out
 
 
 def read_error(workspace, stream=None):

@@ -1,0 +1,367 @@
+// Per-head batched matmuls on either side of the decode, on the tensor cores.
+//
+//   front end  (mla_q_absorb_concat_cache):
+//       ql_nope[b, n, :] = q[b, n, 0:128] . W_UK_T[n]      W_UK_T bf16 [N, 128, 512]
+//       mqa_q[b, n, :]   = [ql_nope[b, n, :] | q[b, n, 128:192]]
+//       cache row `slot_mapping[b]` = [kv_c[b] | k_pe[b]]
+//   up-projection (mla_v_up_proj):
+//       out[b, n, :]     = x[b, n, :] . W_UV[n]            W_UV bf16 [N, 512, 128]
+//
+// vLLM mla_attention API docs, MLAAttention.forward_impl (torch.bmm of
+// (N, B, P) by W_UK_T, then the q concat) and _v_up_proj (torch.bmm by W_UV);
+// raon-1-mini MLA page, _decode_concat_cache (query concat fused with the
+// latent cache insert) and the weight layouts it prepares (W_UK_T =
+// W_UK.permute(1, 2, 0), W_UV transposed to (N, Lkv, V)).
+//
+// CTA (x, n) computes rows 128x..128x+127 (requests) of head n: M = 128
+// batch rows, the whole J-wide result (512 or 128 fp32 columns) accumulated
+// in TMEM, K streamed in 64-wide chunks. A (the activations) is K-major: a
+// TMA box of 128 rows x 64 k at column n * head_stride + 64c of the [B, N *
+// head_stride] view. The weight chunk is MN-major: J / 64 boxes of 64 k-rows
+// x 64 columns of the [N * K, J] view. Both use the 128-byte swizzle.
+// Warp 0 lane 0 loads (a ring of STAGES chunks), warp 1 lane 0 issues
+// tcgen05.mma (M = 128, N = min(J, 256), K = 16), and all four warps read the
+// accumulator back (thread = row), round to bf16 and store. In the front end
+// warps 2-3 copy q_pe and, in the CTAs of head 0, insert the new tokens'
+// latent rows while the MMAs run. Every wait is bounded (MLA_ERR_TIMEOUT);
+// a slot outside the cache is recorded (MLA_ERR_BAD_BLOCK_ID), not written.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+
+#include "mla_device.cuh"
+#include "tc_ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kBmmThreads = 128;
+constexpr int kM = 128;                      // batch rows per CTA
+constexpr int kChunk = 64;                   // K per ring stage
+constexpr int kABytes = kM * kChunk * 2;     // 16 KB
+constexpr int kWBlockBytes = kChunk * 64 * 2;   // one 64 x 64 weight box: 8 KB
+constexpr uint64_t kBmmTimeoutNs = 1000000000ull;
+constexpr uint32_t kBmmSuspendNs = 20000;
+constexpr int kNope = 128;                   // qk_nope_head_dim
+constexpr int kQHead = kNope + kRope;        // q head width (P + R)
+
+enum BmmSite : int32_t { kSiteRingEmpty = 30, kSiteRingFull, kSiteAccFull, kSiteRingDrain };
+
+template <int J, int KD, int STAGES>
+struct BmmShape {
+    static constexpr int kWBytes = (J / 64) * kWBlockBytes;
+    static constexpr int kStageBytes = kABytes + kWBytes;
+    static constexpr int kChunks = KD / kChunk;
+    static constexpr int kPiece = J > 256 ? 256 : J;       // N of one MMA
+    static constexpr int kPieces = J / kPiece;
+    static constexpr int kTmemCols = J < 32 ? 32 : J;
+    static constexpr int kBarOff = STAGES * kStageBytes;   // full[S], empty[S], acc, slot, abort
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;   // + alignment slack
+    static_assert(KD % kChunk == 0 && J % 64 == 0 && J <= 512, "shape");
+    static_assert((J & (J - 1)) == 0, "TMEM allocation is a power of two");
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+struct BmmParams {
+    int batch, heads;
+    int a_head;                  // columns from one head's A to the next (192 or 512)
+    const uint16_t* q;           // front end: q [B, N, 192] (for q_pe)
+    uint16_t* out;               // element (b, n, j) at out + b * out_row + n * out_head + j
+    int64_t out_row;
+    int out_head;
+    const uint16_t* kv_c;        // front end: [B, 512]
+    const uint16_t* k_pe;        // front end: [B, 64]
+    const int64_t* slots;        // front end: [B] or null
+    uint16_t* cache;             // front end: [num_blocks, 64, 576]
+    int64_t num_blocks;
+    int32_t* status;
+};
+
+__device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort,
+                                         int32_t* status, int32_t site, bool ignore_abort) {
+    if (ptx::mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        for (int i = 0; i < 4; ++i)
+            if (ptx::mbar_try_wait_sleep(bar, parity, kBmmSuspendNs)) return true;
+        if (!ignore_abort && *abort != 0) return false;
+        if (ptx::globaltimer() - t0 > kBmmTimeoutNs) {
+            *abort = 1;
+            record_error(status, MLA_ERR_TIMEOUT, site);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void copy16(void* dst, const void* src) {
+    *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+}
+
+template <int J, int KD, int STAGES, bool kFrontEnd>
+__global__ void __launch_bounds__(kBmmThreads, 1)
+mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
+               const __grid_constant__ CUtensorMap tmap_w) {
+    using Sh = BmmShape<J, KD, STAGES>;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t sbase = raw + pad;
+    unsigned char* smem = smem_raw + pad;
+    const uint32_t b_full = sbase + Sh::kBarOff;
+    const uint32_t b_empty = b_full + 8 * STAGES;
+    const uint32_t b_acc = b_empty + 8 * STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::kBarOff + 16 * STAGES + 8);
+    volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n = blockIdx.y;
+    const int m0 = blockIdx.x * kM;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(b_full + 8 * s, 1);
+            ptx::mbar_init(b_empty + 8 * s, 1);
+        }
+        ptx::mbar_init(b_acc, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Sh::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // Producer: chunk c into stage c % STAGES once its previous use is done.
+        int issued = 0;
+        if (ptx::elect_one()) {
+            for (int c = 0; c < Sh::kChunks; ++c) {
+                const int s = c % STAGES;
+                if (c >= STAGES &&
+                    !bmm_wait(b_empty + 8 * s, ((c / STAGES) - 1) & 1, abort, p.status,
+                              kSiteRingEmpty, false))
+                    break;
+                const uint32_t st = sbase + uint32_t(s * Sh::kStageBytes);
+                ptx::mbar_arrive_expect_tx(b_full + 8 * s, Sh::kStageBytes);
+                ptx::tma_load_2d(st, &tmap_a, n * p.a_head + c * kChunk, m0, b_full + 8 * s);
+#pragma unroll
+                for (int jb = 0; jb < J / 64; ++jb)
+                    ptx::tma_load_2d(st + kABytes + uint32_t(jb * kWBlockBytes), &tmap_w, jb * 64,
+                                     n * KD + c * kChunk, b_full + 8 * s);
+                ++issued;
+            }
+            // Copies still in flight (after an abort) land before the CTA exits.
+            for (int c = issued - STAGES < 0 ? 0 : issued - STAGES; c < issued; ++c)
+                bmm_wait(b_full + 8 * (c % STAGES), (c / STAGES) & 1, abort, p.status,
+                         kSiteRingDrain, true);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // MMA issuer.
+        constexpr uint32_t idesc = ptx::idesc_bf16_f32(Sh::kPiece, true);
+        if (ptx::elect_one()) {
+            bool ok = true;
+            for (int c = 0; c < Sh::kChunks && ok; ++c) {
+                const int s = c % STAGES;
+                ok = bmm_wait(b_full + 8 * s, (c / STAGES) & 1, abort, p.status, kSiteRingFull,
+                              false);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const uint32_t a_st = sbase + uint32_t(s * Sh::kStageBytes);
+                const uint32_t w_st = a_st + kABytes;
+                // A: K-major, 16 k = 32 bytes per step; W: MN-major, 16 k-rows
+                // = 2 KB per step, 64-column blocks 8 KB apart.
+                const uint64_t a0 = ptx::desc_sw128(a_st, 16, 1024);
+                const uint64_t a1 = ptx::desc_sw128(a_st + 32, 16, 1024);
+                const uint64_t a2 = ptx::desc_sw128(a_st + 64, 16, 1024);
+                const uint64_t a3 = ptx::desc_sw128(a_st + 96, 16, 1024);
+#pragma unroll
+                for (int pc = 0; pc < Sh::kPieces; ++pc) {
+                    const uint32_t wp = w_st + uint32_t(pc * (Sh::kPiece / 64) * kWBlockBytes);
+                    ptx::mma4_ss(tmem + uint32_t(pc * Sh::kPiece), a0, a1, a2, a3,
+                                 ptx::desc_sw128(wp, kWBlockBytes, 1024),
+                                 ptx::desc_sw128(wp + 2048, kWBlockBytes, 1024),
+                                 ptx::desc_sw128(wp + 4096, kWBlockBytes, 1024),
+                                 ptx::desc_sw128(wp + 6144, kWBlockBytes, 1024), idesc,
+                                 c > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(b_empty + 8 * s);
+            }
+            // Arrives when every MMA issued above has completed (also after an
+            // abort, so the accumulator is idle before TMEM is freed).
+            ptx::mma_commit(b_acc);
+        }
+        __syncwarp();
+    } else if (kFrontEnd) {
+        // q_pe into columns 512..575 of mqa_q, and (head 0 only) the new
+        // tokens' latent rows into the cache.
+        for (int r = threadIdx.x - 64; r < kM; r += 64) {
+            const int b = m0 + r;
+            if (b >= p.batch) break;
+            const uint16_t* src = p.q + (int64_t(b) * p.heads + n) * kQHead + kNope;
+            uint16_t* dst = p.out + b * p.out_row + int64_t(n) * p.out_head + J;
+#pragma unroll
+            for (int i = 0; i < kRope / 8; ++i) copy16(dst + 8 * i, src + 8 * i);
+            if (n == 0 && p.slots != nullptr) {
+                const int64_t slot = p.slots[b];
+                if (slot < 0) continue;
+                if (slot >= p.num_blocks * kPageSize) {
+                    record_error(p.status, MLA_ERR_BAD_BLOCK_ID, int32_t(slot / kPageSize));
+                    continue;
+                }
+                uint16_t* row = p.cache + slot * kD;
+                for (int i = 0; i < kLkv / 8; ++i)
+                    copy16(row + 8 * i, p.kv_c + int64_t(b) * kLkv + 8 * i);
+#pragma unroll
+                for (int i = 0; i < kRope / 8; ++i)
+                    copy16(row + kLkv + 8 * i, p.k_pe + int64_t(b) * kRope + 8 * i);
+            }
+        }
+    }
+
+    // Epilogue: thread = row of the tile = TMEM lane.
+    bool acc_ok = true;
+    if (lane == 0)
+        acc_ok = bmm_wait(b_acc, 0, abort, p.status, kSiteAccFull, true);
+    acc_ok = __shfl_sync(0xffffffffu, acc_ok ? 1 : 0, 0) != 0 && *abort == 0;
+    ptx::tc_fence_after();
+    if (acc_ok) {
+        const int b = m0 + warp * 32 + lane;
+        uint16_t* dst = p.out + int64_t(b) * p.out_row + int64_t(n) * p.out_head;
+#pragma unroll 1
+        for (int c = 0; c < J / 32; ++c) {
+            uint32_t r[32];
+            ptx::tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c * 32), r);
+            if (b < p.batch) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = uint32_t(f32_to_bf16_bits_rn(__uint_as_float(r[2 * i]))) |
+                           (uint32_t(f32_to_bf16_bits_rn(__uint_as_float(r[2 * i + 1]))) << 16);
+                uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem, Sh::kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 bmm_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// Row-major bf16 [rows, cols] view, boxes of box_rows x 64 columns, 128-byte swizzle.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = bmm_encoder();
+    if (encode == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int J, int KD, int STAGES, bool kFrontEnd>
+int launch_bmm(const BmmParams& p, const void* a, const void* w, cudaStream_t st) {
+    using Sh = BmmShape<J, KD, STAGES>;
+    CUtensorMap ta, tw;
+    if (!encode_2d(&ta, a, uint64_t(p.heads) * p.a_head, uint64_t(p.batch), kM) ||
+        !encode_2d(&tw, w, J, uint64_t(p.heads) * KD, kChunk))
+        return int(cudaErrorInvalidValue);
+    auto kernel = mla_bmm_kernel<J, KD, STAGES, kFrontEnd>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Sh::kSmemBytes);
+    if (e != cudaSuccess) return int(e);
+    const dim3 grid(unsigned((p.batch + kM - 1) / kM), unsigned(p.heads));
+    kernel<<<grid, kBmmThreads, Sh::kSmemBytes, st>>>(p, ta, tw);
+    return int(cudaGetLastError());
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int status_of(int e) { return e == 0 ? MLA_OK : MLA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int mla_q_absorb_concat_cache(const void* q, const void* w_uk_t, const void* kv_c,
+                                         const void* k_pe, const int64_t* slot_mapping,
+                                         void* latent_cache, int64_t num_blocks, int batch,
+                                         int num_heads, void* mqa_q, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+    if (batch < 0 || num_heads < 0 || num_heads > kMaxHeads || num_blocks < 0)
+        return MLA_ERR_INVALID_ARG;
+    if (batch == 0 || num_heads == 0) return MLA_OK;
+    if (!q || !w_uk_t || !mqa_q) return MLA_ERR_INVALID_ARG;
+    if (slot_mapping && (!kv_c || !k_pe || !latent_cache)) return MLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kStatusBytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return MLA_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(w_uk_t) || !aligned16(mqa_q) ||
+        (slot_mapping && (!aligned16(kv_c) || !aligned16(k_pe) || !aligned16(latent_cache) ||
+                          (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)))
+        return MLA_ERR_INVALID_ARG;
+    BmmParams p{};
+    p.batch = batch;
+    p.heads = num_heads;
+    p.a_head = kQHead;
+    p.q = static_cast<const uint16_t*>(q);
+    p.out = static_cast<uint16_t*>(mqa_q);
+    p.out_row = int64_t(num_heads) * kD;
+    p.out_head = kD;
+    p.kv_c = static_cast<const uint16_t*>(kv_c);
+    p.k_pe = static_cast<const uint16_t*>(k_pe);
+    p.slots = slot_mapping;
+    p.cache = static_cast<uint16_t*>(latent_cache);
+    p.num_blocks = num_blocks;
+    p.status = static_cast<int32_t*>(workspace);
+    return status_of(launch_bmm<kLkv, kNope, 2, true>(p, q, w_uk_t,
+                                                      static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int mla_v_up_proj(const void* x, const void* w_uv, int batch, int num_heads, void* out,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    if (batch < 0 || num_heads < 0 || num_heads > kMaxHeads) return MLA_ERR_INVALID_ARG;
+    if (batch == 0 || num_heads == 0) return MLA_OK;
+    if (!x || !w_uv || !out) return MLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kStatusBytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return MLA_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+    BmmParams p{};
+    p.batch = batch;
+    p.heads = num_heads;
+    p.a_head = kLkv;
+    p.out = static_cast<uint16_t*>(out);
+    p.out_row = int64_t(num_heads) * kNope;
+    p.out_head = kNope;
+    p.status = static_cast<int32_t*>(workspace);
+    return status_of(launch_bmm<kNope, kLkv, 4, false>(p, x, w_uv,
+                                                       static_cast<cudaStream_t>(stream)));
+}

@@ -204,6 +204,34 @@ def test_dcp_local_seq_lens_rejects_bad_arguments(lib, world, rank, interleave, 
     assert (out == 99).all()
 
 
+def test_front_end_and_up_projection_reject_bad_arguments(lib):
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    null = ctypes.c_void_p(0)
+    ws = ctypes.c_void_p(0x20000)
+    big = binding.STATUS_BYTES
+    qa = lib.mla_q_absorb_concat_cache
+    assert qa(fake, fake, null, null, null, null, 0, 2, 129, fake, ws, big, null) == \
+        binding.MLA_ERR_INVALID_ARG
+    assert qa(null, fake, null, null, null, null, 0, 2, 4, fake, ws, big, null) == \
+        binding.MLA_ERR_INVALID_ARG
+    assert qa(fake, fake, null, null, fake, null, 4, 2, 4, fake, ws, big, null) == \
+        binding.MLA_ERR_INVALID_ARG                     # slots without the cache rows
+    assert qa(fake, fake, null, null, null, null, 0, 2, 4, fake, ws, 256, null) == \
+        binding.MLA_ERR_WORKSPACE
+    assert qa(fake, fake, null, null, null, null, 0, 2, 4, fake, odd, big, null) == \
+        binding.MLA_ERR_WORKSPACE
+    assert qa(odd, fake, null, null, null, null, 0, 2, 4, fake, ws, big, null) == \
+        binding.MLA_ERR_INVALID_ARG
+    assert qa(null, null, null, null, null, null, 0, 0, 4, null, null, 0, null) == binding.MLA_OK
+    up = lib.mla_v_up_proj
+    assert up(fake, fake, 2, 0, fake, ws, big, null) == binding.MLA_OK
+    assert up(fake, fake, -1, 4, fake, ws, big, null) == binding.MLA_ERR_INVALID_ARG
+    assert up(fake, null, 2, 4, fake, ws, big, null) == binding.MLA_ERR_INVALID_ARG
+    assert up(fake, fake, 2, 4, fake, null, big, null) == binding.MLA_ERR_WORKSPACE
+    assert up(fake, fake, 2, 4, odd, ws, big, null) == binding.MLA_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for code in range(-7, 1):
         assert lib.mla_status_string(code)
