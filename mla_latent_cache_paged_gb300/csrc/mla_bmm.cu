@@ -21,9 +21,11 @@
 // x 64 columns of the [N * K, J] view. Both use the 128-byte swizzle.
 // Warp 0 lane 0 loads (a ring of STAGES chunks), warp 1 lane 0 issues
 // tcgen05.mma (M = 128, N = min(J, 256), K = 16), and all four warps read the
-// accumulator back (thread = row), round to bf16 and store. In the front end
-// warps 2-3 copy q_pe and, in the CTAs of head 0, insert the new tokens'
-// latent rows while the MMAs run. Every wait is bounded (MLA_ERR_TIMEOUT);
+// accumulator back (thread = row), round to bf16, stage it in shared memory
+// (the idle ring, 128-byte swizzled) and write it with TMA stores. In the
+// front end the q_pe tile arrives by TMA with the first chunk and leaves by
+// TMA store, and warps 2-3 insert the new tokens' latent rows (the CTAs of
+// a batch tile share them out by head) while the MMAs run. Every wait is bounded (MLA_ERR_TIMEOUT);
 // a slot outside the cache is recorded (MLA_ERR_BAD_BLOCK_ID), not written.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -57,11 +59,13 @@ struct BmmShape {
     static constexpr int kPiece = J > 256 ? 256 : J;       // N of one MMA
     static constexpr int kPieces = J / kPiece;
     static constexpr int kTmemCols = J < 32 ? 32 : J;
-    static constexpr int kBarOff = STAGES * kStageBytes;   // full[S], empty[S], acc, slot, abort
+    static constexpr int kPeOff = STAGES * kStageBytes;    // front end: q_pe tile, 128 x 64
+    static constexpr int kBarOff = kPeOff + kABytes;       // full[S], empty[S], acc, slot, abort
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;   // + alignment slack
     static_assert(KD % kChunk == 0 && J % 64 == 0 && J <= 512, "shape");
     static_assert((J & (J - 1)) == 0, "TMEM allocation is a power of two");
     static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(STAGES * kStageBytes >= (J / 64) * kM * 128, "epilogue staging fits the ring");
 };
 
 struct BmmParams {
@@ -95,14 +99,26 @@ __device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-__device__ __forceinline__ void copy16(void* dst, const void* src) {
-    *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+// Tiled TMA store of the box at (x, y) from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(x), "r"(y), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 template <int J, int KD, int STAGES, bool kFrontEnd>
 __global__ void __launch_bounds__(kBmmThreads, 1)
 mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
-               const __grid_constant__ CUtensorMap tmap_w) {
+               const __grid_constant__ CUtensorMap tmap_w,
+               const __grid_constant__ CUtensorMap tmap_o) {
     using Sh = BmmShape<J, KD, STAGES>;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -149,8 +165,12 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
                               kSiteRingEmpty, false))
                     break;
                 const uint32_t st = sbase + uint32_t(s * Sh::kStageBytes);
-                ptx::mbar_arrive_expect_tx(b_full + 8 * s, Sh::kStageBytes);
+                const bool pe = kFrontEnd && c == 0;
+                ptx::mbar_arrive_expect_tx(b_full + 8 * s, Sh::kStageBytes + (pe ? kABytes : 0));
                 ptx::tma_load_2d(st, &tmap_a, n * p.a_head + c * kChunk, m0, b_full + 8 * s);
+                if (pe)   // q_pe: columns 128..191 of the head, next to q_nope
+                    ptx::tma_load_2d(sbase + Sh::kPeOff, &tmap_a, n * p.a_head + kNope, m0,
+                                     b_full + 8 * s);
 #pragma unroll
                 for (int jb = 0; jb < J / 64; ++jb)
                     ptx::tma_load_2d(st + kABytes + uint32_t(jb * kWBlockBytes), &tmap_w, jb * 64,
@@ -200,58 +220,95 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
         }
         __syncwarp();
     } else if (kFrontEnd) {
-        // q_pe into columns 512..575 of mqa_q, and (head 0 only) the new
-        // tokens' latent rows into the cache.
-        for (int r = threadIdx.x - 64; r < kM; r += 64) {
-            const int b = m0 + r;
-            if (b >= p.batch) break;
-            const uint16_t* src = p.q + (int64_t(b) * p.heads + n) * kQHead + kNope;
-            uint16_t* dst = p.out + b * p.out_row + int64_t(n) * p.out_head + J;
+        const int t = threadIdx.x - 64;   // warps 2-3
+        // q_pe: the tile that landed with stage 0 goes out as four 32-row boxes
+        // to columns 512..575 of the head.
+        if (t == 0 && bmm_wait(b_full, 0, abort, p.status, kSiteRingFull, false)) {
+            for (int slab = 0; slab < kM / 32 && m0 + 32 * slab < p.batch; ++slab)
+                tma_store_2d(&tmap_o, n * p.out_head + J, m0 + 32 * slab,
+                             sbase + uint32_t(Sh::kPeOff + slab * 4096));
+            bulk_commit();
+        }
+        // Cache insert: rows n, n + N, ... of this tile, 72 16-byte pieces each,
+        // four loads in flight per thread before their stores.
+        if (p.slots != nullptr) {
+            constexpr int kPieces = kD / 8;
+            const int rows = (kM - 1 - n) / p.heads + 1;
+            const int total = rows * kPieces;
+            const int64_t limit = p.num_blocks * kPageSize;
+            for (int i0 = t; i0 < total; i0 += 4 * 64) {
+                uint4 v[4];
+                uint16_t* dst[4];
 #pragma unroll
-            for (int i = 0; i < kRope / 8; ++i) copy16(dst + 8 * i, src + 8 * i);
-            if (n == 0 && p.slots != nullptr) {
-                const int64_t slot = p.slots[b];
-                if (slot < 0) continue;
-                if (slot >= p.num_blocks * kPageSize) {
-                    record_error(p.status, MLA_ERR_BAD_BLOCK_ID, int32_t(slot / kPageSize));
-                    continue;
+                for (int k = 0; k < 4; ++k) {
+                    dst[k] = nullptr;
+                    const int i = i0 + 64 * k;
+                    if (i >= total) continue;
+                    const int b = m0 + n + (i / kPieces) * p.heads;
+                    const int piece = i % kPieces;
+                    if (b >= p.batch) continue;
+                    const int64_t slot = p.slots[b];
+                    if (slot < 0) continue;
+                    if (slot >= limit) {
+                        if (piece == 0)
+                            record_error(p.status, MLA_ERR_BAD_BLOCK_ID, int32_t(slot / kPageSize));
+                        continue;
+                    }
+                    const uint16_t* src = piece < kLkv / 8
+                                              ? p.kv_c + int64_t(b) * kLkv + 8 * piece
+                                              : p.k_pe + int64_t(b) * kRope + 8 * (piece - kLkv / 8);
+                    v[k] = __ldg(reinterpret_cast<const uint4*>(src));
+                    dst[k] = p.cache + slot * kD + 8 * piece;
                 }
-                uint16_t* row = p.cache + slot * kD;
-                for (int i = 0; i < kLkv / 8; ++i)
-                    copy16(row + 8 * i, p.kv_c + int64_t(b) * kLkv + 8 * i);
 #pragma unroll
-                for (int i = 0; i < kRope / 8; ++i)
-                    copy16(row + kLkv + 8 * i, p.k_pe + int64_t(b) * kRope + 8 * i);
+                for (int k = 0; k < 4; ++k)
+                    if (dst[k] != nullptr) *reinterpret_cast<uint4*>(dst[k]) = v[k];
             }
         }
     }
 
-    // Epilogue: thread = row of the tile = TMEM lane.
+    // Epilogue: thread = row of the tile = TMEM lane. Each warp stages its 32
+    // rows, 64 columns at a time, in the (now idle) ring in the 128-byte
+    // swizzled layout of the output tensor map and stores them by TMA; rows
+    // past the batch fall outside the map and are not written.
     bool acc_ok = true;
     if (lane == 0)
         acc_ok = bmm_wait(b_acc, 0, abort, p.status, kSiteAccFull, true);
     acc_ok = __shfl_sync(0xffffffffu, acc_ok ? 1 : 0, 0) != 0 && *abort == 0;
     ptx::tc_fence_after();
     if (acc_ok) {
-        const int b = m0 + warp * 32 + lane;
-        uint16_t* dst = p.out + int64_t(b) * p.out_row + int64_t(n) * p.out_head;
+        const uint32_t stage_w = sbase + uint32_t(warp * (J / 64) * 4096);
 #pragma unroll 1
-        for (int c = 0; c < J / 32; ++c) {
-            uint32_t r[32];
-            ptx::tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c * 32), r);
-            if (b < p.batch) {
-                uint32_t w[16];
+        for (int cb = 0; cb < J / 64; ++cb) {
+            uint32_t r0[32], r1[32];
+            const uint32_t taddr = tmem + (uint32_t(warp * 32) << 16) + uint32_t(cb * 64);
+            ptx::tmem_ld32(taddr, r0);
+            ptx::tmem_ld32(taddr + 32, r1);
+            const uint32_t row = stage_w + uint32_t(cb * 4096 + lane * 128);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = uint32_t(f32_to_bf16_bits_rn(__uint_as_float(r[2 * i]))) |
-                           (uint32_t(f32_to_bf16_bits_rn(__uint_as_float(r[2 * i + 1]))) << 16);
-                uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint32_t* r = ch < 4 ? r0 : r1;
+                const int o = (ch & 3) * 8;
+                uint32_t w[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    w[i] = uint32_t(f32_to_bf16_bits_rn(__uint_as_float(r[o + 2 * i]))) |
+                           (uint32_t(f32_to_bf16_bits_rn(__uint_as_float(r[o + 2 * i + 1]))) << 16);
+                const uint32_t addr = row + uint32_t(((ch ^ (lane & 7)) * 16));
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
+                             "r"(w[1]), "r"(w[2]), "r"(w[3])
+                             : "memory");
             }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && m0 + warp * 32 < p.batch)
+                tma_store_2d(&tmap_o, n * p.out_head + cb * 64, m0 + warp * 32,
+                             stage_w + uint32_t(cb * 4096));
         }
+        if (lane == 0) bulk_commit();
     }
+    if (lane == 0) bulk_wait_all();   // stores issued by this thread have completed
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -288,16 +345,17 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
 template <int J, int KD, int STAGES, bool kFrontEnd>
 int launch_bmm(const BmmParams& p, const void* a, const void* w, cudaStream_t st) {
     using Sh = BmmShape<J, KD, STAGES>;
-    CUtensorMap ta, tw;
+    CUtensorMap ta, tw, to;
     if (!encode_2d(&ta, a, uint64_t(p.heads) * p.a_head, uint64_t(p.batch), kM) ||
-        !encode_2d(&tw, w, J, uint64_t(p.heads) * KD, kChunk))
+        !encode_2d(&tw, w, J, uint64_t(p.heads) * KD, kChunk) ||
+        !encode_2d(&to, p.out, uint64_t(p.heads) * p.out_head, uint64_t(p.batch), 32))
         return int(cudaErrorInvalidValue);
     auto kernel = mla_bmm_kernel<J, KD, STAGES, kFrontEnd>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Sh::kSmemBytes);
     if (e != cudaSuccess) return int(e);
     const dim3 grid(unsigned((p.batch + kM - 1) / kM), unsigned(p.heads));
-    kernel<<<grid, kBmmThreads, Sh::kSmemBytes, st>>>(p, ta, tw);
+    kernel<<<grid, kBmmThreads, Sh::kSmemBytes, st>>>(p, ta, tw, to);
     return int(cudaGetLastError());
 }
 
