@@ -51,21 +51,26 @@ constexpr int kQHead = kNope + kRope;        // q head width (P + R)
 
 enum BmmSite : int32_t { kSiteRingEmpty = 30, kSiteRingFull, kSiteAccFull, kSiteRingDrain };
 
+// Shared memory: the whole A tile (all K chunks, loaded at once so that each
+// request's row is read in one burst), a ring of STAGES weight chunks, the
+// front end's q_pe tile, then the barriers. The result is staged over the A
+// tile and the ring once the MMAs are done.
 template <int J, int KD, int STAGES>
 struct BmmShape {
-    static constexpr int kWBytes = (J / 64) * kWBlockBytes;
-    static constexpr int kStageBytes = kABytes + kWBytes;
+    static constexpr int kWBytes = (J / 64) * kWBlockBytes;   // one weight chunk
     static constexpr int kChunks = KD / kChunk;
+    static constexpr int kAllABytes = kChunks * kABytes;
+    static constexpr int kRingOff = kAllABytes;
     static constexpr int kPiece = J > 256 ? 256 : J;       // N of one MMA
     static constexpr int kPieces = J / kPiece;
     static constexpr int kTmemCols = J < 32 ? 32 : J;
-    static constexpr int kPeOff = STAGES * kStageBytes;    // front end: q_pe tile, 128 x 64
-    static constexpr int kBarOff = kPeOff + kABytes;       // full[S], empty[S], acc, slot, abort
+    static constexpr int kPeOff = kRingOff + STAGES * kWBytes;   // front end: q_pe, 128 x 64
+    static constexpr int kBarOff = kPeOff + kABytes;   // a_full, w_full[S], w_empty[S], acc, slot, abort
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;   // + alignment slack
     static_assert(KD % kChunk == 0 && J % 64 == 0 && J <= 512, "shape");
     static_assert((J & (J - 1)) == 0, "TMEM allocation is a power of two");
     static_assert(kSmemBytes <= 232448, "shared memory");
-    static_assert(STAGES * kStageBytes >= (J / 64) * kM * 128, "epilogue staging fits the ring");
+    static_assert(kPeOff >= (J / 64) * kM * 128, "epilogue staging fits A and the ring");
 };
 
 struct BmmParams {
@@ -125,10 +130,11 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
     const uint32_t sbase = raw + pad;
     unsigned char* smem = smem_raw + pad;
-    const uint32_t b_full = sbase + Sh::kBarOff;
+    const uint32_t b_afull = sbase + Sh::kBarOff;
+    const uint32_t b_full = b_afull + 8;
     const uint32_t b_empty = b_full + 8 * STAGES;
     const uint32_t b_acc = b_empty + 8 * STAGES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::kBarOff + 16 * STAGES + 8);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::kBarOff + 16 * STAGES + 16);
     volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -136,7 +142,12 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
     const int n = blockIdx.y;
     const int m0 = blockIdx.x * kM;
 
+    // A programmatic dependent launch of the next kernel may start its setup
+    // now; it waits for this grid before touching global memory, as this one
+    // waits for its predecessor below.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
+        ptx::mbar_init(b_afull, 1);
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(b_full + 8 * s, 1);
             ptx::mbar_init(b_empty + 8 * s, 1);
@@ -153,31 +164,35 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
-        // Producer: chunk c into stage c % STAGES once its previous use is done.
+        // Producer: the whole A tile (and q_pe) at once, then weight chunk c
+        // into stage c % STAGES once its previous use is done.
         int issued = 0;
         if (ptx::elect_one()) {
+            ptx::mbar_arrive_expect_tx(b_afull, Sh::kAllABytes + (kFrontEnd ? kABytes : 0));
+            for (int c = 0; c < Sh::kChunks; ++c)
+                ptx::tma_load_2d(sbase + uint32_t(c * kABytes), &tmap_a,
+                                 n * p.a_head + c * kChunk, m0, b_afull);
+            if (kFrontEnd)   // q_pe: columns 128..191 of the head, next to q_nope
+                ptx::tma_load_2d(sbase + Sh::kPeOff, &tmap_a, n * p.a_head + kNope, m0, b_afull);
             for (int c = 0; c < Sh::kChunks; ++c) {
                 const int s = c % STAGES;
                 if (c >= STAGES &&
                     !bmm_wait(b_empty + 8 * s, ((c / STAGES) - 1) & 1, abort, p.status,
                               kSiteRingEmpty, false))
                     break;
-                const uint32_t st = sbase + uint32_t(s * Sh::kStageBytes);
-                const bool pe = kFrontEnd && c == 0;
-                ptx::mbar_arrive_expect_tx(b_full + 8 * s, Sh::kStageBytes + (pe ? kABytes : 0));
-                ptx::tma_load_2d(st, &tmap_a, n * p.a_head + c * kChunk, m0, b_full + 8 * s);
-                if (pe)   // q_pe: columns 128..191 of the head, next to q_nope
-                    ptx::tma_load_2d(sbase + Sh::kPeOff, &tmap_a, n * p.a_head + kNope, m0,
-                                     b_full + 8 * s);
+                const uint32_t st = sbase + uint32_t(Sh::kRingOff + s * Sh::kWBytes);
+                ptx::mbar_arrive_expect_tx(b_full + 8 * s, Sh::kWBytes);
 #pragma unroll
                 for (int jb = 0; jb < J / 64; ++jb)
-                    ptx::tma_load_2d(st + kABytes + uint32_t(jb * kWBlockBytes), &tmap_w, jb * 64,
+                    ptx::tma_load_2d(st + uint32_t(jb * kWBlockBytes), &tmap_w, jb * 64,
                                      n * KD + c * kChunk, b_full + 8 * s);
                 ++issued;
             }
             // Copies still in flight (after an abort) land before the CTA exits.
+            bmm_wait(b_afull, 0, abort, p.status, kSiteRingDrain, true);
             for (int c = issued - STAGES < 0 ? 0 : issued - STAGES; c < issued; ++c)
                 bmm_wait(b_full + 8 * (c % STAGES), (c / STAGES) & 1, abort, p.status,
                          kSiteRingDrain, true);
@@ -187,15 +202,15 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
         // MMA issuer.
         constexpr uint32_t idesc = ptx::idesc_bf16_f32(Sh::kPiece, true);
         if (ptx::elect_one()) {
-            bool ok = true;
+            bool ok = bmm_wait(b_afull, 0, abort, p.status, kSiteRingFull, false);
             for (int c = 0; c < Sh::kChunks && ok; ++c) {
                 const int s = c % STAGES;
                 ok = bmm_wait(b_full + 8 * s, (c / STAGES) & 1, abort, p.status, kSiteRingFull,
                               false);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                const uint32_t a_st = sbase + uint32_t(s * Sh::kStageBytes);
-                const uint32_t w_st = a_st + kABytes;
+                const uint32_t a_st = sbase + uint32_t(c * kABytes);
+                const uint32_t w_st = sbase + uint32_t(Sh::kRingOff + s * Sh::kWBytes);
                 // A: K-major, 16 k = 32 bytes per step; W: MN-major, 16 k-rows
                 // = 2 KB per step, 64-column blocks 8 KB apart.
                 const uint64_t a0 = ptx::desc_sw128(a_st, 16, 1024);
@@ -223,7 +238,7 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
         const int t = threadIdx.x - 64;   // warps 2-3
         // q_pe: the tile that landed with stage 0 goes out as four 32-row boxes
         // to columns 512..575 of the head.
-        if (t == 0 && bmm_wait(b_full, 0, abort, p.status, kSiteRingFull, false)) {
+        if (t == 0 && bmm_wait(b_afull, 0, abort, p.status, kSiteRingFull, false)) {
             for (int slab = 0; slab < kM / 32 && m0 + 32 * slab < p.batch; ++slab)
                 tma_store_2d(&tmap_o, n * p.out_head + J, m0 + 32 * slab,
                              sbase + uint32_t(Sh::kPeOff + slab * 4096));
@@ -354,9 +369,17 @@ int launch_bmm(const BmmParams& p, const void* a, const void* w, cudaStream_t st
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Sh::kSmemBytes);
     if (e != cudaSuccess) return int(e);
-    const dim3 grid(unsigned((p.batch + kM - 1) / kM), unsigned(p.heads));
-    kernel<<<grid, kBmmThreads, Sh::kSmemBytes, st>>>(p, ta, tw, to);
-    return int(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned((p.batch + kM - 1) / kM), unsigned(p.heads));
+    cfg.blockDim = dim3(kBmmThreads, 1, 1);
+    cfg.dynamicSmemBytes = Sh::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return int(cudaLaunchKernelEx(&cfg, kernel, p, ta, tw, to));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
