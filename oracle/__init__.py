@@ -14,6 +14,7 @@ from .mla_oracle import (  # noqa: F401
     gather_request_latent,
     merge_partials,
     mha_compute_friendly,
+    mla_decode_multi_token_reference,
     mla_decode_reference,
     mla_decode_split_partials,
     q_absorb_concat_cache,

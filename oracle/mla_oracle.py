@@ -31,6 +31,10 @@ Pins (see ``tests/test_oracle.py``):
     weights' printed layouts on tiny inputs, a hand-worked cache insert, and
     the whole decode step (front end, decode, up-projection) equal to the
     compute-friendly MHA over the cache plus the new token.
+  * ``mla_decode_multi_token_reference`` -- T = 1 is the single-token
+    definition; each query token equals the single-token definition over the
+    tokens it sees; torch SDPA in float64 with the causal block mask; a
+    hand-worked two-token case.
 No function here is "parity unpinned".
 """
 
@@ -349,3 +353,45 @@ def v_up_proj(x, w_uv):
     """``out [B, N, V] = bmm(x (N, B, Lkv), W_UV (N, Lkv, V))`` transposed back,
     with ``W_UV`` the ``(Lkv, N, V)`` weight transposed to ``(N, Lkv, V)``."""
     return up_project(x, np.transpose(np.asarray(w_uv, dtype=np.float64), (1, 0, 2)))
+
+
+def mla_decode_multi_token_reference(q, cache, block_table, seq_lens, softmax_scale,
+                                     causal=True, kv_lora_rank=512):
+    """Uniform multi-token decode: ``q [B, T, N, Lkv + R]`` -> ``out [B, T, N,
+    Lkv]``, ``lse [B, T, N]``.
+
+    vLLM ``mla_attention`` API docs, ``QueryLenSupport.UNIFORM`` (every request
+    has the same query length T > 1) and ``MLACommonMetadataBuilder.build``
+    (``causal``; a non-causal query block is also allowed). The T new tokens
+    are already in the cache (they are inserted before the attention), so
+    request b holds ``L = seq_lens[b]`` tokens and its query token i sits at
+    position ``L - T + i``. Reading: with ``causal`` it attends to the tokens
+    ``t <= L - T + i``, else to all ``t < L``; a query token that sees no
+    token gives the neutral element (zero output, ``-inf`` LSE). Written as
+    one masked score matrix ``[T, L]`` per request and head.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    batch, qlen, n_heads, _ = q.shape
+    out = np.zeros((batch, qlen, n_heads, kv_lora_rank), dtype=np.float64)
+    lse = np.full((batch, qlen, n_heads), -np.inf, dtype=np.float64)
+    for b in range(batch):
+        L = int(seq_lens[b])
+        k_rows = gather_request_latent(cache, block_table[b], L)
+        if L == 0:
+            continue
+        pos = np.arange(L)
+        for h in range(n_heads):
+            scores = softmax_scale * (q[b, :, h, :] @ k_rows.T)          # [T, L]
+            if causal:
+                visible = pos[None, :] <= (L - qlen + np.arange(qlen))[:, None]
+                scores = np.where(visible, scores, -np.inf)
+            for i in range(qlen):
+                row = scores[i]
+                if not np.isfinite(row).any():
+                    continue
+                m = row.max()
+                e = np.exp(row - m)
+                s = e.sum()
+                lse[b, i, h] = m + math.log(s)
+                out[b, i, h] = (e / s) @ k_rows[:, :kv_lora_rank]
+    return out, lse

@@ -14,7 +14,8 @@ import pytest
 
 from oracle import (absorb_query, dcp_combine, dcp_decode_partials,
                     dcp_local_seq_lens, dcp_owner, gather_request_latent,
-                    merge_partials, mha_compute_friendly, mla_decode_reference,
+                    merge_partials, mha_compute_friendly, mla_decode_multi_token_reference,
+                    mla_decode_reference,
                     mla_decode_split_partials, q_absorb_concat_cache, split_token_ranges,
                     up_project, v_up_proj)
 
@@ -455,3 +456,68 @@ def test_decode_step_with_front_end_equals_compute_friendly_mha():
     out = v_up_proj(lat, np.transpose(w_uv, (1, 0, 2)))[0]
     np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(lse[0], ref_lse, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------ multi-token (uniform) decode
+
+def test_multi_token_hand_worked():
+    """Two query tokens over a two-token cache, scale ln 2 (worked by hand).
+    Causal: token 0 sits at position 0 and sees only row 0 (out = V[0],
+    lse = 2 ln 2 since q0.k0 = 2); token 1 sees both rows with q1.k = (0, 1):
+    weights 1/3, 2/3 and lse = ln 3. Non-causal: token 0 sees both rows too,
+    q0.k = (2, 2): weights 1/2, 1/2 and lse = 2 ln 2 + ln 2 = 3 ln 2."""
+    # Entries [v0, v1 | rope]: Lkv = 2, R = 1.
+    cache = np.array([[[1.0, 0.0, 2.0], [0.0, 1.0, 2.0]]])     # k0 = (1,0,2), k1 = (0,1,2)
+    table = np.array([[0]])
+    q = np.array([[[[0.0, 0.0, 1.0]], [[-2.0, -1.0, 1.0]]]])   # q0.k = (2, 2); q1.k = (0, 1)
+    out, lse = mla_decode_multi_token_reference(q, cache, table, [2], math.log(2),
+                                                causal=True, kv_lora_rank=2)
+    np.testing.assert_allclose(out[0, 0, 0], [1.0, 0.0], atol=1e-15)
+    assert abs(lse[0, 0, 0] - 2 * math.log(2)) < 1e-14
+    np.testing.assert_allclose(out[0, 1, 0], [1 / 3, 2 / 3], atol=1e-15)
+    assert abs(lse[0, 1, 0] - math.log(3)) < 1e-14
+    out, lse = mla_decode_multi_token_reference(q, cache, table, [2], math.log(2),
+                                                causal=False, kv_lora_rank=2)
+    np.testing.assert_allclose(out[0, 0, 0], [0.5, 0.5], atol=1e-15)
+    assert abs(lse[0, 0, 0] - 3 * math.log(2)) < 1e-14
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_multi_token_equals_single_token_over_the_visible_tokens(causal):
+    rng = np.random.default_rng(400 + causal)
+    T, lens = 3, [1, 2, 3, 64, 65, 130]
+    dense = [rng.standard_normal((L, 576)) for L in lens]
+    cache, table = _paged_from_dense(rng, dense, 64)
+    q = rng.standard_normal((len(lens), T, 4, 576))
+    out, lse = mla_decode_multi_token_reference(q, cache, table, lens, 0.07, causal=causal)
+    for i in range(T):
+        vis = [max(0, L - T + 1 + i) if causal else L for L in lens]
+        o1, l1 = mla_decode_reference(q[:, i], cache, table, vis, 0.07)
+        np.testing.assert_allclose(out[:, i], o1, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(lse[:, i], l1, rtol=1e-13, atol=1e-13)
+    if causal:
+        assert np.isneginf(lse[0, :2]).all() and np.isfinite(lse[0, 2]).all()
+    o_single, l_single = mla_decode_reference(q[:, 0], cache, table, lens, 0.07)
+    o_t1, l_t1 = mla_decode_multi_token_reference(q[:, :1], cache, table, lens, 0.07,
+                                                  causal=causal)
+    np.testing.assert_allclose(o_t1[:, 0], o_single, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(l_t1[:, 0], l_single, rtol=1e-13, atol=1e-13)
+
+
+def test_multi_token_matches_torch_sdpa_with_the_causal_block_mask():
+    import torch
+    rng = np.random.default_rng(402)
+    T, L, N = 4, 37, 3
+    rows = rng.standard_normal((L, 576))
+    cache, table = _paged_from_dense(rng, [rows], 16)
+    q = rng.standard_normal((1, T, N, 576))
+    out, lse = mla_decode_multi_token_reference(q, cache, table, [L], 0.05, causal=True)
+    mask = torch.arange(L)[None, :] <= (L - T + torch.arange(T))[:, None]      # [T, L]
+    qt = torch.from_numpy(q[0]).permute(1, 0, 2)                                 # [N, T, D]
+    k = torch.from_numpy(rows)[None].expand(N, L, 576)
+    v = torch.from_numpy(rows[:, :512])[None].expand(N, L, 512)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, k, v, attn_mask=mask, scale=0.05)
+    np.testing.assert_allclose(out[0].transpose(1, 0, 2), ref.numpy(), rtol=1e-12, atol=1e-12)
+    scores = (qt @ k.transpose(1, 2)) * 0.05
+    ref_lse = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), dim=-1)   # [N, T]
+    np.testing.assert_allclose(lse[0].T, ref_lse.numpy(), rtol=1e-12, atol=1e-12)
