@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--q-len", type=int, default=2,
+                    help="query tokens per request for --stage multi_token")
     ap.add_argument("--stage", choices=["decode"] + sorted(STAGES), default="decode",
                     help="time one of the steps around the decode instead (at the workload's "
                          "batch and head count)")
@@ -246,6 +248,8 @@ STAGES = {
     "front_end": "MLA decode front end (q absorption by W_UK_T, q_pe concat, latent cache "
                  "insert), one launch",
     "v_up_proj": "MLA up-projection of the decode output by W_UV, one launch",
+    "multi_token": "MLA uniform multi-token decode (causal query block of --q-len tokens per "
+                   "request)",
 }
 
 
@@ -263,6 +267,86 @@ def stage_work(stage, batch, heads):
     else:
         nbytes = 2 * (batch * heads * 512 + heads * 512 * 128 + batch * heads * 128)
     return nbytes, 2 * batch * heads * 128 * 512
+
+
+def run_multi_token(args):
+    """Time mla_decode_multi_token on the workload's requests with --q-len
+    query tokens each (the requests' caches are larger than L2)."""
+    import torch
+    from mla_latent_cache_paged_gb300 import binding, build
+    from mla_latent_cache_paged_gb300.workloads import HEADLINE, get_workload, to_torch
+
+    build.build()
+    w = get_workload(args.workload or HEADLINE)
+    T = args.q_len
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    _, cache, table, lens = to_torch(w, dev)
+    gen = torch.Generator(device=dev).manual_seed(20260200)
+    q = torch.randn((w.batch, T, w.num_heads, 576), generator=gen, device=dev).to(torch.bfloat16)
+    plan = binding.make_plan_multi_token(w.batch, T, w.num_heads, w.max_blocks_per_seq,
+                                         seq_lens_host=w.seq_lens, causal=True,
+                                         num_sms=torch.cuda.get_device_properties(dev)
+                                         .multi_processor_count)
+    ws = binding.new_workspace(plan, dev)
+    out = torch.empty((w.batch, T, w.num_heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.batch, T, w.num_heads), dtype=torch.float32, device=dev)
+    nbytes = int(binding.load_library().mla_multi_token_scratch_bytes(w.batch, T,
+                                                                      w.max_blocks_per_seq))
+    scratch = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+
+    def call():
+        binding.mla_decode_multi_token(q, cache, table, lens, w.softmax_scale, causal=True,
+                                       plan=plan, out=out, lse=lse, workspace=ws,
+                                       scratch=scratch)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    if binding.read_error(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    steps = args.steps if args.steps > 0 else 200
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if binding.read_error(ws) != 0:
+        raise RuntimeError("device status after timing")
+    ms = e0.elapsed_time(e1) / steps
+    rows = w.batch * T
+    pages = sum(-(-int(L) // 64) for L in w.seq_lens)
+    # The method needs each request's cache once, q and out per query row.
+    nbytes_alg = 1152 * w.total_tokens + rows * w.num_heads * (1152 + 1024 + 4) + 4 * pages
+    peaks, peak_kind = load_peaks()
+    achieved = nbytes_alg / (ms / 1e3) / 1e9
+    return {
+        "metric": STAGES["multi_token"] + ": cached-tokens x heads x query-tokens / s",
+        "value": w.total_tokens * w.num_heads * T / (ms / 1e3),
+        "unit": "cached-tokens*heads*query-tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}_q{T}", "batch": w.batch, "heads": w.num_heads,
+                   "q_len": T, "causal": True, "cached_tokens": w.total_tokens,
+                   "rows": rows, "num_kv_splits": plan.num_kv_splits,
+                   "schedule": (f"page-balanced over {plan.sched_pairs} CTA pairs + merge"
+                                if plan.sched_pairs > 0 else f"split S={plan.num_kv_splits}"),
+                   "l2": "inputs larger than L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes_per_launch": nbytes_alg,
+                     "note": "each query row reads its request's pages: the cache is read "
+                             f"{T} times per call"},
+        "gpu_launches": steps * (2 + (1 if plan.num_kv_splits > 1 or plan.sched_pairs else 0)),
+        "clocks": clocks,
+    }
 
 
 def run_stage(args, stage):
@@ -565,7 +649,8 @@ def main():
     if args.stage != "decode":
         if world > 1:
             raise SystemExit("--stage runs on one GPU")
-        print(json.dumps(run_stage(args, args.stage)), flush=True)
+        res = run_multi_token(args) if args.stage == "multi_token" else run_stage(args, args.stage)
+        print(json.dumps(res), flush=True)
         return 0
 
     if args.impl == "reference":

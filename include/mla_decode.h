@@ -244,6 +244,42 @@ int mla_merge_splits(const float* o_part, const float* lse_part, int batch, int 
                      int num_splits, int v_dim, void* out, float* lse, void* stream);
 
 /*
+ * Uniform multi-token decode (vLLM mla_attention API docs,
+ * QueryLenSupport.UNIFORM: every request has the same query length
+ * q_len = T > 1, e.g. speculative decoding; MLACommonMetadataBuilder.build:
+ * the query block is causal unless a non-causal one is allowed).
+ *
+ * The T new tokens are already in the cache, so request b holds
+ * L = seq_lens[b] tokens and its query token i (0 <= i < T) sits at position
+ * L - T + i. With `causal` != 0 it attends to tokens t <= L - T + i (a token
+ * that sees none, when L < T - i, gets out = 0, lse = -inf); otherwise to all
+ * t < L.
+ *
+ *   plan          from mla_decode_plan with batch = B * T rows (row
+ *                 r = b * T + i) and, if given, the host lengths of those
+ *                 rows (the visible lengths above).
+ *   q             device, bf16 [B, T, N, 576] contiguous.
+ *   block_table   device, int32 [B, max_blocks_per_seq]; seq_lens int32 [B].
+ *   out, lse      device, bf16 [B, T, N, 512] and fp32 [B, T, N] (or NULL).
+ *   workspace     as for mla_decode with this plan.
+ *   scratch       device, >= mla_multi_token_scratch_bytes(B, T,
+ *                 max_blocks_per_seq) bytes, 256-byte aligned: the rows'
+ *                 block tables and lengths.
+ * One small launch that writes the rows' block tables and lengths into
+ * `scratch`, then mla_decode over the B * T rows (each row reads its
+ * request's pages). Errors as mla_decode; plan->batch not a multiple of
+ * q_len or q_len < 1 gives MLA_ERR_INVALID_ARG, scratch too small or
+ * misaligned MLA_ERR_WORKSPACE.
+ */
+size_t mla_multi_token_scratch_bytes(int batch, int q_len, int max_blocks_per_seq);
+int mla_decode_multi_token(const mla_decode_plan_t* plan, int q_len, int causal,
+                           const void* q, const void* latent_cache, int64_t num_blocks,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           float softmax_scale, void* out, float* lse, void* workspace,
+                           size_t workspace_bytes, void* scratch, size_t scratch_bytes,
+                           void* stream);
+
+/*
  * Decode context parallelism (DCP): each of `world` ranks holds a shard of
  * every request's cached tokens, runs mla_decode over its shard (with its own
  * block table and the shard lengths below as seq_lens), and the ranks'

@@ -39,7 +39,8 @@ EXPORTED_SYMBOLS = (
     "mla_decode_plan", "mla_workspace_init", "mla_decode", "mla_merge_splits",
     "mla_read_error", "mla_status_string", "mla_abi_version", "mla_debug_gather_pages",
     "mla_decode_noalloc", "mla_dcp_local_seq_lens", "mla_dcp_combine",
-    "mla_q_absorb_concat_cache", "mla_v_up_proj",
+    "mla_q_absorb_concat_cache", "mla_v_up_proj", "mla_multi_token_scratch_bytes",
+    "mla_decode_multi_token",
 )
 
 
@@ -106,9 +107,13 @@ def load_library(path=None):
     lib.mla_q_absorb_concat_cache.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp, sz,
                                               vp]
     lib.mla_v_up_proj.argtypes = [vp, vp, i32, i32, vp, vp, sz, vp]
+    lib.mla_multi_token_scratch_bytes.argtypes = [i32, i32, i32]
+    lib.mla_decode_multi_token.argtypes = [ctypes.POINTER(MlaDecodePlan), i32, i32, vp, vp, i64,
+                                           vp, vp, f32, vp, vp, vp, sz, vp, sz, vp]
     for name in EXPORTED_SYMBOLS:
-        if name not in ("mla_status_string",):
+        if name not in ("mla_status_string", "mla_multi_token_scratch_bytes"):
             getattr(lib, name).restype = ctypes.c_int
+    lib.mla_multi_token_scratch_bytes.restype = ctypes.c_size_t
     if path == LIB_PATH:
         _LIB = lib
     return lib
@@ -232,6 +237,67 @@ def mla_decode(q, latent_cache, block_table, seq_lens, softmax_scale, *, plan=No
         _ptr(block_table), _ptr(seq_lens), float(softmax_scale), _ptr(out), _ptr(lse),
         _ptr(workspace), int(workspace.numel()), _stream_ptr(stream))
     _check(rc, "mla_decode")
+    return out, lse
+
+
+def multi_token_row_lens(seq_lens_host, q_len, causal=True):
+    """Visible length of every (request, query token) row, row r = b * T + i:
+    ``L - (T - 1 - i)`` (at least 0) when causal, else ``L`` (host, numpy int32)."""
+    import numpy as np
+    lens = np.asarray(seq_lens_host, dtype=np.int64)
+    if not causal:
+        return np.repeat(lens, q_len).astype(np.int32)
+    shift = (q_len - 1 - np.arange(q_len))[None, :]
+    return np.maximum(lens[:, None] - shift, 0).reshape(-1).astype(np.int32)
+
+
+def make_plan_multi_token(batch, q_len, num_heads, max_blocks_per_seq, *, seq_lens_host=None,
+                          causal=True, **kw):
+    """A plan over the B * T rows of a uniform multi-token decode."""
+    if seq_lens_host is not None:
+        rows = multi_token_row_lens(seq_lens_host, q_len, causal)
+        kw.setdefault("max_seq_len", int(rows.max()) if rows.size else 0)
+        kw["seq_lens_host"] = rows
+    return make_plan(int(batch) * int(q_len), num_heads, max_blocks_per_seq, **kw)
+
+
+def mla_decode_multi_token(q, latent_cache, block_table, seq_lens, softmax_scale, *,
+                           causal=True, plan=None, num_kv_splits=0, out=None, lse=None,
+                           return_lse=True, workspace=None, scratch=None, stream=None):
+    """Uniform multi-token decode: ``q [B, T, N, 576]`` -> ``(out [B, T, N, 512],
+    lse [B, T, N] | None)``; one ``mla_decode_multi_token`` call."""
+    import torch
+    B, T, N, D = q.shape
+    if D != HEAD_DIM:
+        raise ValueError(f"q last dim must be {HEAD_DIM}")
+    _check_tensor(q, "q", torch.bfloat16)
+    _check_tensor(latent_cache, "latent_cache", torch.bfloat16)
+    _check_tensor(block_table, "block_table", torch.int32)
+    _check_tensor(seq_lens, "seq_lens", torch.int32, (B,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks_per_seq]")
+    if plan is None:
+        plan = make_plan_multi_token(B, T, N, block_table.shape[1], causal=causal,
+                                     num_kv_splits=num_kv_splits)
+    if out is None:
+        out = torch.empty((B, T, N, KV_LORA_RANK), dtype=torch.bfloat16, device=q.device)
+    _check_tensor(out, "out", torch.bfloat16, (B, T, N, KV_LORA_RANK))
+    if lse is None and return_lse:
+        lse = torch.empty((B, T, N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32, (B, T, N))
+    if workspace is None:
+        workspace = new_workspace(plan, q.device, stream)
+    lib = load_library()
+    if scratch is None:
+        nbytes = int(lib.mla_multi_token_scratch_bytes(B, T, block_table.shape[1]))
+        scratch = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.mla_decode_multi_token(
+        ctypes.byref(plan), int(T), 1 if causal else 0, _ptr(q), _ptr(latent_cache),
+        int(latent_cache.shape[0]), _ptr(block_table), _ptr(seq_lens), float(softmax_scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), int(workspace.numel()), _ptr(scratch),
+        int(scratch.numel()), _stream_ptr(stream))
+    _check(rc, "mla_decode_multi_token")
     return out, lse
 
 

@@ -1,0 +1,88 @@
+// Uniform multi-token decode (mla_decode_multi_token).
+//
+// vLLM mla_attention API docs, QueryLenSupport.UNIFORM: every request has the
+// same query length T > 1 (speculative decoding), and the query block is
+// causal unless the attention group allows a non-causal one
+// (MLACommonMetadataBuilder.build). The T new tokens are in the cache already,
+// so query token i of a request with L tokens sits at position L - T + i and,
+// causally, sees the first L - T + 1 + i tokens.
+//
+// Each (request, query token) becomes one row of the decode: a small kernel
+// writes, into caller scratch, row r = b * T + i's block-table row (a copy of
+// request b's) and its visible length, and the decode runs over the B * T
+// rows, whose q, out and lse are already laid out row after row in the
+// caller's [B, T, N, ...] tensors. Every row reads its request's pages, so
+// this version reads a request's cache T times.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+__global__ void mla_expand_rows_kernel(const int32_t* __restrict__ block_table,
+                                       const int32_t* __restrict__ seq_lens, int q_len,
+                                       int causal, int max_blocks, int32_t* __restrict__ table_out,
+                                       int32_t* __restrict__ lens_out) {
+    const int r = blockIdx.x;
+    const int b = r / q_len;
+    const int i = r - b * q_len;
+    const int32_t* src = block_table + int64_t(b) * max_blocks;
+    int32_t* dst = table_out + int64_t(r) * max_blocks;
+    for (int j = threadIdx.x; j < max_blocks; j += blockDim.x) dst[j] = src[j];
+    if (threadIdx.x == 0) {
+        const int L = seq_lens[b];
+        int eff = L;
+        // A length outside [0, max_blocks * 64] passes through unchanged so
+        // that the decode reports it (MLA_ERR_BAD_SEQ_LEN).
+        if (causal && L >= 0 && int64_t(L) <= int64_t(max_blocks) * kPageSize) {
+            eff = L - (q_len - 1 - i);
+            if (eff < 0) eff = 0;
+        }
+        lens_out[r] = eff;
+    }
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" size_t mla_multi_token_scratch_bytes(int batch, int q_len, int max_blocks_per_seq) {
+    if (batch < 0 || q_len < 1 || max_blocks_per_seq < 1) return 0;
+    const size_t rows = size_t(batch) * size_t(q_len);
+    return round256(rows * size_t(max_blocks_per_seq) * 4) + round256(rows * 4);
+}
+
+extern "C" int mla_decode_multi_token(const mla_decode_plan_t* plan, int q_len, int causal,
+                                      const void* q, const void* latent_cache,
+                                      int64_t num_blocks, const int32_t* block_table,
+                                      const int32_t* seq_lens, float softmax_scale, void* out,
+                                      float* lse, void* workspace, size_t workspace_bytes,
+                                      void* scratch, size_t scratch_bytes, void* stream) {
+    if (!plan || q_len < 1 || plan->batch < 0 || plan->batch % q_len != 0)
+        return MLA_ERR_INVALID_ARG;
+    const int batch = plan->batch / q_len;
+    if (batch == 0) return MLA_OK;
+    if (!block_table || !seq_lens) return MLA_ERR_INVALID_ARG;
+    const int max_blocks = plan->max_blocks_per_seq;
+    const size_t need = mla_multi_token_scratch_bytes(batch, q_len, max_blocks);
+    if (need == 0) return MLA_ERR_INVALID_ARG;
+    if (!scratch || scratch_bytes < need || (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
+        return MLA_ERR_WORKSPACE;
+    const size_t rows = size_t(batch) * size_t(q_len);
+    int32_t* table_rows = static_cast<int32_t*>(scratch);
+    int32_t* lens_rows = reinterpret_cast<int32_t*>(static_cast<char*>(scratch) +
+                                                    round256(rows * size_t(max_blocks) * 4));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    mla_expand_rows_kernel<<<unsigned(rows), 128, 0, st>>>(block_table, seq_lens, q_len,
+                                                           causal ? 1 : 0, max_blocks,
+                                                           table_rows, lens_rows);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    return mla_decode(plan, q, latent_cache, num_blocks, table_rows, lens_rows, softmax_scale,
+                      out, lse, workspace, workspace_bytes, stream);
+}

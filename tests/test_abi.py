@@ -23,7 +23,7 @@ def lib():
 
 def _declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(mla_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(mla_\w+)\s*\(", text, re.M)))
 
 
 def test_every_declared_function_is_exported(lib):
@@ -230,6 +230,39 @@ def test_front_end_and_up_projection_reject_bad_arguments(lib):
     assert up(fake, null, 2, 4, fake, ws, big, null) == binding.MLA_ERR_INVALID_ARG
     assert up(fake, fake, 2, 4, fake, null, big, null) == binding.MLA_ERR_WORKSPACE
     assert up(fake, fake, 2, 4, odd, ws, big, null) == binding.MLA_ERR_INVALID_ARG
+
+
+def test_multi_token_scratch_size_and_argument_checks(lib):
+    assert lib.mla_multi_token_scratch_bytes(3, 2, 10) == 256 + 256      # 240 B + 24 B, each rounded
+    assert lib.mla_multi_token_scratch_bytes(64, 4, 128) == 64 * 4 * 128 * 4 + 1024
+    assert lib.mla_multi_token_scratch_bytes(3, 0, 10) == 0
+    assert lib.mla_multi_token_scratch_bytes(-1, 2, 10) == 0
+    plan = binding.make_plan(6, 128, 4, num_sms=152)
+    fake = ctypes.c_void_p(0x10000)
+    null = ctypes.c_void_p(0)
+    call = lib.mla_decode_multi_token
+    args = lambda q_len, scratch, nbytes: (ctypes.byref(plan), q_len, 1, fake, fake, 8, fake,
+                                           fake, 0.1, fake, null, fake, 1 << 20, scratch, nbytes,
+                                           null)
+    assert call(*args(4, fake, 1 << 20)) == binding.MLA_ERR_INVALID_ARG     # 6 rows, T = 4
+    assert call(*args(0, fake, 1 << 20)) == binding.MLA_ERR_INVALID_ARG
+    assert call(*args(3, null, 1 << 20)) == binding.MLA_ERR_WORKSPACE
+    assert call(*args(3, fake, 64)) == binding.MLA_ERR_WORKSPACE
+    assert call(*args(3, ctypes.c_void_p(0x10010), 1 << 20)) == binding.MLA_ERR_WORKSPACE
+
+
+def test_multi_token_row_lengths_match_the_oracle_visibility():
+    """Host row lengths (used for the plan) against counting, per row, the
+    tokens the oracle's definition lets query token i see."""
+    lens = [0, 1, 2, 3, 5, 64, 100]
+    for T in [1, 2, 3, 4]:
+        for causal in [True, False]:
+            got = binding.multi_token_row_lens(lens, T, causal)
+            want = []
+            for L in lens:
+                for i in range(T):
+                    want.append(sum(1 for t in range(L) if (not causal) or t <= L - T + i))
+            np.testing.assert_array_equal(got, want)
 
 
 def test_status_strings(lib):

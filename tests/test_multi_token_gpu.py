@@ -1,0 +1,57 @@
+"""Uniform multi-token decode through the C ABI against the oracle.
+
+vLLM mla_attention API docs, QueryLenSupport.UNIFORM: every request has T
+query tokens at positions L - T .. L - 1; causal blocks see the tokens up to
+their own position, non-causal blocks see all L. Ragged lengths include
+requests shorter than T (rows that see nothing: zero output, -inf LSE).
+"""
+
+import numpy as np
+import pytest
+
+from mla_latent_cache_paged_gb300 import binding
+from mla_latent_cache_paged_gb300.workloads import (bf16_bits_to_f64, bf16_tensor_bits,
+                                                    f32_to_bf16_bits, make_workload, to_torch)
+from oracle import mla_decode_multi_token_reference
+from parity_util import assert_lse_close, assert_out_close, value_abs_max
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, T, causal, q_bits, **plan_kw):
+    import torch
+    _, cache, table, lens = to_torch(w)
+    q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    plan = binding.make_plan_multi_token(w.batch, T, w.num_heads, w.max_blocks_per_seq,
+                                         seq_lens_host=w.seq_lens, causal=causal, **plan_kw)
+    ws = binding.new_workspace(plan)
+    out, lse = binding.mla_decode_multi_token(q, cache, table, lens, w.softmax_scale,
+                                              causal=causal, plan=plan, workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.read_error(ws) == 0
+    return bf16_bits_to_f64(bf16_tensor_bits(out)), lse.double().cpu().numpy(), plan
+
+
+@pytest.mark.parametrize("T,causal,N,plan_kw", [
+    (2, True, 128, {}),
+    (3, False, 16, {}),
+    (4, True, 128, {"num_kv_splits": 4}),
+    (2, True, 64, {"schedule": "balanced"}),
+    (3, True, 128, {"num_kv_splits": 1}),
+])
+def test_multi_token_against_the_oracle(T, causal, N, plan_kw):
+    lens = [1, 2, 63, 64, 65, 300, 1000]
+    w = make_workload("mt", len(lens), N, lens, seed=1400 + 10 * T + N)
+    rng = np.random.default_rng(1500 + T)
+    q_bits = f32_to_bf16_bits(rng.standard_normal((len(lens), T, N, 576)).astype(np.float32))
+    got, lse, plan = _run(w, T, causal, q_bits, **plan_kw)
+    ref, ref_lse = mla_decode_multi_token_reference(bf16_bits_to_f64(q_bits), w.cache_f64(),
+                                                    w.block_table, w.seq_lens, w.softmax_scale,
+                                                    causal=causal)
+    vmax = value_abs_max(w, range(w.batch))[:, None]           # [B, 1, 1, 512]
+    assert_out_close(got, ref, f"T={T} causal={causal}", vmax)
+    assert_lse_close(lse, ref_lse, "multi-token lse")
+    if causal:
+        # The one-token request: only its last query token sees anything.
+        assert np.isneginf(lse[0, :T - 1]).all() and np.isfinite(lse[0, T - 1]).all()
+        assert (got[0, :T - 1] == 0).all()
