@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--dcp-world", type=int, default=2,
+                    help="ranks whose results --stage dcp_combine merges")
     ap.add_argument("--q-len", type=int, default=2,
                     help="query tokens per request for --stage multi_token")
     ap.add_argument("--stage", choices=["decode"] + sorted(STAGES), default="decode",
@@ -248,9 +250,14 @@ STAGES = {
     "front_end": "MLA decode front end (q absorption by W_UK_T, q_pe concat, latent cache "
                  "insert), one launch",
     "v_up_proj": "MLA up-projection of the decode output by W_UV, one launch",
+    "dcp_combine": "MLA decode-context-parallel combine of --dcp-world ranks' bf16 results, "
+                   "one launch",
     "multi_token": "MLA uniform multi-token decode (causal query block of --q-len tokens per "
                    "request)",
 }
+
+
+world_of_stage = 2
 
 
 def stage_work(stage, batch, heads):
@@ -264,6 +271,10 @@ def stage_work(stage, batch, heads):
     if stage == "front_end":
         nbytes = 2 * (heads * 128 * 512 + batch * heads * 192 + batch * heads * 576 +
                       2 * batch * 576) + 8 * batch
+    elif stage == "dcp_combine":
+        # R ranks' bf16 rows and fp32 LSEs read, one bf16 row and LSE written.
+        world = world_of_stage
+        return (world + 1) * batch * heads * (1024 + 4), 0
     else:
         nbytes = 2 * (batch * heads * 512 + heads * 512 * 128 + batch * heads * 128)
     return nbytes, 2 * batch * heads * 128 * 512
@@ -372,7 +383,19 @@ def run_stage(args, stage):
 
     ws = binding.new_status_workspace(dev)
     sets = []
-    if stage == "front_end":
+    if stage == "dcp_combine":
+        R = world_of_stage
+        for i in range(nsets):
+            lse_parts = torch.randn((R, B, N), generator=gen, device=dev) * 3
+            lse_parts[:, :, ::7] = float("-inf")   # some ranks without tokens of a row
+            sets.append(dict(o=rnd((R, B, N, 512)), lse=lse_parts,
+                             out=torch.empty((B, N, 512), dtype=torch.bfloat16, device=dev),
+                             lse_out=torch.empty((B, N), dtype=torch.float32, device=dev)))
+
+        def call(i):
+            t = sets[i % nsets]
+            binding.mla_dcp_combine(t["o"], t["lse"], out=t["out"], lse=t["lse_out"])
+    elif stage == "front_end":
         blocks = -(-B // 64)
         cache = rnd((blocks * nsets, 64, 576))
         for i in range(nsets):
@@ -432,6 +455,7 @@ def run_stage(args, stage):
                      "algorithmic_bytes_per_launch": nbytes,
                      "tensor_achieved_tflops": flops / (ms / 1e3) / 1e12,
                      "tensor_peak_tflops": peaks["bf16_tflops"]},
+        **({"dcp_world": world_of_stage} if stage == "dcp_combine" else {}),
         "gpu_launches": steps,
         "clocks": clocks,
     }
@@ -649,6 +673,8 @@ def main():
     if args.stage != "decode":
         if world > 1:
             raise SystemExit("--stage runs on one GPU")
+        global world_of_stage
+        world_of_stage = args.dcp_world
         res = run_multi_token(args) if args.stage == "multi_token" else run_stage(args, args.stage)
         print(json.dumps(res), flush=True)
         return 0

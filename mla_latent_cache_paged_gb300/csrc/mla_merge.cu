@@ -24,7 +24,8 @@ constexpr int kRowsPerCta = kMergeThreads / 32;
 // per row, so the value columns are then cut into 128-wide groups, one per
 // CTA row of the grid: CTA (x, y) covers rows 8x..8x+7 and columns
 // 128y..128y+127, and each warp keeps four partials' loads in flight.
-// Otherwise CTA x covers rows 8x..8x+7 and each warp walks its whole row.
+// Otherwise CTA x covers rows 8x..8x+7 and each warp walks its whole row
+// (with at most 4 partials, issuing all of its loads first).
 // Every warp first forms its row's LSE and the S weights; a partial with
 // weight 0 (an empty split, a rank without tokens) is never read.
 //
@@ -59,7 +60,11 @@ __device__ __forceinline__ void store_bf16x4(uint16_t* p, float4 r) {
     *reinterpret_cast<uint2*>(p) = packed;
 }
 
-template <typename TP, bool kColumnGroups>
+// Row layouts with at most 4 partials of 512 values: a lane issues the loads
+// of two column groups for every partial (8) before using any.
+constexpr int kFewSplits = 4;
+
+template <typename TP, int kMode>   // 0: whole rows, 1: column groups, 2: few partials
 __global__ void __launch_bounds__(kMergeThreads, 4) mla_merge_kernel(const TP* __restrict__ o_part,
                                                                    const MergeArgs a) {
     __shared__ float weights[kRowsPerCta][kMaxMergeSplits];
@@ -92,7 +97,34 @@ __global__ void __launch_bounds__(kMergeThreads, 4) mla_merge_kernel(const TP* _
 
     const TP* base = o_part + row * a.o_row;
     uint16_t* dst = a.out + size_t(row) * a.v_dim;
-    if constexpr (kColumnGroups) {
+    if constexpr (kMode == 2) {
+        float wk[kFewSplits];
+#pragma unroll
+        for (int k = 0; k < kFewSplits; ++k) wk[k] = k < S ? w[k] : 0.f;
+#pragma unroll
+        for (int g0 = 0; g0 < 4; g0 += 2) {   // two column groups' loads at a time
+            float4 v[2][kFewSplits];
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+#pragma unroll
+                for (int k = 0; k < kFewSplits; ++k)
+                    v[g][k] = wk[k] != 0.f
+                                  ? load_partial4(base + k * a.o_split + (g0 + g) * 128 + lane * 4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < kFewSplits; ++k) {
+                    acc.x = fmaf(wk[k], v[g][k].x, acc.x);
+                    acc.y = fmaf(wk[k], v[g][k].y, acc.y);
+                    acc.z = fmaf(wk[k], v[g][k].z, acc.z);
+                    acc.w = fmaf(wk[k], v[g][k].w, acc.w);
+                }
+                store_bf16x4(dst + (g0 + g) * 128 + lane * 4, acc);
+            }
+        }
+    } else if constexpr (kMode == 1) {
         const int d = int(blockIdx.y) * 128 + lane * 4;
         if (d >= a.v_dim) return;
         float4 acc[4];
@@ -145,10 +177,12 @@ int launch_merge_strided(const TP* o_part, const MergeArgs& a, cudaStream_t st) 
         return int(cudaErrorInvalidValue);
     const dim3 rows_grid((a.rows + kRowsPerCta - 1) / kRowsPerCta);
     if (a.rows < kChunkedMergeRows)
-        mla_merge_kernel<TP, true>
+        mla_merge_kernel<TP, 1>
                 <<<dim3(rows_grid.x, (a.v_dim + 127) / 128), kMergeThreads, 0, st>>>(o_part, a);
+    else if (a.S <= kFewSplits && a.v_dim == 512)
+        mla_merge_kernel<TP, 2><<<rows_grid, kMergeThreads, 0, st>>>(o_part, a);
     else
-        mla_merge_kernel<TP, false><<<rows_grid, kMergeThreads, 0, st>>>(o_part, a);
+        mla_merge_kernel<TP, 0><<<rows_grid, kMergeThreads, 0, st>>>(o_part, a);
     return int(cudaGetLastError());
 }
 

@@ -97,7 +97,7 @@ def _bf16(x):
 
 @pytest.mark.parametrize("world,batch,heads,v_dim", [
     (1, 2, 8, 512), (2, 3, 16, 512), (8, 2, 5, 136), (3, 17, 128, 512), (5, 20, 128, 8),
-    (4, 2, 3, 1032)])
+    (4, 2, 3, 1032), (2, 17, 128, 512), (1, 17, 128, 512)])
 def test_dcp_combine_against_the_oracle(world, batch, heads, v_dim):
     """Combine of bf16 rank results, both grid shapes (rows below and above 2048)."""
     import torch
@@ -125,7 +125,9 @@ def test_dcp_combine_against_the_oracle(world, batch, heads, v_dim):
 
 
 @pytest.mark.parametrize("batch,heads,S,v_dim", [(2, 6, 5, 8), (3, 4, 7, 136),
-                                                 (17, 128, 3, 136), (2, 2, 4, 2048)])
+                                                 (17, 128, 3, 136), (2, 2, 4, 2048),
+                                                 (17, 128, 2, 512), (16, 128, 4, 512),
+                                                 (17, 128, 5, 512)])
 def test_merge_splits_at_other_widths(batch, heads, S, v_dim):
     import torch
     rng = np.random.default_rng(S * 7 + v_dim)
