@@ -255,24 +255,30 @@ int mla_merge_splits(const float* o_part, const float* lse_part, int batch, int 
  * that sees none, when L < T - i, gets out = 0, lse = -inf); otherwise to all
  * t < L.
  *
- *   plan          from mla_decode_plan with batch = B * T rows (row
- *                 r = b * T + i) and, if given, the host lengths of those
- *                 rows (the visible lengths above).
+ *   plan          one of two shapes, which selects how the work is laid out:
+ *                 (a) T * N <= 128: mla_decode_plan with batch = B and
+ *                     num_heads = T * N (the tokens' heads are the rows of
+ *                     one decode, which reads each page once; host lengths,
+ *                     if given, are the requests' lengths);
+ *                 (b) mla_decode_plan with batch = B * T rows (row
+ *                     r = b * T + i) of N heads and, if given, the host
+ *                     lengths of those rows (the visible lengths above).
+ *   num_heads     N, the heads of one query token.
  *   q             device, bf16 [B, T, N, 576] contiguous.
  *   block_table   device, int32 [B, max_blocks_per_seq]; seq_lens int32 [B].
  *   out, lse      device, bf16 [B, T, N, 512] and fp32 [B, T, N] (or NULL).
  *   workspace     as for mla_decode with this plan.
- *   scratch       device, >= mla_multi_token_scratch_bytes(B, T,
- *                 max_blocks_per_seq) bytes, 256-byte aligned: the rows'
- *                 block tables and lengths.
- * One small launch that writes the rows' block tables and lengths into
- * `scratch`, then mla_decode over the B * T rows (each row reads its
- * request's pages). Errors as mla_decode; plan->batch not a multiple of
- * q_len or q_len < 1 gives MLA_ERR_INVALID_ARG, scratch too small or
- * misaligned MLA_ERR_WORKSPACE.
+ *   scratch       shape (b) only (else may be NULL): device, >=
+ *                 mla_multi_token_scratch_bytes(B, T, max_blocks_per_seq)
+ *                 bytes, 256-byte aligned: the rows' block tables and lengths.
+ * Shape (a) is one mla_decode launch (plus its merge); shape (b) one small
+ * launch that writes the rows' block tables and lengths into `scratch`, then
+ * mla_decode over the B * T rows (each row reads its request's pages).
+ * Errors as mla_decode; a plan of neither shape or q_len < 1 gives
+ * MLA_ERR_INVALID_ARG, scratch too small or misaligned MLA_ERR_WORKSPACE.
  */
 size_t mla_multi_token_scratch_bytes(int batch, int q_len, int max_blocks_per_seq);
-int mla_decode_multi_token(const mla_decode_plan_t* plan, int q_len, int causal,
+int mla_decode_multi_token(const mla_decode_plan_t* plan, int q_len, int num_heads, int causal,
                            const void* q, const void* latent_cache, int64_t num_blocks,
                            const int32_t* block_table, const int32_t* seq_lens,
                            float softmax_scale, void* out, float* lse, void* workspace,

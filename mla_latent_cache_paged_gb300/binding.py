@@ -108,8 +108,8 @@ def load_library(path=None):
                                               vp]
     lib.mla_v_up_proj.argtypes = [vp, vp, i32, i32, vp, vp, sz, vp]
     lib.mla_multi_token_scratch_bytes.argtypes = [i32, i32, i32]
-    lib.mla_decode_multi_token.argtypes = [ctypes.POINTER(MlaDecodePlan), i32, i32, vp, vp, i64,
-                                           vp, vp, f32, vp, vp, vp, sz, vp, sz, vp]
+    lib.mla_decode_multi_token.argtypes = [ctypes.POINTER(MlaDecodePlan), i32, i32, i32, vp, vp,
+                                           i64, vp, vp, f32, vp, vp, vp, sz, vp, sz, vp]
     for name in EXPORTED_SYMBOLS:
         if name not in ("mla_status_string", "mla_multi_token_scratch_bytes"):
             getattr(lib, name).restype = ctypes.c_int
@@ -252,8 +252,16 @@ def multi_token_row_lens(seq_lens_host, q_len, causal=True):
 
 
 def make_plan_multi_token(batch, q_len, num_heads, max_blocks_per_seq, *, seq_lens_host=None,
-                          causal=True, **kw):
-    """A plan over the B * T rows of a uniform multi-token decode."""
+                          causal=True, expand=None, **kw):
+    """A plan for a uniform multi-token decode: the T query tokens' heads as
+    the rows of one decode when T * N <= 128 (each page read once), else
+    B * T rows of N heads. ``expand=True`` forces the second form."""
+    if expand is None:
+        expand = int(q_len) * int(num_heads) > 128
+    if not expand:
+        if seq_lens_host is not None:
+            kw["seq_lens_host"] = seq_lens_host
+        return make_plan(batch, int(q_len) * int(num_heads), max_blocks_per_seq, **kw)
     if seq_lens_host is not None:
         rows = multi_token_row_lens(seq_lens_host, q_len, causal)
         kw.setdefault("max_seq_len", int(rows.max()) if rows.size else 0)
@@ -289,14 +297,14 @@ def mla_decode_multi_token(q, latent_cache, block_table, seq_lens, softmax_scale
     if workspace is None:
         workspace = new_workspace(plan, q.device, stream)
     lib = load_library()
-    if scratch is None:
+    if scratch is None and plan.num_heads != T * N:
         nbytes = int(lib.mla_multi_token_scratch_bytes(B, T, block_table.shape[1]))
         scratch = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
     rc = lib.mla_decode_multi_token(
-        ctypes.byref(plan), int(T), 1 if causal else 0, _ptr(q), _ptr(latent_cache),
+        ctypes.byref(plan), int(T), int(N), 1 if causal else 0, _ptr(q), _ptr(latent_cache),
         int(latent_cache.shape[0]), _ptr(block_table), _ptr(seq_lens), float(softmax_scale),
         _ptr(out), _ptr(lse), _ptr(workspace), int(workspace.numel()), _ptr(scratch),
-        int(scratch.numel()), _stream_ptr(stream))
+        int(scratch.numel()) if scratch is not None else 0, _stream_ptr(stream))
     _check(rc, "mla_decode_multi_token")
     return out, lse
 

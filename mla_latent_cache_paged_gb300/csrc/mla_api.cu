@@ -26,10 +26,13 @@ extern "C" int mla_workspace_init(void* workspace, size_t workspace_bytes, void*
                                            static_cast<cudaStream_t>(stream))));
 }
 
-extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
-                          int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
-                          float softmax_scale, void* out, float* lse, void* workspace,
-                          size_t workspace_bytes, void* stream) {
+namespace mla {
+
+int decode_impl(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
+                int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                float softmax_scale, void* out, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream, int q_len, int heads_per_token,
+                int causal) {
     int rc = validate_plan(plan);
     if (rc != MLA_OK) return rc;
     if (!q || !latent_cache || !block_table || !seq_lens || !out) return MLA_ERR_INVALID_ARG;
@@ -63,6 +66,9 @@ extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const vo
     p.lse = lse;
     p.status = reinterpret_cast<int32_t*>(ws);
     p.sched_pairs = plan->sched_pairs;
+    p.q_len = q_len;
+    p.heads_per_token = heads_per_token;
+    p.causal = causal;
     if (S > 1 || plan->sched_pairs > 0) {
         p.o_part = reinterpret_cast<float*>(ws + plan->partial_offset);
         p.lse_part = reinterpret_cast<float*>(ws + plan->lse_partial_offset);
@@ -79,6 +85,17 @@ extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const vo
         if (e != 0) return MLA_ERR_CUDA;
     }
     return MLA_OK;
+}
+
+}  // namespace mla
+
+extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
+                          int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                          float softmax_scale, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    return decode_impl(plan, q, latent_cache, num_blocks, block_table, seq_lens, softmax_scale,
+                       out, lse, workspace, workspace_bytes, stream, 1,
+                       plan ? plan->num_heads : 1, 0);
 }
 
 extern "C" int mla_merge_splits(const float* o_part, const float* lse_part, int batch,

@@ -140,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 2) mla_decode_simt_kernel(DecodePara
             float s = 0.f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) s += sm.red[w][h][t];
-            sm.ps[h][t] = (c0 + t < t_hi) ? s * p.scale_log2 : -INFINITY;
+            const bool seen = c0 + t < t_hi && c0 + t < L - row_shift(p, h0 + h);
+            sm.ps[h][t] = seen ? s * p.scale_log2 : -INFINITY;
         }
         __syncthreads();
 

@@ -176,6 +176,7 @@ __host__ __device__ constexpr int k_block(int rank, int pos) {
 // (the page offsets pfx[b] = pages of requests 0..b-1 are in shared memory).
 struct Segment {
     int b;
+    int L;             // the request's length (multi-token rows end before it)
     int t_lo, t_hi;
     int prow0;         // partial row of head 0, or -1: write out / lse directly
     int prow_stride;   // partial rows from one head to the next
@@ -223,7 +224,8 @@ __device__ __forceinline__ bool walk_next(const DecodeParams& p, const int32_t* 
         const int64_t item = w.g0++;
         const int split = int(item % S);
         s.b = int(item / S);
-        split_range(checked_seq_len(p, s.b), S, split, &s.t_lo, &s.t_hi);
+        s.L = checked_seq_len(p, s.b);
+        split_range(s.L, S, split, &s.t_lo, &s.t_hi);
         s.prow0 = S == 1 ? -1 : s.b * p.num_heads * S + split;
         s.prow_stride = S;
         return true;
@@ -237,6 +239,7 @@ __device__ __forceinline__ bool walk_next(const DecodeParams& p, const int32_t* 
         const int64_t hi = pe < w.g1 ? pe : w.g1;
         if (lo >= hi) continue;   // only the fixed cost falls in this range
         s.b = b;
+        s.L = p.seq_lens[b];
         s.t_lo = int(lo - pb) * kPageSize;
         s.t_hi = min(p.seq_lens[b], int(hi - pb) * kPageSize);
         s.prow0 = (lo == pb && hi == pe) ? -1 : (w.first ? 2 * pair : 2 * pair + 1) * p.num_heads;
@@ -652,6 +655,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
         const int h = quarter * 32 + lane;
         const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
         const bool live_head = h < N;
+        const int shift = row_shift(p, h);   // multi-token rows: tokens past this row's end
         bool issued_pv = false;
         bool ok = true;
         // q of request qb, copied with coalesced 16-byte cp.async (a warp
@@ -749,6 +753,11 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 // score that scales to -inf.
                 const uint32_t sbuf = trow + kTmemS + uint32_t(sl * 64);
                 const int valid = min(kTile, sg.t_hi - (sg.t_lo + j * kTile));
+                // This row's visible tokens on the page (fewer for an earlier
+                // query token of a causal multi-token block; possibly none).
+                const int valid_row =
+                    shift == 0 ? valid
+                               : min(valid, sg.L - shift - (sg.t_lo + j * kTile));
                 const float sc = p.scale_log2;
                 float x[64];
                 {
@@ -757,10 +766,10 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
 #pragma unroll
                     for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(r[i]);
                 }
-                if (valid < kTile) {
+                if (valid_row < kTile) {
                     const float masked = sc > 0.f ? -INFINITY : INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) x[i] = i < valid ? x[i] : masked;
+                    for (int i = 0; i < 64; ++i) x[i] = i < valid_row ? x[i] : masked;
                 }
                 float mx;
                 if (sc > 0.f) {
@@ -790,7 +799,10 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 float2 lb2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 {
-                    const float2 negm2 = make_float2(-m_ref, -m_ref);
+                    // A row that has seen no token yet keeps m_ref = -inf:
+                    // its weights are exp2(-inf) = 0, not NaN.
+                    const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;
+                    const float2 negm2 = make_float2(mneg, mneg);
                     const float2 sc2 = make_float2(sc, sc);
                     uint32_t pk[32];
 #pragma unroll

@@ -17,6 +17,13 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits_rn(float f) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
+// Tokens row h must not see at the end of its request (multi-token rows).
+__device__ __forceinline__ int row_shift(const DecodeParams& p, int h) {
+    if (p.q_len <= 1 || !p.causal) return 0;
+    const int tok = h / p.heads_per_token;
+    return tok < p.q_len ? p.q_len - 1 - tok : 0;
+}
+
 // Record the first device-side error of a call; later ones are dropped.
 __device__ __forceinline__ void record_error(int32_t* status, int32_t code, int32_t detail) {
     if (status != nullptr && atomicCAS(status, 0, code) == 0) {

@@ -58,7 +58,15 @@ struct DecodeParams {
                                   //                    or [2 * pairs, N, 512] (balanced)
     float* lse_part;              // fp32 [B, N, S] or [2 * pairs, N]
     int32_t* status;              // status header in the workspace
+    // Uniform multi-token decode with the query tokens' heads as rows: row h
+    // is head h % heads_per_token of query token h / heads_per_token; with
+    // `causal` that token sees q_len - 1 - token fewer of the request's
+    // tokens. A plain decode has q_len = 1.
+    int32_t q_len;
+    int32_t heads_per_token;
+    int32_t causal;
 };
+
 
 // Launchers (return a cudaError_t as int; 0 = success).
 int launch_decode_simt(const DecodeParams& p, void* stream);
@@ -73,6 +81,14 @@ int launch_merge_balanced(const DecodeParams& p, void* stream);
 int launch_gather(const uint16_t* cache, int64_t num_blocks, const int32_t* block_table,
                   const int32_t* seq_lens, int batch, int max_blocks, int dst_max_tokens,
                   uint16_t* dst, int32_t* status, void* stream);
+
+// mla_decode with multi-token rows (q_len query tokens' heads as the rows;
+// q_len = 1 is the plain decode).
+int decode_impl(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
+                int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                float softmax_scale, void* out, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream, int q_len, int heads_per_token,
+                int causal);
 
 // Host-side helpers from mla_plan.cpp.
 int validate_plan(const mla_decode_plan_t* plan);

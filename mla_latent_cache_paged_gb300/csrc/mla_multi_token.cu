@@ -7,12 +7,18 @@
 // so query token i of a request with L tokens sits at position L - T + i and,
 // causally, sees the first L - T + 1 + i tokens.
 //
-// Each (request, query token) becomes one row of the decode: a small kernel
-// writes, into caller scratch, row r = b * T + i's block-table row (a copy of
-// request b's) and its visible length, and the decode runs over the B * T
-// rows, whose q, out and lse are already laid out row after row in the
-// caller's [B, T, N, ...] tensors. Every row reads its request's pages, so
-// this version reads a request's cache T times.
+// Two ways, chosen by the plan's shape:
+//   * T * N <= 128 (the plan has T * N heads): q [B, T, N, 576] is q [B, T * N,
+//     576], so the T query tokens' heads are the rows of one decode, which
+//     reads each page once; the kernels end each row's tokens at its own
+//     causal limit.
+//   * otherwise (the plan has B * T rows of N heads): each (request, query
+//     token) becomes a row of the decode: a small kernel writes, into caller
+//     scratch, row r = b * T + i's block-table row (a copy of request b's) and
+//     its visible length, and the decode runs over the B * T rows, whose q,
+//     out and lse are already laid out row after row in the caller's tensors.
+//     Every row reads its request's pages, so a request's cache is read T
+//     times.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -58,14 +64,18 @@ extern "C" size_t mla_multi_token_scratch_bytes(int batch, int q_len, int max_bl
     return round256(rows * size_t(max_blocks_per_seq) * 4) + round256(rows * 4);
 }
 
-extern "C" int mla_decode_multi_token(const mla_decode_plan_t* plan, int q_len, int causal,
-                                      const void* q, const void* latent_cache,
+extern "C" int mla_decode_multi_token(const mla_decode_plan_t* plan, int q_len, int num_heads,
+                                      int causal, const void* q, const void* latent_cache,
                                       int64_t num_blocks, const int32_t* block_table,
                                       const int32_t* seq_lens, float softmax_scale, void* out,
                                       float* lse, void* workspace, size_t workspace_bytes,
                                       void* scratch, size_t scratch_bytes, void* stream) {
-    if (!plan || q_len < 1 || plan->batch < 0 || plan->batch % q_len != 0)
-        return MLA_ERR_INVALID_ARG;
+    if (!plan || q_len < 1 || num_heads < 1 || plan->batch < 0) return MLA_ERR_INVALID_ARG;
+    if (int64_t(plan->num_heads) == int64_t(q_len) * num_heads)   // the tokens' heads as rows
+        return decode_impl(plan, q, latent_cache, num_blocks, block_table, seq_lens,
+                           softmax_scale, out, lse, workspace, workspace_bytes, stream, q_len,
+                           num_heads, causal ? 1 : 0);
+    if (plan->num_heads != num_heads || plan->batch % q_len != 0) return MLA_ERR_INVALID_ARG;
     const int batch = plan->batch / q_len;
     if (batch == 0) return MLA_OK;
     if (!block_table || !seq_lens) return MLA_ERR_INVALID_ARG;

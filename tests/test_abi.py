@@ -241,14 +241,17 @@ def test_multi_token_scratch_size_and_argument_checks(lib):
     fake = ctypes.c_void_p(0x10000)
     null = ctypes.c_void_p(0)
     call = lib.mla_decode_multi_token
-    args = lambda q_len, scratch, nbytes: (ctypes.byref(plan), q_len, 1, fake, fake, 8, fake,
-                                           fake, 0.1, fake, null, fake, 1 << 20, scratch, nbytes,
-                                           null)
+    # A plan of 6 rows of 128 heads: the B * T-row form (T * N = 128 * T > 128).
+    args = lambda q_len, scratch, nbytes, n=128: (ctypes.byref(plan), q_len, n, 1, fake, fake, 8,
+                                                  fake, fake, 0.1, fake, null, fake, 1 << 20,
+                                                  scratch, nbytes, null)
     assert call(*args(4, fake, 1 << 20)) == binding.MLA_ERR_INVALID_ARG     # 6 rows, T = 4
     assert call(*args(0, fake, 1 << 20)) == binding.MLA_ERR_INVALID_ARG
     assert call(*args(3, null, 1 << 20)) == binding.MLA_ERR_WORKSPACE
     assert call(*args(3, fake, 64)) == binding.MLA_ERR_WORKSPACE
     assert call(*args(3, ctypes.c_void_p(0x10010), 1 << 20)) == binding.MLA_ERR_WORKSPACE
+    assert call(*args(3, fake, 1 << 20, n=0)) == binding.MLA_ERR_INVALID_ARG
+    assert call(*args(3, fake, 1 << 20, n=64)) == binding.MLA_ERR_INVALID_ARG   # neither shape
 
 
 def test_multi_token_row_lengths_match_the_oracle_visibility():

@@ -33,11 +33,19 @@ def _run(w, T, causal, q_bits, **plan_kw):
 
 
 @pytest.mark.parametrize("T,causal,N,plan_kw", [
+    # T * N > 128: B * T rows of N heads.
     (2, True, 128, {}),
-    (3, False, 16, {}),
     (4, True, 128, {"num_kv_splits": 4}),
-    (2, True, 64, {"schedule": "balanced"}),
     (3, True, 128, {"num_kv_splits": 1}),
+    (2, True, 64, {"schedule": "balanced", "expand": True}),
+    # T * N <= 128: the tokens' heads as the rows of one decode.
+    (3, False, 16, {}),
+    (2, True, 64, {"schedule": "balanced"}),
+    (4, True, 16, {}),
+    (8, True, 16, {"num_kv_splits": 4}),
+    (3, True, 40, {"num_kv_splits": 1}),
+    (2, True, 32, {"force_simt": True}),
+    (4, True, 16, {"force_simt": True, "num_kv_splits": 3}),
 ])
 def test_multi_token_against_the_oracle(T, causal, N, plan_kw):
     lens = [1, 2, 63, 64, 65, 300, 1000]
@@ -45,6 +53,8 @@ def test_multi_token_against_the_oracle(T, causal, N, plan_kw):
     rng = np.random.default_rng(1500 + T)
     q_bits = f32_to_bf16_bits(rng.standard_normal((len(lens), T, N, 576)).astype(np.float32))
     got, lse, plan = _run(w, T, causal, q_bits, **plan_kw)
+    packed = T * N <= 128 and not plan_kw.get("expand", False)
+    assert (plan.num_heads, plan.batch) == ((T * N, w.batch) if packed else (N, w.batch * T))
     ref, ref_lse = mla_decode_multi_token_reference(bf16_bits_to_f64(q_bits), w.cache_f64(),
                                                     w.block_table, w.seq_lens, w.softmax_scale,
                                                     causal=causal)
