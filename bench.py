@@ -257,10 +257,7 @@ STAGES = {
 }
 
 
-world_of_stage = 2
-
-
-def stage_work(stage, batch, heads):
+def stage_work(stage, batch, heads, world=2):
     """Algorithmic bytes and flops of one call of a step around the decode.
 
     front end: W_UK_T (N*128*512 bf16) + q (B*N*192) + mqa_q written
@@ -272,8 +269,7 @@ def stage_work(stage, batch, heads):
         nbytes = 2 * (heads * 128 * 512 + batch * heads * 192 + batch * heads * 576 +
                       2 * batch * 576) + 8 * batch
     elif stage == "dcp_combine":
-        # R ranks' bf16 rows and fp32 LSEs read, one bf16 row and LSE written.
-        world = world_of_stage
+        # R = world ranks' bf16 rows and fp32 LSEs read, one bf16 row and LSE written.
         return (world + 1) * batch * heads * (1024 + 4), 0
     else:
         nbytes = 2 * (batch * heads * 512 + heads * 512 * 128 + batch * heads * 128)
@@ -373,7 +369,7 @@ def run_stage(args, stage):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    nbytes, flops = stage_work(stage, B, N)
+    nbytes, flops = stage_work(stage, B, N, args.dcp_world)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     nsets = max(2, -(-2 * l2 // nbytes) + 1)
     gen = torch.Generator(device=dev).manual_seed(20260100)
@@ -384,7 +380,7 @@ def run_stage(args, stage):
     ws = binding.new_status_workspace(dev)
     sets = []
     if stage == "dcp_combine":
-        R = world_of_stage
+        R = args.dcp_world
         for i in range(nsets):
             lse_parts = torch.randn((R, B, N), generator=gen, device=dev) * 3
             lse_parts[:, :, ::7] = float("-inf")   # some ranks without tokens of a row
@@ -455,7 +451,7 @@ def run_stage(args, stage):
                      "algorithmic_bytes_per_launch": nbytes,
                      "tensor_achieved_tflops": flops / (ms / 1e3) / 1e12,
                      "tensor_peak_tflops": peaks["bf16_tflops"]},
-        **({"dcp_world": world_of_stage} if stage == "dcp_combine" else {}),
+        **({"dcp_world": args.dcp_world} if stage == "dcp_combine" else {}),
         "gpu_launches": steps,
         "clocks": clocks,
     }
@@ -673,8 +669,6 @@ def main():
     if args.stage != "decode":
         if world > 1:
             raise SystemExit("--stage runs on one GPU")
-        global world_of_stage
-        world_of_stage = args.dcp_world
         res = run_multi_token(args) if args.stage == "multi_token" else run_stage(args, args.stage)
         print(json.dumps(res), flush=True)
         return 0
