@@ -19,8 +19,8 @@
 //     score tile is computed in both CTAs; that keeps the softmax local. q's
 //     dims 0..255 are the A operand in TMEM, dims 256..575 in shared memory.
 //   * Each page is TMA-loaded by both CTAs (the second read of a page is
-//     served from L2; each CTA also pulls half of a page four pages ahead
-//     into L2). Its 64-column blocks go to two page rings: this CTA's four
+//     served from L2; pulling pages into L2 ahead of the loads measured
+//     slower). Its 64-column blocks go to two page rings: this CTA's four
 //     value blocks to a V ring (kept until the P.V MMA of the page), the five
 //     other blocks to a K ring (released once the page's score MMAs finish).
 //   * Softmax: 128 threads, one per head (= TMEM lane), fp32, base 2 with the
@@ -66,8 +66,7 @@ constexpr int kBlockBytes = kTile * 128;       // 64 rows x 64 bf16 columns = 8 
 constexpr int kKPerPage = 5;                   // K-ring blocks per page
 constexpr int kVBytes = 4 * kBlockBytes;       // a page's four value blocks: 32 KB
 constexpr int kKBytes = kKPerPage * kBlockBytes;   // a page's five K-ring blocks: 40 KB
-constexpr int kPageBytes = kTile * kD * 2;     // one page of the cache: 73,728 contiguous bytes
-constexpr int kPrefetchAhead = 4;              // pages pulled into L2 ahead of their loads
+constexpr int kQPrefetchPages = 1;             // next request's q pulled into L2 this many pages early
 
 constexpr int kOffQS = 0;                      // q dims 256..575: 5 x [128 x 64] bf16, SW128
 constexpr int kOffV = 5 * 16384;               // V ring: 2 pages
@@ -573,17 +572,6 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 const int ntiles = seg_pages(sg);
                 const int page0 = sg.t_lo / kTile;
                 const int32_t* table = p.block_table + size_t(sg.b) * p.max_blocks;
-                // The K producer of each CTA pulls its half of page
-                // j + kPrefetchAhead into L2, so that the ring loads of both
-                // CTAs hit L2.
-                auto prefetch = [&](int j) {
-                    if (!k_ring || j >= ntiles) return;
-                    const int32_t blk = table[page0 + j];
-                    if (blk < 0 || int64_t(blk) >= p.num_blocks) return;
-                    const unsigned char* page =
-                        reinterpret_cast<const unsigned char*>(p.cache) + size_t(blk) * kPageBytes;
-                    ptx::prefetch_l2(page + rank * (kPageBytes / 2), kPageBytes / 2);
-                };
                 // q of the next segment's request into L2 (half per CTA) a
                 // few pages before this segment ends (earlier, the page
                 // stream would evict it), so that staging it is short.
@@ -601,14 +589,12 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                     const uint32_t half = (qbytes / 2) & ~15u;
                     ptx::prefetch_l2(qb + rank * half, rank == 0 ? half : qbytes - half);
                 };
-                if (ntiles <= kPrefetchAhead) prefetch_q();
-                for (int j = 0; j < kPrefetchAhead; ++j) prefetch(j);
+                if (ntiles <= kQPrefetchPages) prefetch_q();
                 int next = ntiles > 0 ? table[page0] : 0;
                 for (int j = 0; j < ntiles; ++j, ++jg) {
                     const int blk = next;
                     if (j + 1 < ntiles) next = table[page0 + j + 1];
-                    prefetch(j + kPrefetchAhead);
-                    if (j + kPrefetchAhead == ntiles) prefetch_q();
+                    if (j + kQPrefetchPages == ntiles) prefetch_q();
                     int32_t y;
                     if (blk >= 0 && int64_t(blk) < p.num_blocks) {
                         y = blk * kTile;
