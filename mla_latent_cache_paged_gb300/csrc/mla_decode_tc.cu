@@ -34,7 +34,7 @@
 // Two score buffers in TMEM let the score MMAs of the next page run while the
 // softmax works on the current one.
 //
-// Warp roles: 0 = K-ring loads (and L2 prefetch), 6 = V-ring loads,
+// Warp roles: 0 = K-ring loads (and the next q's L2 prefetch), 6 = V-ring loads,
 // 1 = score MMAs (one elected lane per segment), 2-5 = softmax, P.V MMAs, O
 // correction and epilogue. The two rings have their own producers, so a
 // page's K blocks never wait behind the previous page's V slot; the softmax
