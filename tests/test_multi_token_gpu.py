@@ -48,7 +48,7 @@ def _run(w, T, causal, q_bits, **plan_kw):
     (4, True, 16, {"force_simt": True, "num_kv_splits": 3}),
 ])
 def test_multi_token_against_the_oracle(T, causal, N, plan_kw):
-    lens = [1, 2, 63, 64, 65, 300, 1000]
+    lens = [1, 2, 63, 64, 65, 300, 1000, 0]
     w = make_workload("mt", len(lens), N, lens, seed=1400 + 10 * T + N)
     rng = np.random.default_rng(1500 + T)
     q_bits = f32_to_bf16_bits(rng.standard_normal((len(lens), T, N, 576)).astype(np.float32))
@@ -65,3 +65,5 @@ def test_multi_token_against_the_oracle(T, causal, N, plan_kw):
         # The one-token request: only its last query token sees anything.
         assert np.isneginf(lse[0, :T - 1]).all() and np.isfinite(lse[0, T - 1]).all()
         assert (got[0, :T - 1] == 0).all()
+    # The empty request: every query token sees nothing.
+    assert np.isneginf(lse[-1]).all() and (got[-1] == 0).all()
