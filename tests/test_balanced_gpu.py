@@ -10,7 +10,8 @@ against the oracle on exactly the token ranges the cut gives them.
 import numpy as np
 import pytest
 
-from mla_latent_cache_paged_gb300.workloads import make_workload
+from mla_latent_cache_paged_gb300.workloads import (bf16_bits_to_f64, bf16_tensor_bits,
+                                                    make_workload, to_torch)
 from parity_util import (assert_lse_close, assert_out_close, oracle_rows, run_decode,
                          value_abs_max)
 
@@ -124,3 +125,37 @@ def test_balanced_merge_counters_return_to_zero():
         assert torch.equal(out, first_out) and torch.equal(lse, first_lse)
     words = ws[:binding.STATUS_BYTES].view(torch.int32).cpu().numpy()
     assert not words[2:].any(), np.nonzero(words[2:])
+
+
+def test_merge_wait_runs_out_and_reports_a_timeout():
+    """Failure detection without a fault: the balanced merge waits (bounded,
+    4 s) for a request's pieces through a counter in the status header. A
+    counter started far below zero never reaches its target, so the wait runs
+    out: the call reports MLA_ERR_TIMEOUT (detail 20: the merge's wait), the
+    context stays usable, and after mla_workspace_init the same plan decodes
+    correctly again."""
+    import torch
+    from mla_latent_cache_paged_gb300 import binding
+    ready_word = 64          # status header: int32 word 64 + b counts request b's pieces
+    lens = [4096, 4096]
+    w = make_workload("bal_timeout", len(lens), 128, lens, seed=93, num_kv_splits=0)
+    q, cache, table, lens_d = to_torch(w)
+    plan = binding.make_plan(w.batch, w.num_heads, w.max_blocks_per_seq,
+                             seq_lens_host=w.seq_lens, schedule="balanced")
+    assert plan.sched_pairs > 1
+    ws = binding.new_workspace(plan)
+    ws[:binding.STATUS_BYTES].view(torch.int32)[ready_word + 0] = -(1 << 30)
+    binding.mla_decode(q, cache, table, lens_d, w.softmax_scale, plan=plan, workspace=ws)
+    torch.cuda.synchronize()
+    words = ws[:8].view(torch.int32).cpu().numpy()
+    assert words[0] == binding.MLA_ERR_TIMEOUT and words[1] == 20, words
+    assert binding.read_error(ws) == binding.MLA_ERR_TIMEOUT
+    ws2 = binding.new_workspace(plan)
+    out, lse = binding.mla_decode(q, cache, table, lens_d, w.softmax_scale, plan=plan,
+                                  workspace=ws2)
+    torch.cuda.synchronize()
+    assert binding.read_error(ws2) == 0
+    ref_out, ref_lse = oracle_rows(w, range(w.batch))
+    assert_out_close(bf16_bits_to_f64(bf16_tensor_bits(out)), ref_out, "after the timeout",
+                     value_abs_max(w, range(w.batch)))
+    assert_lse_close(lse.double().cpu().numpy(), ref_lse, "after the timeout")
