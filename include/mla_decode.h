@@ -239,6 +239,7 @@ int mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q, const void*
  *   v_dim      a multiple of 8, 8 <= v_dim <= 2048.
  *   out        device, bf16 [B, N, v_dim].
  *   lse        device, fp32 [B, N], or NULL.
+ * B * N above INT_MAX gives MLA_ERR_UNSUPPORTED.
  */
 int mla_merge_splits(const float* o_part, const float* lse_part, int batch, int num_heads,
                      int num_splits, int v_dim, void* out, float* lse, void* stream);

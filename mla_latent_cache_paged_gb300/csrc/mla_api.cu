@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cfloat>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 
@@ -103,6 +104,7 @@ extern "C" int mla_merge_splits(const float* o_part, const float* lse_part, int 
                                 void* stream) {
     if (batch < 0 || num_heads < 0 || num_splits < 1 || num_splits > kMaxMergeSplits)
         return MLA_ERR_INVALID_ARG;
+    if (int64_t(batch) * num_heads > INT_MAX) return MLA_ERR_UNSUPPORTED;
     if (v_dim < 8 || v_dim > 2048 || v_dim % 8 != 0) return MLA_ERR_UNSUPPORTED;
     if (batch == 0 || num_heads == 0) return MLA_OK;
     if (!o_part || !lse_part || !out) return MLA_ERR_INVALID_ARG;
@@ -118,6 +120,7 @@ extern "C" int mla_dcp_combine(const void* out_parts, const float* lse_parts, in
                                void* stream) {
     if (batch < 0 || num_heads < 0 || world < 1 || world > kMaxMergeSplits)
         return MLA_ERR_INVALID_ARG;
+    if (int64_t(batch) * num_heads > INT_MAX) return MLA_ERR_UNSUPPORTED;
     if (v_dim < 8 || v_dim > 2048 || v_dim % 8 != 0) return MLA_ERR_UNSUPPORTED;
     if (batch == 0 || num_heads == 0) return MLA_OK;
     if (!out_parts || !lse_parts || !out) return MLA_ERR_INVALID_ARG;

@@ -179,6 +179,16 @@ def test_dcp_combine_rejects_bad_arguments(lib):
     assert lib.mla_dcp_combine(null, null, 2, 0, 1, 512, null, null, null) == binding.MLA_OK
 
 
+def test_merge_and_combine_reject_row_counts_past_int32(lib):
+    fake = ctypes.c_void_p(0x10000)
+    null = ctypes.c_void_p(0)
+    big = 1 << 24                                   # 2^24 requests x 2^8 heads = 2^32 rows
+    assert lib.mla_merge_splits(fake, fake, big, 256, 2, 512, fake, null, null) == \
+        binding.MLA_ERR_UNSUPPORTED
+    assert lib.mla_dcp_combine(fake, fake, 2, big, 256, 512, fake, null, null) == \
+        binding.MLA_ERR_UNSUPPORTED
+
+
 def test_dcp_local_seq_lens_match_the_oracle_placement():
     """Host-side shard lengths, bit-exact against counting every token's owner."""
     from oracle import dcp_local_seq_lens as oracle_counts
