@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--force-simt", action="store_true",
                     help="run the CUDA-core kernel instead of the planner's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the headline workload only (no per-config list)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--dcp-world", type=int, default=2,
@@ -85,6 +87,17 @@ def algorithmic_work(w):
     nbytes = 1152 * T + 1152 * BN + 1024 * BN + 4 * BN + 4 * pages
     flops = 2 * (576 + 512) * w.num_heads * T
     return nbytes, flops
+
+
+def roofline_of(w, ms, peaks):
+    """Achieved GB/s and the fractions of the roofline for one call of `ms`."""
+    nbytes, flops = algorithmic_work(w)
+    t_s = ms / 1e3
+    t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    gbs = nbytes / t_s / 1e9
+    return {"achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+            "frac_of_roofline": t_roof / t_s, "t_roof_us": t_roof * 1e6,
+            "algorithmic_bytes": nbytes, "algorithmic_flops": flops}
 
 
 def kernel_source_hash(kernel):
@@ -200,6 +213,48 @@ def cpu_baseline(w, budget_s):
             "sample": f"{len(reqs)} of {w.batch} requests ({done_tokens} cached tokens x "
                       f"{w.num_heads} heads), numpy float64, {dt:.1f} s",
             "seconds": dt}
+
+
+def cpu_parity(w, got_out_bits, got_lse, strict):
+    """Part of the CPU-baseline leg: the oracle over every request of `w`,
+    compared with the GPU's bf16 output bits and fp32 LSE (host copies).
+    Returns the max absolute errors and whether the stated bounds hold
+    (out 2e-2, LSE 1e-3; the x8-outlier workload's out bound also allows one
+    bf16 ulp of the oracle and 2^-8 max_t |V[t, d]|, the bf16-weight term)."""
+    import numpy as np
+    from oracle import mla_decode_reference
+    from mla_latent_cache_paged_gb300.workloads import bf16_bits_to_f64
+
+    t0 = time.perf_counter()
+    got = bf16_bits_to_f64(got_out_bits)
+    e_out = e_lse = 0.0
+    ok = True
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        n = -(-L // w.page_size)
+        pool = bf16_bits_to_f64(w.cache_bits[w.block_table[b, :n].astype(np.int64)]) if n else \
+            np.zeros((1, w.page_size, 576))
+        ref_o, ref_l = mla_decode_reference(bf16_bits_to_f64(w.q_bits[b:b + 1]), pool,
+                                            np.arange(max(n, 1))[None, :], [L], w.softmax_scale)
+        err = np.abs(got[b] - ref_o[0])
+        gl = np.asarray(got_lse[b], dtype=np.float64)
+        same_inf = np.isneginf(gl) & np.isneginf(ref_l[0])
+        with np.errstate(invalid="ignore"):
+            lerr = np.where(same_inf, 0.0, np.abs(gl - ref_l[0]))
+        e_out = max(e_out, float(err.max()))
+        e_lse = max(e_lse, float(lerr.max()))
+        if strict:
+            tol = 2e-2
+        else:
+            a = np.abs(ref_o[0])
+            ulp = np.exp2(np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 7)
+            vmax = np.abs(pool.reshape(-1, 576)[:L, :512]).max(axis=0) if L else 0.0
+            tol = np.maximum(np.maximum(2e-2, ulp), 2.0 ** -8 * vmax)
+        ok = ok and bool(np.all(err <= tol)) and bool(np.all(lerr <= 1e-3))
+    return {"max_abs_out_err": e_out, "max_abs_lse_err": e_lse, "requests": w.batch,
+            "bound": ("out 2e-2, lse 1e-3" if strict else
+                      "out max(2e-2, bf16 ulp, 2^-8 max|V|), lse 1e-3 (x8 outlier rows)"),
+            "within_bound": ok, "cpu_seconds": time.perf_counter() - t0}
 
 
 # ------------------------------------------------------------------ arms
@@ -457,6 +512,99 @@ def run_stage(args, stage):
     }
 
 
+OTHER_CONFIGS = [
+    ("b1_n16_l256_pool8", True),
+    ("b32_n128_l1k-4k", True),
+    ("b4_n128_l32k_s64", True),
+    ("b4_n128_l64k_s64", True),
+    ("b4_n128_l96k_s64", True),
+    ("b4_n128_l128k_s64", True),
+    ("b256_n128_logu16-32k_outliers", False),
+]
+
+
+def run_configs(args, with_parity):
+    """The other workloads, each timed as the headline is (one mla_decode call
+    per rep on the current stream, CUDA events around it) but rep by rep with
+    an L2 flush (a write of twice the L2 size) between reps: the median over
+    at least 20 reps and at least 0.5 s of them, after 5 warm-ups, with the
+    SM clock sampled during those reps."""
+    import torch
+    from mla_latent_cache_paged_gb300 import binding
+    from mla_latent_cache_paged_gb300.workloads import bf16_tensor_bits, get_workload, to_torch
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(dev)
+    flush = torch.empty(2 * props.L2_cache_size, dtype=torch.uint8, device=dev)
+    peaks, peak_kind = load_peaks()
+    rows = []
+    for name, strict in OTHER_CONFIGS:
+        w = get_workload(name)
+        q, cache, table, lens = to_torch(w, dev)
+        plan = binding.make_plan(w.batch, w.num_heads, w.max_blocks_per_seq,
+                                 seq_lens_host=w.seq_lens, max_seq_len=w.max_seq_len,
+                                 num_kv_splits=w.num_kv_splits,
+                                 num_sms=props.multi_processor_count)
+        ws = binding.new_workspace(plan, dev)
+        out = torch.empty((w.batch, w.num_heads, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((w.batch, w.num_heads), dtype=torch.float32, device=dev)
+
+        def call():
+            binding.mla_decode(q, cache, table, lens, w.softmax_scale, plan=plan, out=out,
+                               lse=lse, workspace=ws)
+
+        for _ in range(5):
+            flush.zero_()
+            call()
+        torch.cuda.synchronize()
+        if binding.read_error(ws) != 0:
+            raise RuntimeError(f"{name}: device status after warm-up")
+        sampler = ClockSampler(dev.index)
+        sampler.start()
+        time.sleep(0.3)
+        events = []
+        t0 = time.perf_counter()
+        while len(events) < 20 or time.perf_counter() - t0 < 0.5:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush.zero_()
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            events.append((e0, e1))
+            if len(events) % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
+        if binding.read_error(ws) != 0:
+            raise RuntimeError(f"{name}: device status after timing")
+        ms = statistics.median(a.elapsed_time(b) for a, b in events)
+        roof = roofline_of(w, ms, peaks)
+        row = {
+            "workload": name, "batch": w.batch, "heads": w.num_heads,
+            "cached_tokens": w.total_tokens, "ms_per_step": ms,
+            "value": w.total_tokens * w.num_heads / (ms / 1e3), "unit": UNIT,
+            "reps": len(events), "timing": "median of per-call CUDA events, L2 flushed between",
+            "num_kv_splits": plan.num_kv_splits,
+            "schedule": (f"page-balanced over {plan.sched_pairs} CTA pairs + merge"
+                         if plan.sched_pairs > 0 else f"split S={plan.num_kv_splits}"),
+            "kernel": {1: "simt", 2: "tcgen05"}[plan.kernel],
+            "roofline": {"bound": "hbm", "achieved": roof["achieved_gbs"],
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": roof["frac"],
+                         "frac_of_roofline": roof["frac_of_roofline"],
+                         "t_roof_us": roof["t_roof_us"],
+                         "algorithmic_bytes_per_call": roof["algorithmic_bytes"]},
+            "gpu_launches_per_call": 1 + (1 if plan.num_kv_splits > 1 or plan.sched_pairs else 0),
+            "clocks": clocks,
+        }
+        if with_parity:
+            row["parity"] = cpu_parity(w, bf16_tensor_bits(out), lse.cpu().numpy(), strict)
+        rows.append(row)
+        del q, cache, table, lens, ws, out, lse, w
+        torch.cuda.empty_cache()
+    return rows
+
+
 def max_over_ranks(x, world, device):
     """The largest of the ranks' values (the slowest rank's time); x itself at
     world 1. Every rank must call it."""
@@ -603,6 +751,7 @@ def run_ours(args, w, rank, world):
     if rank != 0:
         return None
 
+    from mla_latent_cache_paged_gb300.workloads import bf16_tensor_bits
     units = w.total_tokens * w.num_heads
     ms_per_step = elapsed_ms / steps
     value = whole_job_rate(units, world, steps, elapsed_ms)
@@ -658,6 +807,9 @@ def run_ours(args, w, rank, world):
                 "ms_per_step": e2e_ms / e2e_steps,
                 "copies": "per step; on two copy streams, overlapping the neighbouring "
                           "steps' decodes (double-buffered device inputs and outputs)"},
+        # host copies of the last step's results, for the CPU-baseline leg's
+        # parity check (removed before printing)
+        "_out_bits": bf16_tensor_bits(out), "_lse": lse.cpu().numpy(),
     }
     return res
 
@@ -694,8 +846,15 @@ def main():
     w = get_workload(name)
     res = run_ours(args, w, rank, world)
     if rank == 0:
-        if not args.no_cpu_baseline and world == 1:
+        with_cpu = not args.no_cpu_baseline and world == 1
+        if with_cpu:
             res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+            res["cpu_baseline"]["parity"] = cpu_parity(w, res.pop("_out_bits"),
+                                                       res.pop("_lse"), True)
+        res.pop("_out_bits", None)
+        res.pop("_lse", None)
+        if not args.no_configs and world == 1 and args.workload is None:
+            res["configs"] = run_configs(args, with_cpu)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MLA_DECODE_ABI_VERSION 4
+#define MLA_DECODE_ABI_VERSION 5
 
 /* Status codes. */
 #define MLA_OK                 0
@@ -71,6 +71,13 @@ extern "C" {
 #define MLA_PLAN_SPLIT_ONLY  0x2u  /* never choose the page-balanced schedule */
 #define MLA_PLAN_FORCE_BALANCED 0x4u  /* with num_kv_splits = 0: the page-balanced schedule
                                          wherever it applies, whatever the estimate */
+/* Test only (failure detection without a fault): the tensor-core kernel's
+ * CTA 0 never issues its first K-ring load and every bounded wait of the call
+ * is shortened to 2 ms (the merge's to 8 ms). The score warp's wait for that
+ * load runs out, the call records MLA_ERR_TIMEOUT with detail 8 (that wait
+ * site), every role drains its own loads and MMAs, TMEM is freed and the
+ * kernel returns; the context stays usable. Never set in normal use. */
+#define MLA_PLAN_DEBUG_WITHHOLD_LOAD 0x100u
 
 /*
  * A decode plan: the sizes, the schedule and the kernel variant. It is plain
@@ -198,24 +205,30 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* latent_
  * offer, and bindings that can pass only the operation's own tensors. Such a
  * caller passes the inputs and outputs of mla_decode and no workspace.
  *
- * Scratch: the status words and the split partials live in one fixed device
- * array of 32 MiB inside the library; every GPU that loads the library holds
- * it until the process exits. A plan whose workspace_bytes exceeds 32 MiB is
- * rejected with MLA_ERR_SCRATCH_LIMIT (the partials take B*N*S*2,052 bytes:
- * for example B=32, N=128, S=4 fits; B=4, N=128, S=64 does not).
+ * Scratch: the status words, the page-balanced merge's counters and the
+ * partial rows live in one fixed device array of 32 MiB inside the library;
+ * every GPU that loads the library holds it until the process exits. A plan
+ * whose workspace_bytes exceeds 32 MiB is rejected with MLA_ERR_SCRATCH_LIMIT.
+ * The partials take 2,052 bytes per row, and 8 KiB go to the status header:
+ * up to 16,348 rows fit (split schedule: B*N*S rows, e.g. B=32, N=128, S=3
+ * fits and S=4 does not; page-balanced over C CTA pairs: 2*C*N rows, e.g.
+ * C=32, N=128).
  *
  *   plan, q, latent_cache, num_blocks, block_table, seq_lens, softmax_scale,
  *   out, lse, stream   as for mla_decode.
  *   device_status      optional device int32[2] (4-byte aligned) that receives
  *                      the device-detected status (MLA_OK or MLA_ERR_*) and a
- *                      detail word; the call zeroes it first. NULL keeps the
- *                      status inside the library's scratch, unreadable.
+ *                      detail word; the call zeroes it first. Only these two
+ *                      words are written. NULL keeps the status inside the
+ *                      library's scratch, unreadable.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture. Every call uses the same array and leaves its contents behind, so
- * calls that overlap on the GPU (other streams, other host threads, the same
- * device) race with each other: serialise them.
+ * Every call zeroes the array's status header (8 KiB, on `stream`) before its
+ * kernels, so the counters a timed-out call left behind cannot mislead the
+ * next one. The first call on each device looks up the array's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture. Every call uses the same array and leaves its contents
+ * behind, so calls that overlap on the GPU (other streams, other host
+ * threads, the same device) race with each other: serialise them.
  */
 int mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
                        int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
@@ -279,6 +292,21 @@ int mla_merge_splits(const float* o_part, const float* lse_part, int batch, int 
  * MLA_ERR_INVALID_ARG, scratch too small or misaligned MLA_ERR_WORKSPACE.
  */
 size_t mla_multi_token_scratch_bytes(int batch, int q_len, int max_blocks_per_seq);
+
+/*
+ * mla_multi_token_row_lens -- host only, no device work: the number of cached
+ * tokens each (request, query token) row sees, row r = b * q_len + i, under
+ * the reading above: max(L - (q_len - 1 - i), 0) with `causal` != 0, else L
+ * (L = seq_lens_host[b]). These are the host lengths a shape-(b) plan is made
+ * from (mla_decode_plan with batch = B * q_len).
+ *
+ *   seq_lens_host   host, int32 [batch], every entry >= 0.
+ *   row_lens_host   host, int32 [batch * q_len], written.
+ * Returns MLA_ERR_INVALID_ARG for a null pointer, batch < 0, q_len < 1 or a
+ * negative length (nothing written).
+ */
+int mla_multi_token_row_lens(const int32_t* seq_lens_host, int batch, int q_len, int causal,
+                             int32_t* row_lens_host);
 int mla_decode_multi_token(const mla_decode_plan_t* plan, int q_len, int num_heads, int causal,
                            const void* q, const void* latent_cache, int64_t num_blocks,
                            const int32_t* block_table, const int32_t* seq_lens,
@@ -391,25 +419,50 @@ const char* mla_status_string(int status);
 int mla_abi_version(void);
 
 /*
- * mla_debug_gather_pages -- test hook for the page-table indexing.
+ * mla_debug_gather_pages -- test hook for the page-table reading.
  *
  * Copies, for every request b and token t < seq_lens[b], the 576-wide cache
- * row the decode kernels read for that token into
- * dst[b, t, 0:576] (bf16 [B, dst_max_tokens, 576], contiguous), moving it
- * with the same TMA tensor map and page loader the tensor-core decode kernel
- * uses. Rows t >= seq_lens[b] of dst are left untouched. Block ids outside
- * [0, num_blocks) are recorded in the workspace status word and their rows
- * are left untouched. This is the semantics of vLLM's gather_cache /
- * cp_gather_cache (mla_attention API docs, _compute_prefill_context), used
- * here only to check the indexing bit for bit. `workspace` is a status
- * header: device, >= 8192 bytes, 256-byte aligned, zeroed by
- * mla_workspace_init.
+ * row of token t (row t % 64 of block block_table[b, t / 64]) into
+ * dst[b, t, 0:576] (bf16 [B, dst_max_tokens, 576], contiguous) with plain
+ * 16-byte loads and stores (no tensor map: the decode kernels' own loader is
+ * checked by mla_debug_loader_pages). Rows t >= seq_lens[b] of dst are left
+ * untouched. Block ids outside [0, num_blocks) are recorded in the workspace
+ * status word and their rows are left untouched. This is the semantics of
+ * vLLM's gather_cache / cp_gather_cache (mla_attention API docs,
+ * _compute_prefill_context). `workspace` is a status header: device, >= 8192
+ * bytes, 256-byte aligned, zeroed by mla_workspace_init.
  */
 int mla_debug_gather_pages(const void* latent_cache, int64_t num_blocks,
                            const int32_t* block_table, const int32_t* seq_lens,
                            int batch, int max_blocks_per_seq, int dst_max_tokens,
                            void* dst, void* workspace, size_t workspace_bytes,
                            void* stream);
+
+/*
+ * mla_debug_loader_pages -- test hook: the tensor-core decode kernel's own page
+ * loaders, run alone.
+ *
+ * Launches the tensor-core decode kernel of `plan` (MLA_KERNEL_TC, any
+ * schedule) in a mode where only its two TMA page loaders run: the same
+ * segment walk over the plan's work, the same block-table reads, the same
+ * tensor map over the cache viewed as [num_blocks * 64, 576] with 64 x 64
+ * boxes at row block * 64, into the same swizzled shared-memory rings. Each
+ * CTA then copies every page it received out of its rings: CTA rank r of a
+ * pair writes the rows of token t of request b, as it holds them, to
+ * dst[r, b, t, 0:576] (bf16 [2, B, dst_max_tokens, 576], contiguous). A CTA
+ * receives all 576 columns of each page of its pair's work (its value
+ * columns in one ring, the rest in the other), so both halves of dst hold
+ * every token of every request whose pages the plan covers. Rows past a
+ * request's length, or at t >= dst_max_tokens, are not written. Block ids
+ * outside [0, num_blocks) are recorded (MLA_ERR_BAD_BLOCK_ID) and their rows
+ * are written as zeros, which is what the decode reads there. No MMA runs and
+ * q is not read. workspace: a status header as for mla_debug_gather_pages.
+ * MLA_ERR_UNSUPPORTED for a plan of the CUDA-core kernel.
+ */
+int mla_debug_loader_pages(const mla_decode_plan_t* plan, const void* latent_cache,
+                           int64_t num_blocks, const int32_t* block_table,
+                           const int32_t* seq_lens, int dst_max_tokens, void* dst,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

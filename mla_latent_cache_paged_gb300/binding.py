@@ -28,6 +28,7 @@ MLA_KERNEL_TC = 2
 MLA_PLAN_FORCE_SIMT = 0x1
 MLA_PLAN_SPLIT_ONLY = 0x2
 MLA_PLAN_FORCE_BALANCED = 0x4
+MLA_PLAN_DEBUG_WITHHOLD_LOAD = 0x100
 
 KV_LORA_RANK = 512
 ROPE_DIM = 64
@@ -40,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "mla_read_error", "mla_status_string", "mla_abi_version", "mla_debug_gather_pages",
     "mla_decode_noalloc", "mla_dcp_local_seq_lens", "mla_dcp_combine",
     "mla_q_absorb_concat_cache", "mla_v_up_proj", "mla_multi_token_scratch_bytes",
-    "mla_decode_multi_token",
+    "mla_decode_multi_token", "mla_debug_loader_pages", "mla_multi_token_row_lens",
 )
 
 
@@ -107,7 +108,10 @@ def load_library(path=None):
     lib.mla_q_absorb_concat_cache.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp, sz,
                                               vp]
     lib.mla_v_up_proj.argtypes = [vp, vp, i32, i32, vp, vp, sz, vp]
+    lib.mla_debug_loader_pages.argtypes = [ctypes.POINTER(MlaDecodePlan), vp, i64, vp, vp, i32,
+                                           vp, vp, sz, vp]
     lib.mla_multi_token_scratch_bytes.argtypes = [i32, i32, i32]
+    lib.mla_multi_token_row_lens.argtypes = [vp, i32, i32, i32, vp]
     lib.mla_decode_multi_token.argtypes = [ctypes.POINTER(MlaDecodePlan), i32, i32, i32, vp, vp,
                                            i64, vp, vp, f32, vp, vp, vp, sz, vp, sz, vp]
     for name in EXPORTED_SYMBOLS:
@@ -143,12 +147,13 @@ def _stream_ptr(stream):
 
 
 def make_plan(batch, num_heads, max_blocks_per_seq, max_seq_len=None, *, seq_lens_host=None,
-              num_kv_splits=0, num_sms=None, force_simt=False, schedule="auto"):
+              num_kv_splits=0, num_sms=None, force_simt=False, schedule="auto", extra_flags=0):
     """Call mla_decode_plan (host only; no device work).
 
     ``schedule``: "auto" (the planner's estimate), "split" (never the
     page-balanced schedule) or "balanced" (the page-balanced schedule wherever
-    it applies; needs num_kv_splits = 0).
+    it applies; needs num_kv_splits = 0). ``extra_flags``: further MLA_PLAN_*
+    bits (tests use MLA_PLAN_DEBUG_WITHHOLD_LOAD).
     """
     if schedule not in ("auto", "split", "balanced"):
         raise ValueError(f"schedule must be auto, split or balanced, not {schedule!r}")
@@ -171,7 +176,8 @@ def make_plan(batch, num_heads, max_blocks_per_seq, max_seq_len=None, *, seq_len
                              int(num_kv_splits), int(num_sms),
                              (MLA_PLAN_FORCE_SIMT if force_simt else 0) |
                              (MLA_PLAN_SPLIT_ONLY if schedule == "split" else 0) |
-                             (MLA_PLAN_FORCE_BALANCED if schedule == "balanced" else 0),
+                             (MLA_PLAN_FORCE_BALANCED if schedule == "balanced" else 0) |
+                             int(extra_flags),
                              ctypes.byref(plan))
     del keep
     _check(rc, "mla_decode_plan")
@@ -241,14 +247,16 @@ def mla_decode(q, latent_cache, block_table, seq_lens, softmax_scale, *, plan=No
 
 
 def multi_token_row_lens(seq_lens_host, q_len, causal=True):
-    """Visible length of every (request, query token) row, row r = b * T + i:
-    ``L - (T - 1 - i)`` (at least 0) when causal, else ``L`` (host, numpy int32)."""
+    """Tokens each (request, query token) row sees, row r = b * T + i, from
+    ``mla_multi_token_row_lens`` (host C; numpy int32 ``[B * T]``)."""
     import numpy as np
-    lens = np.asarray(seq_lens_host, dtype=np.int64)
-    if not causal:
-        return np.repeat(lens, q_len).astype(np.int32)
-    shift = (q_len - 1 - np.arange(q_len))[None, :]
-    return np.maximum(lens[:, None] - shift, 0).reshape(-1).astype(np.int32)
+    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32).reshape(-1))
+    rows = np.empty(lens.size * int(q_len), dtype=np.int32)
+    rc = load_library().mla_multi_token_row_lens(
+        ctypes.c_void_p(lens.ctypes.data), int(lens.size), int(q_len), 1 if causal else 0,
+        ctypes.c_void_p(rows.ctypes.data))
+    _check(rc, "mla_multi_token_row_lens")
+    return rows
 
 
 def make_plan_multi_token(batch, q_len, num_heads, max_blocks_per_seq, *, seq_lens_host=None,
@@ -426,6 +434,22 @@ def debug_gather_pages(latent_cache, block_table, seq_lens, dst, workspace, stre
         int(block_table.shape[1]), int(dst.shape[1]), _ptr(dst), _ptr(workspace),
         int(workspace.numel()), _stream_ptr(stream))
     _check(rc, "mla_debug_gather_pages")
+    return dst
+
+
+def debug_loader_pages(plan, latent_cache, block_table, seq_lens, dst, workspace, stream=None):
+    """Test hook: the tensor-core kernel's page loaders alone under ``plan``;
+    ``dst`` bf16 ``[2, B, T, 576]`` receives, per CTA rank, the rows it loaded."""
+    import torch
+    _check_tensor(latent_cache, "latent_cache", torch.bfloat16)
+    _check_tensor(dst, "dst", torch.bfloat16)
+    if dst.dim() != 4 or dst.shape[0] != 2 or dst.shape[1] != plan.batch or dst.shape[3] != 576:
+        raise ValueError("dst must be [2, B, T, 576]")
+    rc = load_library().mla_debug_loader_pages(
+        ctypes.byref(plan), _ptr(latent_cache), int(latent_cache.shape[0]), _ptr(block_table),
+        _ptr(seq_lens), int(dst.shape[2]), _ptr(dst), _ptr(workspace), int(workspace.numel()),
+        _stream_ptr(stream))
+    _check(rc, "mla_debug_loader_pages")
     return dst
 
 

@@ -29,25 +29,12 @@ extern "C" int mla_workspace_init(void* workspace, size_t workspace_bytes, void*
 
 namespace mla {
 
-int decode_impl(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
-                int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
-                float softmax_scale, void* out, float* lse, void* workspace,
-                size_t workspace_bytes, void* stream, int q_len, int heads_per_token,
-                int causal) {
-    int rc = validate_plan(plan);
-    if (rc != MLA_OK) return rc;
-    if (!q || !latent_cache || !block_table || !seq_lens || !out) return MLA_ERR_INVALID_ARG;
-    if (num_blocks < 1 || !std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(latent_cache, 16) || !aligned(out, 16) ||
-        !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)))
-        return MLA_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < plan->workspace_bytes || !aligned(workspace, 256))
-        return MLA_ERR_WORKSPACE;
-    if (plan->kernel == MLA_KERNEL_TC && num_blocks > tc_max_blocks()) return MLA_ERR_UNSUPPORTED;
-    if (plan->batch == 0) return MLA_OK;
-
+DecodeParams make_decode_params(const mla_decode_plan_t* plan, const void* q,
+                                const void* latent_cache, int64_t num_blocks,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                float softmax_scale, void* out, float* lse, char* ws,
+                                int32_t* status, int q_len, int heads_per_token, int causal) {
     const int S = plan->num_kv_splits;
-    char* ws = static_cast<char*>(workspace);
     DecodeParams p{};
     p.q = static_cast<const uint16_t*>(q);
     p.cache = static_cast<const uint16_t*>(latent_cache);
@@ -65,27 +52,59 @@ int decode_impl(const mla_decode_plan_t* plan, const void* q, const void* latent
     if (p.scale_log2 == 0.f) p.scale_log2 = FLT_MIN;
     p.out = static_cast<uint16_t*>(out);
     p.lse = lse;
-    p.status = reinterpret_cast<int32_t*>(ws);
+    p.status = status ? status : reinterpret_cast<int32_t*>(ws);
+    p.counters = reinterpret_cast<int32_t*>(ws);
     p.sched_pairs = plan->sched_pairs;
     p.q_len = q_len;
     p.heads_per_token = heads_per_token;
     p.causal = causal;
+    p.timeout_ns = kDefaultTimeoutNs;
+    if (plan->flags & MLA_PLAN_DEBUG_WITHHOLD_LOAD) {
+        p.debug = kDebugWithholdLoad;
+        p.timeout_ns = kDebugTimeoutNs;
+    }
     if (S > 1 || plan->sched_pairs > 0) {
         p.o_part = reinterpret_cast<float*>(ws + plan->partial_offset);
         p.lse_part = reinterpret_cast<float*>(ws + plan->lse_partial_offset);
     }
+    return p;
+}
 
+int launch_decode_and_merge(const DecodeParams& p, const mla_decode_plan_t* plan, void* stream) {
     int e = plan->kernel == MLA_KERNEL_TC ? launch_decode_tc(p, plan->grid_ctas, stream)
                                           : launch_decode_simt(p, stream);
     if (e != 0) return MLA_ERR_CUDA;
     if (plan->sched_pairs > 0) {
         if (launch_merge_balanced(p, stream) != 0) return MLA_ERR_CUDA;
-    } else if (S > 1) {
-        e = launch_merge(p.o_part, p.lse_part, plan->batch * plan->num_heads, S, kLkv, p.out,
-                         lse, stream);
+    } else if (plan->num_kv_splits > 1) {
+        e = launch_merge(p.o_part, p.lse_part, plan->batch * plan->num_heads,
+                         plan->num_kv_splits, kLkv, p.out, p.lse, stream);
         if (e != 0) return MLA_ERR_CUDA;
     }
     return MLA_OK;
+}
+
+int decode_impl(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
+                int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                float softmax_scale, void* out, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream, int q_len, int heads_per_token,
+                int causal) {
+    int rc = validate_plan(plan);
+    if (rc != MLA_OK) return rc;
+    if (!q || !latent_cache || !block_table || !seq_lens || !out) return MLA_ERR_INVALID_ARG;
+    if (num_blocks < 1 || !std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(latent_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)))
+        return MLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < plan->workspace_bytes || !aligned(workspace, 256))
+        return MLA_ERR_WORKSPACE;
+    if (plan->kernel == MLA_KERNEL_TC && num_blocks > tc_max_blocks()) return MLA_ERR_UNSUPPORTED;
+    if (plan->batch == 0) return MLA_OK;
+    const DecodeParams p = make_decode_params(plan, q, latent_cache, num_blocks, block_table,
+                                              seq_lens, softmax_scale, out, lse,
+                                              static_cast<char*>(workspace), nullptr, q_len,
+                                              heads_per_token, causal);
+    return launch_decode_and_merge(p, plan, stream);
 }
 
 }  // namespace mla
@@ -142,6 +161,43 @@ extern "C" int mla_read_error(void* workspace, int* device_status, void* stream)
     if (cudaMemset(workspace, 0, sizeof(words)) != cudaSuccess) return MLA_ERR_CUDA;
     *device_status = words[0];
     return MLA_OK;
+}
+
+extern "C" int mla_debug_loader_pages(const mla_decode_plan_t* plan, const void* latent_cache,
+                                      int64_t num_blocks, const int32_t* block_table,
+                                      const int32_t* seq_lens, int dst_max_tokens, void* dst,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = validate_plan(plan);
+    if (rc != MLA_OK) return rc;
+    if (plan->kernel != MLA_KERNEL_TC) return MLA_ERR_UNSUPPORTED;
+    if (!latent_cache || !block_table || !seq_lens || !dst || dst_max_tokens < 0 ||
+        num_blocks < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned(latent_cache, 16) || !aligned(dst, 16) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4))
+        return MLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kStatusBytes || !aligned(workspace, 256))
+        return MLA_ERR_WORKSPACE;
+    if (num_blocks > tc_max_blocks()) return MLA_ERR_UNSUPPORTED;
+    if (plan->batch == 0) return MLA_OK;
+    DecodeParams p{};
+    p.cache = static_cast<const uint16_t*>(latent_cache);
+    p.num_blocks = num_blocks;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.max_blocks = plan->max_blocks_per_seq;
+    p.batch = plan->batch;
+    p.num_heads = plan->num_heads;
+    p.num_splits = plan->num_kv_splits;
+    p.sched_pairs = plan->sched_pairs;
+    p.status = static_cast<int32_t*>(workspace);
+    p.counters = static_cast<int32_t*>(workspace);
+    p.q_len = 1;
+    p.heads_per_token = plan->num_heads;
+    p.timeout_ns = kDefaultTimeoutNs;
+    p.dump = static_cast<uint16_t*>(dst);
+    p.dump_max_tokens = dst_max_tokens;
+    return cuda_status(launch_decode_tc_loader_dump(p, plan->grid_ctas, stream));
 }
 
 extern "C" int mla_debug_gather_pages(const void* latent_cache, int64_t num_blocks,

@@ -89,7 +89,6 @@ constexpr uint32_t kTmemS = 128;   // two 64-column score buffers; P (32 columns
 constexpr uint32_t kTmemO = 256;   // 256 fp32 columns of O
 constexpr int kQTmemBlocks = 4;    // 64-dim blocks of q held in TMEM
 
-constexpr uint64_t kTimeoutNs = 1000000000ull;   // 1 s per wait
 // A waiting thread sleeps in mbarrier.try_wait until the phase completes (or
 // this long), so waiting warps take no issue slots from the working ones.
 constexpr uint32_t kSuspendNs = 20000;
@@ -132,16 +131,20 @@ __device__ __forceinline__ void set_abort(TcBars* bars, int32_t* status, int32_t
     record_error(status, MLA_ERR_TIMEOUT, site);
 }
 
-// Bounded wait on a local mbarrier phase. Returns false when the kernel is
-// aborting (another role timed out) or when this wait expires.
+// Bounded wait on a local mbarrier phase (at most `limit_ns`). Returns false
+// when the kernel is aborting (another role timed out) or when this wait
+// expires. The score warp waits with the call's limit and the roles that
+// depend on it (the loaders, the softmax warps) with twice that, so that
+// when something stops, the wait nearest the cause is the one recorded.
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, TcBars* bars,
-                                       int32_t* status, int32_t site, bool ignore_abort) {
+                                       int32_t* status, int32_t site, bool ignore_abort,
+                                       uint64_t limit_ns) {
     const uint64_t t0 = ptx::globaltimer();
     while (true) {
         for (int i = 0; i < 4; ++i)
             if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
         if (!ignore_abort && aborting(bars)) return false;
-        if (ptx::globaltimer() - t0 > kTimeoutNs) {
+        if (ptx::globaltimer() - t0 > limit_ns) {
             set_abort(bars, status, site);
             return false;
         }
@@ -149,10 +152,10 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, TcBars* ba
 }
 
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, TcBars* bars,
-                                           int32_t* status, int32_t site,
+                                           int32_t* status, int32_t site, uint64_t limit_ns,
                                            bool ignore_abort = false) {
     if (ptx::mbar_test_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, bars, status, site, ignore_abort);
+    return wait_slow(bar, parity, bars, status, site, ignore_abort, limit_ns);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -265,12 +268,13 @@ struct MmaWarpArgs {
     TcBars* bars;
     int32_t* status;
     unsigned char* smem;
+    uint64_t limit_ns;   // the score warp's wait limit
 };
 
 // Slow path of warp_wait, out of line. Called by the whole warp; returns
 // lane 0's answer.
 __device__ __noinline__ int warp_wait_slow(uint32_t bar, uint32_t parity, TcBars* bars,
-                                           int32_t* status, int32_t site) {
+                                           int32_t* status, int32_t site, uint64_t limit_ns) {
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (__shfl_sync(0xffffffffu, ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs) ? 1 : 0,
@@ -278,7 +282,7 @@ __device__ __noinline__ int warp_wait_slow(uint32_t bar, uint32_t parity, TcBars
             return 1;
         if ((it & 3u) == 0u) {
             int stop = aborting(bars) ? 1 : 0;
-            if (!stop && ptx::globaltimer() - t0 > kTimeoutNs) stop = 2;
+            if (!stop && ptx::globaltimer() - t0 > limit_ns) stop = 2;
             stop = __shfl_sync(0xffffffffu, stop, 0);
             if (stop != 0) {
                 if (stop == 2 && (threadIdx.x & 31) == 0) set_abort(bars, status, site);
@@ -294,14 +298,15 @@ __device__ __noinline__ int warp_wait_slow(uint32_t bar, uint32_t parity, TcBars
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const MmaWarpArgs& a,
                                           int32_t site) {
     if (__shfl_sync(0xffffffffu, ptx::mbar_test_wait(bar, parity) ? 1 : 0, 0) != 0) return true;
-    return __shfl_sync(0xffffffffu, warp_wait_slow(bar, parity, a.bars, a.status, site), 0) != 0;
+    return __shfl_sync(0xffffffffu,
+                       warp_wait_slow(bar, parity, a.bars, a.status, site, a.limit_ns), 0) != 0;
 }
 
 // Every tcgen05 op this warp issued completes before the CTA frees TMEM.
 __device__ __forceinline__ void warp_drain(uint32_t bar, const MmaWarpArgs& a) {
     if (ptx::elect_one()) ptx::mma_commit(bar);
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) wait_phase(bar, 0, a.bars, a.status, kSiteDrain, true);
+    if ((threadIdx.x & 31) == 0) wait_phase(bar, 0, a.bars, a.status, kSiteDrain, a.limit_ns, true);
     __syncwarp();
 }
 
@@ -404,9 +409,11 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
                 const uint32_t ph = uint32_t(jc >> 1) & 1u;
                 // The score buffer is free once the P.V MMA of page jc-2 has read P.
                 if (jc >= 2 && !pf_ready &&
-                    !wait_phase(b_pfree + 8 * sl, ph ^ 1u, a.bars, a.status, kSiteSFree))
+                    !wait_phase(b_pfree + 8 * sl, ph ^ 1u, a.bars, a.status, kSiteSFree,
+                                a.limit_ns))
                     break;
-                if (!kf_ready && !wait_phase(b_kfull + 8 * sl, ph, a.bars, a.status, kSiteKFull))
+                if (!kf_ready &&
+                    !wait_phase(b_kfull + 8 * sl, ph, a.bars, a.status, kSiteKFull, a.limit_ns))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + kTmemS + uint32_t(sl * 64);
@@ -427,7 +434,7 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
                     d, tmem, desc, bk + 12, false, b_vf, ph);
                 score_block<k_block(RANK, 4)>(d, tmem, desc, bk + 16, false);
                 ptx::mma_commit(b_kempty + 8 * sl);
-                if (!vr && !wait_phase(b_vf, ph, a.bars, a.status, kSiteVFull)) break;
+                if (!vr && !wait_phase(b_vf, ph, a.bars, a.status, kSiteVFull, a.limit_ns)) break;
                 score_block<4 * RANK + 0>(d, tmem, desc, bv + 0, false);
                 score_block<4 * RANK + 1>(d, tmem, desc, bv + 4, false);
                 score_block<4 * RANK + 2>(d, tmem, desc, bv + 8, false);
@@ -463,6 +470,129 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int np, 
     ptx::mma_commit(b_pfree + 8 * sl);
 }
 
+
+// ------------------------------------------------------------ page loaders
+// Loader dump (test hook): the rows of a page as this CTA received them, from
+// a ring slot of 64 x 64 bf16 blocks in the 128-byte swizzled layout (16-byte
+// chunk c of row r at r * 128 + (c ^ (r % 8)) * 16), to
+// p.dump[rank, b, t0 + r, :].
+__device__ void dump_slot(const DecodeParams& p, const unsigned char* slot, bool k_ring,
+                          uint32_t rank, int b, int t0, int rows) {
+    const int nblk = k_ring ? kKPerPage : 4;
+    for (int k = 0; k < nblk; ++k) {
+        const int col0 = k_ring ? 64 * k_block(int(rank), k) : 256 * int(rank) + 64 * k;
+        const unsigned char* blk = slot + k * kBlockBytes;
+        for (int r = 0; r < rows && t0 + r < p.dump_max_tokens; ++r) {
+            uint4* dst = reinterpret_cast<uint4*>(
+                p.dump + ((size_t(rank) * p.batch + b) * p.dump_max_tokens + t0 + r) * kD + col0);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                dst[c] = *reinterpret_cast<const uint4*>(blk + r * 128 + ((c ^ (r & 7)) * 16));
+        }
+    }
+}
+
+// One of the two page loaders (K ring or V ring), run by one thread. For
+// every page of the pair's segments it waits for its ring slot to be free,
+// then TMA-loads the page's blocks for this ring: box 64 columns x 64 rows of
+// the tensor map over the cache viewed as [num_blocks * 64, 576], at row
+// y = block * 64 (block = block_table[b, page]). With kDump the loader runs
+// alone (no consumers free the slots): it waits for each page to land and
+// copies it out with dump_slot.
+template <bool kDump>
+__device__ __forceinline__ void page_loader(const DecodeParams& p, const CUtensorMap* tmap,
+                                            const int32_t* pfx, int pair, uint32_t rank,
+                                            bool k_ring, TcBars* bars, unsigned char* smem,
+                                            uint32_t sbase, uint32_t b_full, uint32_t b_empty,
+                                            uint64_t limit_ns) {
+    const int N = p.num_heads;
+    const int bytes = k_ring ? kKBytes : kVBytes;
+    const int off0 = k_ring ? kOffK : kOffV;
+    const uint32_t dst0 = sbase + uint32_t(off0);
+    // Test hook: CTA 0 withholds its first K-ring load, so the score warp's
+    // wait for it runs out.
+    const bool withhold =
+        !kDump && k_ring && blockIdx.x == 0 && (p.debug & kDebugWithholdLoad) != 0;
+    SegmentWalk walk = walk_begin(p, pfx, pair);
+    Segment sg;
+    int jg = 0;   // pages issued so far, across segments
+    bool ok = true;
+    while (ok && walk_next(p, pfx, pair, walk, sg)) {
+        const int ntiles = seg_pages(sg);
+        const int page0 = sg.t_lo / kTile;
+        const int32_t* table = p.block_table + size_t(sg.b) * p.max_blocks;
+        // q of the next segment's request into L2 (half per CTA) a few pages
+        // before this segment ends (earlier, the page stream would evict
+        // it), so that staging it is short.
+        int q_next = -1;
+        if (k_ring && !kDump) {
+            SegmentWalk peek = walk;
+            Segment nx;
+            if (walk_next(p, pfx, pair, peek, nx)) q_next = nx.b;
+        }
+        auto prefetch_q = [&]() {
+            if (q_next < 0) return;
+            const uint32_t qbytes = uint32_t(N) * kD * 2;   // a multiple of 16
+            const unsigned char* qb =
+                reinterpret_cast<const unsigned char*>(p.q + size_t(q_next) * N * kD);
+            const uint32_t half = (qbytes / 2) & ~15u;
+            ptx::prefetch_l2(qb + rank * half, rank == 0 ? half : qbytes - half);
+        };
+        if (ntiles <= kQPrefetchPages) prefetch_q();
+        int next = ntiles > 0 ? table[page0] : 0;
+        for (int j = 0; j < ntiles; ++j, ++jg) {
+            const int blk = next;
+            if (j + 1 < ntiles) next = table[page0 + j + 1];
+            if (j + kQPrefetchPages == ntiles) prefetch_q();
+            int32_t y;
+            if (blk >= 0 && int64_t(blk) < p.num_blocks) {
+                y = blk * kTile;
+            } else {
+                if (k_ring) record_error(p.status, MLA_ERR_BAD_BLOCK_ID, blk);
+                y = -kTile;   // wholly outside the tensor: TMA writes zeros
+            }
+            const int sl = jg & 1;
+            if (!kDump && !wait_phase(b_empty + 8 * sl, (uint32_t(jg >> 1) & 1u) ^ 1u, bars,
+                                      p.status, k_ring ? kSiteKEmpty : kSiteVEmpty, limit_ns)) {
+                ok = false;
+                break;
+            }
+            if (withhold && jg == 0) continue;
+            ptx::mbar_arrive_expect_tx(b_full + 8 * sl, uint32_t(bytes));
+            const uint32_t dst = dst0 + uint32_t(sl * bytes);
+            if (k_ring) {
+                // The five K-ring blocks, in score order.
+                for (int pos = 0; pos < kKPerPage; ++pos)
+                    ptx::tma_load_2d(dst + uint32_t(pos * kBlockBytes), tmap,
+                                     64 * k_block(int(rank), pos), y, b_full + 8 * sl);
+            } else {
+                // This CTA's four value blocks.
+                for (int k = 0; k < 4; ++k)
+                    ptx::tma_load_2d(dst + uint32_t(k * kBlockBytes), tmap,
+                                     256 * int(rank) + 64 * k, y, b_full + 8 * sl);
+            }
+            if constexpr (kDump) {
+                if (!wait_phase(b_full + 8 * sl, uint32_t(jg >> 1) & 1u, bars, p.status,
+                                kSiteDrain, limit_ns, true)) {
+                    ok = false;
+                    ++jg;   // issued: the drain below waits for it once more
+                    break;
+                }
+                const int t0 = sg.t_lo + j * kTile;
+                dump_slot(p, smem + off0 + sl * bytes, k_ring, rank, sg.b, t0,
+                          min(kTile, sg.t_hi - t0));
+            }
+        }
+    }
+    // Every issued load lands before the CTA may exit.
+    for (int j = jg > 2 ? jg - 2 : 0; j < jg; ++j) {
+        if (withhold && j == 0) continue;
+        wait_phase(b_full + 8 * (j & 1), uint32_t(j >> 1) & 1u, bars, p.status, kSiteDrain,
+                   limit_ns, true);
+    }
+}
+
+template <bool kDump>
 __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -544,90 +674,28 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             if (lane == 0) pfx[0] = 0;
         }
     }
-    if (warp == 1) {
+    if (!kDump && warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(&bars->tmem_base), kTmemCols);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tmem = bars->tmem_base;
-    const MmaWarpArgs margs{tmem, sbase, bars, p.status, smem};
+    const uint32_t tmem = kDump ? 0u : bars->tmem_base;
+    const uint64_t lim_score = p.timeout_ns;       // the score warp's waits
+    const uint64_t lim_dep = 2 * p.timeout_ns;     // the roles that depend on it
+    const MmaWarpArgs margs{tmem, sbase, bars, p.status, smem, lim_score};
 
     if (!aligned_ok) {
         // nothing runs; the error is recorded
     } else if (warp == 0 || warp == 6) {
         // ------------------------------------------------------ TMA producers
-        if (lane == 0) {
-            const bool k_ring = warp == 0;
-            const uint32_t b_full = k_ring ? b_kfull : b_vfull;
-            const uint32_t b_empty = k_ring ? b_kempty : b_vempty;
-            const int bytes = k_ring ? kKBytes : kVBytes;
-            const uint32_t dst0 = sbase + uint32_t(k_ring ? kOffK : kOffV);
-            SegmentWalk walk = walk_begin(p, pfx, pair);
-            Segment sg;
-            int jg = 0;   // pages issued so far, across segments
-            bool ok = true;
-            while (ok && walk_next(p, pfx, pair, walk, sg)) {
-                const int ntiles = seg_pages(sg);
-                const int page0 = sg.t_lo / kTile;
-                const int32_t* table = p.block_table + size_t(sg.b) * p.max_blocks;
-                // q of the next segment's request into L2 (half per CTA) a
-                // few pages before this segment ends (earlier, the page
-                // stream would evict it), so that staging it is short.
-                int q_next = -1;
-                if (k_ring) {
-                    SegmentWalk peek = walk;
-                    Segment nx;
-                    if (walk_next(p, pfx, pair, peek, nx)) q_next = nx.b;
-                }
-                auto prefetch_q = [&]() {
-                    if (q_next < 0) return;
-                    const uint32_t qbytes = uint32_t(N) * kD * 2;   // a multiple of 16
-                    const unsigned char* qb =
-                        reinterpret_cast<const unsigned char*>(p.q + size_t(q_next) * N * kD);
-                    const uint32_t half = (qbytes / 2) & ~15u;
-                    ptx::prefetch_l2(qb + rank * half, rank == 0 ? half : qbytes - half);
-                };
-                if (ntiles <= kQPrefetchPages) prefetch_q();
-                int next = ntiles > 0 ? table[page0] : 0;
-                for (int j = 0; j < ntiles; ++j, ++jg) {
-                    const int blk = next;
-                    if (j + 1 < ntiles) next = table[page0 + j + 1];
-                    if (j + kQPrefetchPages == ntiles) prefetch_q();
-                    int32_t y;
-                    if (blk >= 0 && int64_t(blk) < p.num_blocks) {
-                        y = blk * kTile;
-                    } else {
-                        if (k_ring) record_error(p.status, MLA_ERR_BAD_BLOCK_ID, blk);
-                        y = -kTile;   // wholly outside the tensor: TMA writes zeros
-                    }
-                    const int sl = jg & 1;
-                    if (!wait_phase(b_empty + 8 * sl, (uint32_t(jg >> 1) & 1u) ^ 1u, bars, p.status,
-                                    k_ring ? kSiteKEmpty : kSiteVEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::mbar_arrive_expect_tx(b_full + 8 * sl, uint32_t(bytes));
-                    const uint32_t dst = dst0 + uint32_t(sl * bytes);
-                    if (k_ring) {
-                        // The five K-ring blocks, in score order.
-                        for (int pos = 0; pos < kKPerPage; ++pos)
-                            ptx::tma_load_2d(dst + uint32_t(pos * kBlockBytes), &tmap,
-                                             64 * k_block(int(rank), pos), y, b_full + 8 * sl);
-                    } else {
-                        // This CTA's four value blocks.
-                        for (int k = 0; k < 4; ++k)
-                            ptx::tma_load_2d(dst + uint32_t(k * kBlockBytes), &tmap,
-                                             256 * int(rank) + 64 * k, y, b_full + 8 * sl);
-                    }
-                }
-            }
-            // Every issued load lands before the CTA may exit.
-            for (int j = jg > 2 ? jg - 2 : 0; j < jg; ++j)
-                wait_phase(b_full + 8 * (j & 1), uint32_t(j >> 1) & 1u, bars, p.status, kSiteDrain,
-                           true);
-        }
+        if (lane == 0)
+            page_loader<kDump>(p, &tmap, pfx, pair, rank, warp == 0, bars, smem, sbase,
+                               warp == 0 ? b_kfull : b_vfull, warp == 0 ? b_kempty : b_vempty,
+                               2 * p.timeout_ns);
+    } else if (kDump) {
+        // loader dump: only the loaders run
     } else if (warp == 1) {
         // ------------------------------------------------------ score MMAs
         const uint32_t bq[7] = {b_kfull, b_kempty, b_vfull, b_sfull, b_pfree, b_qready, b_final_qk};
@@ -666,7 +734,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             }
             ptx::cp_async_wait_all();
             ptx::mbar_arrive(b_qstaged);
-            if (!wait_phase(b_qstaged, ph, bars, p.status, kSiteQReady)) return false;
+            if (!wait_phase(b_qstaged, ph, bars, p.status, kSiteQReady, lim_dep)) return false;
 #pragma unroll 1
             for (int blk = 0; blk < kQTmemBlocks; ++blk) {
                 uint32_t r32[32];
@@ -683,7 +751,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 ptx::tmem_st32(trow + kTmemQ + uint32_t(blk * 32), r32);
             }
             ptx::mbar_arrive(b_qread);
-            if (!wait_phase(b_qread, ph, bars, p.status, kSiteQReady)) return false;
+            if (!wait_phase(b_qread, ph, bars, p.status, kSiteQReady, lim_dep)) return false;
 #pragma unroll 4
             for (int k = 0; k < 40; ++k) {
                 const int i = t + 128 * k;   // 128 rows x 40 chunks (dims 256..575)
@@ -728,7 +796,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                     ok = ptx::mbar_test_wait(b_sfull + 8 * sl, uint32_t(jg >> 1) & 1u);
                 if (!ok)
                     ok = wait_phase(b_sfull + 8 * sl, uint32_t(jg >> 1) & 1u, bars, p.status,
-                                    kSiteSFull);
+                                    kSiteSFull, lim_dep);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 ptx::tc_fence_after();
                 // The page's 64 raw scores of this head. The scale (log2
@@ -812,7 +880,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 // O rescale once the P.V of the previous page is done.
                 if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
                     ok = wait_phase(b_pfree + 8 * ((jg - 1) & 1), uint32_t((jg - 1) >> 1) & 1u, bars,
-                                    p.status, kSitePvDone);
+                                    p.status, kSitePvDone, lim_dep);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     ptx::tc_fence_after();
 #pragma unroll 1
@@ -871,7 +939,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 // earlier one too.
                 const int jl = jg0 + ntiles - 1;
                 ok = wait_phase(b_pfree + 8 * (jl & 1), uint32_t(jl >> 1) & 1u, bars, p.status,
-                                kSitePvDone);
+                                kSitePvDone, lim_dep);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 ptx::tc_fence_after();
@@ -939,7 +1007,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 // other CTAs have left (it waits for kPieceArrivals per piece).
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) atomicAdd(p.status + kReadyWord + sg.b, 1);
+                if (lane == 0) atomicAdd(p.counters + kReadyWord + sg.b, 1);
             }
             // The next segment's first P.V overwrites O: every softmax warp
             // has read it by then, since that P.V waits for all four warps
@@ -954,7 +1022,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+    if (!kDump && warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -976,7 +1044,10 @@ bool tc_kernel_built() { return true; }
 
 int tc_max_blocks() { return INT_MAX / kTile - 1; }
 
-int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream) {
+namespace {
+
+template <bool kDump>
+int launch_tc(const DecodeParams& p, int grid_ctas, void* stream) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encoder();
     if (encode == nullptr) return int(cudaErrorNotSupported);
     CUtensorMap tmap;
@@ -989,7 +1060,7 @@ int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream) {
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return int(cudaErrorInvalidValue);
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel,
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel<kDump>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return int(e);
     cudaLaunchConfig_t cfg = {};
@@ -1004,8 +1075,18 @@ int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, p, tmap);
+    e = cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<kDump>, p, tmap);
     return int(e);
+}
+
+}  // namespace
+
+int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream) {
+    return launch_tc<false>(p, grid_ctas, stream);
+}
+
+int launch_decode_tc_loader_dump(const DecodeParams& p, int grid_ctas, void* stream) {
+    return launch_tc<true>(p, grid_ctas, stream);
 }
 
 }  // namespace mla

@@ -34,6 +34,14 @@ static_assert((kDoneWord + kMaxBalancedBatch) * 4 <= int(kStatusBytes), "status 
 //                     set of request b in this call
 //   [kDoneWord + b]   merge warps done with request b; the last one resets
 //                     both words to 0 for the next call
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s
+// Test-only behaviour of the tensor-core decode kernel (DecodeParams.debug):
+// CTA 0 never issues its first K-ring load, so the score warp's wait for it
+// runs out (no fault: the wait is bounded and the kernel drains and returns).
+constexpr uint32_t kDebugWithholdLoad = 0x1u;
+// Wait limit that MLA_PLAN_DEBUG_WITHHOLD_LOAD sets (2 ms).
+constexpr uint64_t kDebugTimeoutNs = 2000000ull;
+
 struct StatusWords {
     int32_t code;
     int32_t detail;
@@ -57,7 +65,14 @@ struct DecodeParams {
     float* o_part;                // fp32 partial rows: [B, N, S, 512] (split, S > 1)
                                   //                    or [2 * pairs, N, 512] (balanced)
     float* lse_part;              // fp32 [B, N, S] or [2 * pairs, N]
-    int32_t* status;              // status header in the workspace
+    int32_t* status;              // error word and its detail (int32[2])
+    int32_t* counters;            // status header holding the page-balanced merge's
+                                  // per-request counters ([kReadyWord + b], [kDoneWord + b])
+    uint64_t timeout_ns;          // limit of a bounded wait (kDefaultTimeoutNs unless a
+                                  // test shortens it)
+    uint32_t debug;               // kDebug* bits (tests only; 0 in normal calls)
+    uint16_t* dump;               // loader dump: bf16 [2, B, dump_max_tokens, 576] or null
+    int32_t dump_max_tokens;
     // Uniform multi-token decode with the query tokens' heads as rows: row h
     // is head h % heads_per_token of query token h / heads_per_token; with
     // `causal` that token sees q_len - 1 - token fewer of the request's
@@ -71,6 +86,9 @@ struct DecodeParams {
 // Launchers (return a cudaError_t as int; 0 = success).
 int launch_decode_simt(const DecodeParams& p, void* stream);
 int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream);
+// The tensor-core kernel's page loaders alone (no MMAs): every page each CTA
+// receives is copied from its shared-memory rings to p.dump.
+int launch_decode_tc_loader_dump(const DecodeParams& p, int grid_ctas, void* stream);
 int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,
                  int v_dim, uint16_t* out, float* lse, void* stream);
 // Combine of per-rank results in rank-major layout: bf16 [world, rows, v_dim]
@@ -81,6 +99,16 @@ int launch_merge_balanced(const DecodeParams& p, void* stream);
 int launch_gather(const uint16_t* cache, int64_t num_blocks, const int32_t* block_table,
                   const int32_t* seq_lens, int batch, int max_blocks, int dst_max_tokens,
                   uint16_t* dst, int32_t* status, void* stream);
+
+// The parameters of one decode call under `plan` (status and counters both
+// in the status header `ws` unless `status` is given).
+DecodeParams make_decode_params(const mla_decode_plan_t* plan, const void* q,
+                                const void* latent_cache, int64_t num_blocks,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                float softmax_scale, void* out, float* lse, char* ws,
+                                int32_t* status, int q_len, int heads_per_token, int causal);
+// The decode kernel of `plan`, then its merge (S > 1 or page-balanced).
+int launch_decode_and_merge(const DecodeParams& p, const mla_decode_plan_t* plan, void* stream);
 
 // mla_decode with multi-token rows (q_len query tokens' heads as the rows;
 // q_len = 1 is the plain decode).

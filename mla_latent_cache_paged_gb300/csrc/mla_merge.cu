@@ -264,15 +264,15 @@ __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel
     }
     // This kernel may run while the decode grid is still working on other
     // requests: wait until every piece of request b is written (each piece
-    // counts kPieceArrivals softmax warps). Bounded: 4 s, then
-    // MLA_ERR_TIMEOUT and no output for the request.
-    int32_t* ready = p.status + kReadyWord + b;
+    // counts kPieceArrivals softmax warps). Bounded: four times the call's
+    // wait limit (4 s), then MLA_ERR_TIMEOUT and no output for the request.
+    int32_t* ready = p.counters + kReadyWord + b;
     if (threadIdx.x == 0) {
         const int target = kPieceArrivals * pieces;
         const uint64_t t0 = globaltimer_ns();
         int ok = 1;
         while (*reinterpret_cast<volatile int32_t*>(ready) < target) {
-            if (globaltimer_ns() - t0 > 4000000000ull) {
+            if (globaltimer_ns() - t0 > 4 * p.timeout_ns) {
                 record_error(p.status, MLA_ERR_TIMEOUT, kMergeWaitSite);
                 ok = 0;
                 break;
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel
     // the pieces; the last one resets both counters for the next call.
     __syncwarp();
     if (lane == 0 && go) {
-        int32_t* done = p.status + kDoneWord + b;
+        int32_t* done = p.counters + kDoneWord + b;
         if (atomicAdd(done, 1) == int(gridDim.y) * kBalMergeWarps - 1) {
             *reinterpret_cast<volatile int32_t*>(ready) = 0;
             *reinterpret_cast<volatile int32_t*>(done) = 0;

@@ -10,7 +10,6 @@
 // size that every GPU which loads the library keeps until the process exits.
 #include <cuda_runtime.h>
 
-#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -20,8 +19,10 @@
 namespace mla {
 namespace {
 
-// 32 MiB: room for the status header plus B*N*S split partials up to
-// B*N*S = 16,000 or so (2,052 bytes each), e.g. B=32, N=128, S=4.
+// 32 MiB: room for the 8 KiB status header plus split partials of 2,052
+// bytes per (request, head, split) row, each of the two arrays rounded up to
+// 256 bytes: up to 16,348 rows, e.g. B=32, N=128, S=3 (12,288 rows; S=4 is 16,384).
+// A page-balanced plan over C CTA pairs has 2*C*N rows (C=32, N=128: 8,192).
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -76,44 +77,17 @@ extern "C" int mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q,
     if (rc != MLA_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(scratch);
-    int32_t* status = device_status ? device_status : reinterpret_cast<int32_t*>(ws);
-    // The array keeps whatever the previous call left: the status words must
-    // start at zero; the split partials are written before they are read.
-    if (cudaMemsetAsync(status, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return MLA_ERR_CUDA;
-
-    const int S = plan->num_kv_splits;
-    DecodeParams p{};
-    p.q = static_cast<const uint16_t*>(q);
-    p.cache = static_cast<const uint16_t*>(latent_cache);
-    p.num_blocks = num_blocks;
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.max_blocks = plan->max_blocks_per_seq;
-    p.batch = plan->batch;
-    p.num_heads = plan->num_heads;
-    p.num_splits = S;
-    p.scale_log2 = softmax_scale * 1.4426950408889634f;
-    // A zero scale weighs every token 1; the smallest normal scale does the
-    // same in fp32 (every scaled score rounds 2^x to 1) and keeps the
-    // tensor-core kernel's scaled masking sentinel at -inf.
-    if (p.scale_log2 == 0.f) p.scale_log2 = FLT_MIN;
-    p.out = static_cast<uint16_t*>(out);
-    p.lse = lse;
-    p.status = status;
-    p.sched_pairs = plan->sched_pairs;
-    if (S > 1 || plan->sched_pairs > 0) {
-        p.o_part = reinterpret_cast<float*>(ws + plan->partial_offset);
-        p.lse_part = reinterpret_cast<float*>(ws + plan->lse_partial_offset);
-    }
-    int e = plan->kernel == MLA_KERNEL_TC ? launch_decode_tc(p, plan->grid_ctas, stream)
-                                          : launch_decode_simt(p, stream);
-    if (e != 0) return MLA_ERR_CUDA;
-    if (plan->sched_pairs > 0) {
-        if (launch_merge_balanced(p, stream) != 0) return MLA_ERR_CUDA;
-    } else if (S > 1) {
-        e = launch_merge(p.o_part, p.lse_part, plan->batch * plan->num_heads, S, kLkv, p.out,
-                         lse, stream);
-        if (e != 0) return MLA_ERR_CUDA;
-    }
-    return MLA_OK;
+    // The array keeps whatever the previous call left. The status words
+    // start at zero; so do the page-balanced merge's counters, which stay in
+    // the array's own status header even when the status goes to
+    // device_status (a call that timed out may have left them non-zero, and
+    // the caller cannot re-initialise this array). The split partials are
+    // written before they are read.
+    if (cudaMemsetAsync(ws, 0, kStatusBytes, s) != cudaSuccess) return MLA_ERR_CUDA;
+    if (device_status && cudaMemsetAsync(device_status, 0, 2 * sizeof(int32_t), s) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    const DecodeParams p = make_decode_params(plan, q, latent_cache, num_blocks, block_table,
+                                              seq_lens, softmax_scale, out, lse, ws,
+                                              device_status, 1, plan->num_heads, 0);
+    return launch_decode_and_merge(p, plan, stream);
 }

@@ -263,6 +263,23 @@ extern "C" int mla_dcp_local_seq_lens(const int32_t* seq_lens_host, int batch, i
     return MLA_OK;
 }
 
+extern "C" int mla_multi_token_row_lens(const int32_t* seq_lens_host, int batch, int q_len,
+                                        int causal, int32_t* row_lens_host) {
+    if (!seq_lens_host || !row_lens_host || batch < 0 || q_len < 1) return MLA_ERR_INVALID_ARG;
+    for (int b = 0; b < batch; ++b)
+        if (seq_lens_host[b] < 0) return MLA_ERR_INVALID_ARG;
+    for (int b = 0; b < batch; ++b) {
+        for (int i = 0; i < q_len; ++i) {
+            // Query token i sits at position L - q_len + i and, causally,
+            // sees the tokens up to and including its own position.
+            const int64_t L = seq_lens_host[b];
+            const int64_t seen = causal ? L - (q_len - 1 - i) : L;
+            row_lens_host[int64_t(b) * q_len + i] = int32_t(seen > 0 ? seen : 0);
+        }
+    }
+    return MLA_OK;
+}
+
 extern "C" const char* mla_status_string(int status) {
     switch (status) {
         case MLA_OK: return "ok";

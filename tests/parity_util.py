@@ -26,6 +26,36 @@ LSE_ATOL = 1e-3
 BF16_UNIT_ROUNDOFF = 2.0 ** -8
 
 
+def oracle_rows_chunked(w, requests, max_tokens=1 << 18):
+    """oracle_rows over `requests` in groups of at most `max_tokens` cached
+    tokens (bounds the float64 copy of the pages: 1.2 GB per 2^18 tokens of
+    576 float64 columns), concatenated in request order."""
+    requests = list(requests)
+    outs, lses, group, tokens = [], [], [], 0
+    for b in requests + [None]:
+        L = 0 if b is None else int(w.seq_lens[b])
+        if group and (b is None or tokens + L > max_tokens):
+            o, l = oracle_rows(w, group)
+            outs.append(o)
+            lses.append(l)
+            group, tokens = [], 0
+        if b is not None:
+            group.append(b)
+            tokens += L
+    return np.concatenate(outs), np.concatenate(lses)
+
+
+def max_abs_err(got, ref):
+    """max |got - ref| over entries where both are finite (an LSE of -inf on
+    both sides counts as equal)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    same_inf = np.isinf(got) & np.isinf(ref) & (np.sign(got) == np.sign(ref))
+    with np.errstate(invalid="ignore"):
+        err = np.where(same_inf, 0.0, np.abs(got - ref))
+    return float(np.max(err)) if err.size else 0.0
+
+
 def bf16_ulp(x):
     x = np.abs(np.asarray(x, dtype=np.float64))
     e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))

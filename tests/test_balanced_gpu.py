@@ -150,11 +150,14 @@ def test_merge_wait_runs_out_and_reports_a_timeout():
     words = ws[:8].view(torch.int32).cpu().numpy()
     assert words[0] == binding.MLA_ERR_TIMEOUT and words[1] == 20, words
     assert binding.read_error(ws) == binding.MLA_ERR_TIMEOUT
-    ws2 = binding.new_workspace(plan)
+    assert binding.load_library().mla_workspace_init(binding._ptr(ws), ws.numel(),
+                                                     binding._stream_ptr(None)) == 0
     out, lse = binding.mla_decode(q, cache, table, lens_d, w.softmax_scale, plan=plan,
-                                  workspace=ws2)
+                                  workspace=ws)
     torch.cuda.synchronize()
-    assert binding.read_error(ws2) == 0
+    assert binding.read_error(ws) == 0
+    header = ws[:binding.STATUS_BYTES].view(torch.int32).cpu().numpy()
+    assert not header.any(), np.nonzero(header)
     ref_out, ref_lse = oracle_rows(w, range(w.batch))
     assert_out_close(bf16_bits_to_f64(bf16_tensor_bits(out)), ref_out, "after the timeout",
                      value_abs_max(w, range(w.batch)))

@@ -9,8 +9,8 @@ from mla_latent_cache_paged_gb300 import binding
 from mla_latent_cache_paged_gb300.workloads import (BF16_NAN, bf16_tensor_bits, get_workload,
                                                     make_workload, to_torch)
 from oracle import merge_partials, mla_decode_split_partials
-from parity_util import (assert_lse_close, assert_out_close, oracle_rows, run_decode,
-                         value_abs_max)
+from parity_util import (OUT_ATOL, assert_lse_close, assert_out_close, max_abs_err,
+                         oracle_rows, oracle_rows_chunked, run_decode, value_abs_max)
 
 pytestmark = pytest.mark.gpu
 
@@ -160,35 +160,44 @@ def test_bad_seq_len_is_reported(kernel):
 
 # ---------------------------------------------------------------- full size
 
-@pytest.mark.parametrize("name,sample", [
-    ("b1_n16_l256_pool8", None),
-    ("b32_n128_l1k-4k", None),
-    ("b128_n128_l8192", [0, 17, 63, 64, 101, 127]),
-    ("b16_n128_l8192", [0, 7, 15]),
-    ("b4_n128_l32k_s64", None),
-    ("b4_n128_l64k_s64", [0, 3]),
-    ("b4_n128_l96k_s64", [1]),
-    ("b4_n128_l128k_s64", [0, 2]),
-    ("b256_n128_logu16-32k_outliers", "mix"),
-])
-def test_full_size_configs(name, sample):
-    """Full-size configs in the launch configuration the benchmark uses
-    (the planner's kernel and split count), checked on sampled requests."""
+# The stated bounds (bf16 out 2e-2 absolute, LSE 1e-3 absolute) hold on every
+# request of the N(0, 1) configurations with no allowance for the bf16
+# rounding of the softmax weights. Only the workload with x8 outlier rows
+# keeps that allowance (out within max(2e-2, one bf16 ulp of the oracle,
+# 2^-8 * max_t |V[t, d]|)): there a few scaled rows dominate short requests,
+# |out| reaches 8-32 and half a bf16 ulp alone exceeds 2e-2.
+FULL_SIZE = [
+    ("b1_n16_l256_pool8", True),
+    ("b32_n128_l1k-4k", True),
+    ("b128_n128_l8192", True),
+    ("b16_n128_l8192", True),
+    ("b4_n128_l32k_s64", True),
+    ("b4_n128_l64k_s64", True),
+    ("b4_n128_l96k_s64", True),
+    ("b4_n128_l128k_s64", True),
+    ("b256_n128_logu16-32k_outliers", False),
+]
+
+
+@pytest.mark.parametrize("name,strict", FULL_SIZE)
+def test_full_size_configs(name, strict):
+    """Full-size configs in the launch configuration the benchmark uses (the
+    planner's kernel, schedule and split count), every request of every
+    config against the oracle."""
     w = get_workload(name)
     got, lse, plan, _ = run_decode(w)
-    if sample is None:
-        reqs = list(range(w.batch))
-    elif sample == "mix":
-        order = np.argsort(w.seq_lens)
-        reqs = sorted(set(order[:6].tolist() + order[-4:].tolist() + [100, 200]))
+    reqs = list(range(w.batch))
+    ref_out, ref_lse = oracle_rows_chunked(w, reqs)
+    if strict:
+        err = np.abs(got - ref_out)
+        worst = np.unravel_index(np.argmax(err), err.shape)
+        assert err.max() <= OUT_ATOL, (name, float(err.max()), worst)
     else:
-        reqs = sample
-    ref_out, ref_lse = oracle_rows(w, reqs)
-    e_out = assert_out_close(got[reqs], ref_out, name, value_abs_max(w, reqs))
-    strict = float(np.abs(got[reqs] - ref_out).max())
-    e_lse = assert_lse_close(lse[reqs], ref_lse, name)
-    print(f"{name}: kernel={plan.kernel} S={plan.num_kv_splits} "
-          f"max|out err|={strict:.3g} max|lse err|={e_lse:.3g}")
+        assert_out_close(got, ref_out, name, value_abs_max(w, reqs))
+    assert_lse_close(lse, ref_lse, name)
+    print(f"{name}: kernel={plan.kernel} S={plan.num_kv_splits} pairs={plan.sched_pairs} "
+          f"max|out err|={max_abs_err(got, ref_out):.3g} "
+          f"max|lse err|={max_abs_err(lse, ref_lse):.3g}")
 
 
 def test_output_at_a_16_byte_offset_matches_aligned_output():

@@ -53,6 +53,9 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
     build.build()
     plan = binding.make_plan(4, 128, 2048, num_kv_splits=64)   # 4*128*64*2052 B of partials
     assert plan.workspace_bytes > (32 << 20)
+    # The stated bound: 16,348 partial rows fit, e.g. B=32, N=128, S=3, and S=4 does not.
+    assert binding.make_plan(32, 128, 64, num_kv_splits=3).workspace_bytes <= (32 << 20)
+    assert binding.make_plan(32, 128, 64, num_kv_splits=4).workspace_bytes > (32 << 20)
     import torch
     q = torch.zeros((4, 128, 576), dtype=torch.bfloat16, device="cuda")
     cache = torch.zeros((8, 64, 576), dtype=torch.bfloat16, device="cuda")
@@ -61,3 +64,78 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
     with pytest.raises(binding.MlaError) as info:
         binding.mla_decode_noalloc(q, cache, table, seq, 0.07, plan=plan)
     assert info.value.status == binding.MLA_ERR_SCRATCH_LIMIT
+
+
+def _balanced_case(seed):
+    lens = [1000, 3000, 64, 2000, 1, 700, 129, 4096]
+    w = make_workload("noalloc_bal", len(lens), 128, lens, seed=seed, extra_blocks=2,
+                      num_kv_splits=0)
+    return w
+
+
+def test_noalloc_page_balanced_writes_only_its_two_status_words():
+    """A page-balanced plan: the merge's per-request counters stay in the
+    library's scratch. device_status is the first two words of a larger
+    buffer filled with a sentinel; every other word must keep it."""
+    import torch
+    build.build()
+    w = _balanced_case(501)
+    q, cache, table, seq = to_torch(w)
+    plan = binding.make_plan(w.batch, 128, w.max_blocks_per_seq, seq_lens_host=w.seq_lens,
+                             max_seq_len=w.max_seq_len, schedule="balanced", num_sms=64)
+    assert plan.sched_pairs == 32 and plan.workspace_bytes <= (32 << 20)
+    ws = binding.new_workspace(plan)
+    ref_out, ref_lse = binding.mla_decode(q, cache, table, seq, w.softmax_scale, plan=plan,
+                                          workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.read_error(ws) == 0
+    ref = bf16_bits_to_f64(bf16_tensor_bits(ref_out))
+    vmax = value_abs_max(w, range(w.batch))
+    guard = torch.full((4096,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        out, lse = binding.mla_decode_noalloc(q, cache, table, seq, w.softmax_scale, plan=plan,
+                                              device_status=guard[:2])
+        torch.cuda.synchronize()
+        words = guard.cpu().numpy()
+        assert words[0] == 0 and words[1] == 0, words[:2]
+        assert np.all(words[2:] == 0x5A5A5A5A), np.nonzero(words[2:] != 0x5A5A5A5A)
+        got = bf16_bits_to_f64(bf16_tensor_bits(out))
+        assert_out_close(got, ref, "noalloc balanced vs mla_decode", vmax)
+        assert_lse_close(lse.double().cpu().numpy(), ref_lse.double().cpu().numpy(),
+                         "noalloc balanced lse")
+
+
+def test_noalloc_after_a_timed_out_call_starts_from_clean_counters():
+    """A call that times out leaves the balanced merge's counters part-way in
+    the library's scratch (no caller can reset that array). The test flag
+    MLA_PLAN_DEBUG_WITHHOLD_LOAD makes one call time out without a fault;
+    the next ordinary call must still match mla_decode."""
+    import torch
+    build.build()
+    w = _balanced_case(502)
+    q, cache, table, seq = to_torch(w)
+    kw = dict(seq_lens_host=w.seq_lens, max_seq_len=w.max_seq_len, schedule="balanced",
+              num_sms=64)
+    plan = binding.make_plan(w.batch, 128, w.max_blocks_per_seq, **kw)
+    bad = binding.make_plan(w.batch, 128, w.max_blocks_per_seq,
+                            extra_flags=binding.MLA_PLAN_DEBUG_WITHHOLD_LOAD, **kw)
+    ws = binding.new_workspace(plan)
+    ref_out, ref_lse = binding.mla_decode(q, cache, table, seq, w.softmax_scale, plan=plan,
+                                          workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.read_error(ws) == 0
+    status = torch.zeros(2, dtype=torch.int32, device="cuda")
+    binding.mla_decode_noalloc(q, cache, table, seq, w.softmax_scale, plan=bad,
+                               device_status=status)
+    torch.cuda.synchronize()
+    assert int(status[0].item()) == binding.MLA_ERR_TIMEOUT
+    for _ in range(2):
+        out, lse = binding.mla_decode_noalloc(q, cache, table, seq, w.softmax_scale, plan=plan,
+                                              device_status=status)
+        torch.cuda.synchronize()
+        assert int(status[0].item()) == 0
+        assert_out_close(bf16_bits_to_f64(bf16_tensor_bits(out)),
+                         bf16_bits_to_f64(bf16_tensor_bits(ref_out)), "noalloc after timeout",
+                         value_abs_max(w, range(w.batch)))
+        assert_lse_close(lse.double().cpu().numpy(), ref_lse.double().cpu().numpy(),
+                         "noalloc after timeout lse")
