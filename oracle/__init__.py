@@ -11,11 +11,14 @@ from .mla_oracle import (  # noqa: F401
     dcp_decode_partials,
     dcp_local_seq_lens,
     dcp_owner,
+    dequantize_e4m3_cache,
+    e4m3_to_float,
     gather_request_latent,
     merge_partials,
     mha_compute_friendly,
     mla_decode_multi_token_reference,
     mla_decode_reference,
+    mla_decode_reference_fp8,
     mla_decode_split_partials,
     q_absorb_concat_cache,
     split_token_ranges,

@@ -35,6 +35,12 @@ Pins (see ``tests/test_oracle.py``):
     definition; each query token equals the single-token definition over the
     tokens it sees; torch SDPA in float64 with the causal block mask; a
     hand-worked two-token case.
+  * ``e4m3_to_float`` -- a golden table of codes worked by hand from the
+    format, every one of the 256 codes against torch's ``float8_e4m3fn``,
+    order and sign symmetry; ``mla_decode_reference_fp8`` -- a hand-worked
+    fp8 case, and equality (bit for bit in float64) with the bf16 definition
+    when the scale is a power of two, so that every dequantized value is
+    also a bf16 number.
 No function here is "parity unpinned".
 """
 
@@ -395,3 +401,50 @@ def mla_decode_multi_token_reference(q, cache, block_table, seq_lens, softmax_sc
                 lse[b, i, h] = m + math.log(s)
                 out[b, i, h] = (e / s) @ k_rows[:, :kv_lora_rank]
     return out, lse
+
+
+def e4m3_to_float(bits):
+    """8-bit floating point E4M3 codes -> float64 values.
+
+    The pages store a plain per-tensor fp8 latent cache as bytes and have the
+    attention read it "as E4M3" (raon-1-mini MLA page,
+    ``_attn_read_kv_cache``; vLLM ``mla_attention`` API docs,
+    ``MLAAttention.forward_impl``: ``kv_cache.view(current_platform.fp8_dtype())``).
+    The format is not printed there; this is the OCP 8-bit floating point
+    E4M3 encoding, the finite variant NVIDIA hardware and torch's
+    ``float8_e4m3fn`` use: bit 7 the sign, bits 6..3 the exponent e (bias 7),
+    bits 2..0 the mantissa m. e = 0 encodes the subnormals m * 2^-9; otherwise
+    the value is (1 + m / 8) * 2^(e - 7). There are no infinities; the codes
+    with all seven low bits set (0x7F, 0xFF) are NaN, so the largest finite
+    magnitude is 1.75 * 2^8 = 448.
+    """
+    b = np.asarray(bits).astype(np.int64) & 0xFF
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    val = sign * mag
+    return np.where((b & 0x7F) == 0x7F, np.nan, val)
+
+
+def dequantize_e4m3_cache(cache_bits, k_scale):
+    """A per-tensor-scaled fp8 cache as float64: ``e4m3(code) * k_scale``.
+
+    vLLM ``mla_attention`` API docs, ``MLAAttention.forward``: the cache
+    update and the attention take the layer's single ``_k_scale`` with the
+    cache dtype (per-tensor scale); the stored code times that scale is the
+    latent entry.
+    """
+    return e4m3_to_float(cache_bits) * float(k_scale)
+
+
+def mla_decode_reference_fp8(q, cache_bits, block_table, seq_lens, softmax_scale, k_scale,
+                             kv_lora_rank=512):
+    """Absorbed MLA decode over an fp8 (E4M3, per-tensor ``k_scale``) latent
+    cache: the definition of ``mla_decode_reference`` applied to the
+    dequantized cache. K is the whole dequantized entry and V its first
+    ``Lkv`` columns; the query stays in its own precision (a backend that
+    takes a quantized query is optional on the vLLM page:
+    ``supports_quant_query_input``)."""
+    return mla_decode_reference(q, dequantize_e4m3_cache(cache_bits, k_scale), block_table,
+                                seq_lens, softmax_scale, kv_lora_rank)

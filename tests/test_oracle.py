@@ -521,3 +521,92 @@ def test_multi_token_matches_torch_sdpa_with_the_causal_block_mask():
     scores = (qt @ k.transpose(1, 2)) * 0.05
     ref_lse = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), dim=-1)   # [N, T]
     np.testing.assert_allclose(lse[0].T, ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- fp8 (E4M3) cache
+
+def _code(text):
+    return int(text, 16)
+
+
+def test_e4m3_golden_codes():
+    from oracle import e4m3_to_float
+    with open(os.path.join(GOLDEN, "e4m3_decode.json")) as f:
+        g = json.load(f)
+    for case in g["cases"]:
+        got = float(e4m3_to_float(np.array([_code(case["code"])], dtype=np.uint8))[0])
+        want = case["value"]
+        if want == "nan":
+            assert math.isnan(got), case
+        else:
+            assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), case
+
+
+def test_e4m3_every_code_matches_torch_float8_e4m3fn():
+    """Library special case: torch's float8_e4m3fn decodes the same 256 codes."""
+    import torch
+    from oracle import e4m3_to_float
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = e4m3_to_float(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_e4m3_order_and_symmetry():
+    from oracle import e4m3_to_float
+    pos = e4m3_to_float(np.arange(0x7F, dtype=np.uint8))          # 0x00 .. 0x7E
+    assert np.all(np.diff(pos) > 0) and pos[-1] == 448.0
+    neg = e4m3_to_float(np.arange(0x80, 0xFF, dtype=np.uint8))
+    np.testing.assert_array_equal(neg, -pos)
+    # 126 distinct positive finite values, plus zero
+    assert len(set(pos.tolist())) == 127
+
+
+def test_golden_hand_worked_fp8_decode():
+    from oracle import mla_decode_reference_fp8
+    with open(os.path.join(GOLDEN, "decode_fp8_hand_worked.json")) as f:
+        g = json.load(f)
+    codes = np.array([[[_code(c) for c in row] for row in blk] for blk in g["cache_codes"]],
+                     dtype=np.uint8)
+    table = np.array(g["block_table"], dtype=np.int64)
+    seq = np.array(g["seq_lens"])
+    q = np.array(g["q"], dtype=np.float64)
+    from oracle import dequantize_e4m3_cache
+    deq = dequantize_e4m3_cache(codes, g["k_scale"])
+    got_rows = gather_request_latent(deq, table[0], seq[0], g["page_size"])
+    np.testing.assert_array_equal(got_rows, np.array(g["dequantized_rows"], dtype=np.float64))
+    out, lse = mla_decode_reference_fp8(q, codes, table, seq, math.log(2.0), g["k_scale"],
+                                        kv_lora_rank=g["kv_lora_rank"])
+    np.testing.assert_allclose(out, np.array(g["expected_out"]), rtol=0, atol=1e-14)
+    exact = np.array([[_exact(x) for x in row] for row in g["expected_lse_exact"]])
+    np.testing.assert_allclose(lse, exact, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, np.array(g["expected_lse"]), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("log2_scale", [-3, 0, 2])
+def test_fp8_decode_equals_bf16_decode_on_exact_values(log2_scale):
+    """With a power-of-two k_scale every dequantized entry is a bf16 number
+    (3 mantissa bits in 7, exponents in range), so the fp8 definition must
+    equal the bf16 one on the bf16 encoding of the same values, bit for bit
+    in float64."""
+    from oracle import dequantize_e4m3_cache, mla_decode_reference_fp8
+    from mla_latent_cache_paged_gb300.workloads import bf16_bits_to_f64, f32_to_bf16_bits
+    rng = np.random.default_rng(40 + log2_scale)
+    nb, ps, width = 7, 4, 24
+    codes = rng.integers(0, 256, size=(nb, ps, width), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38              # no NaN codes in the live rows
+    k_scale = 2.0 ** log2_scale
+    deq = dequantize_e4m3_cache(codes, k_scale)
+    bf16 = bf16_bits_to_f64(f32_to_bf16_bits(deq.astype(np.float32)))
+    assert np.array_equal(bf16, deq)                   # the values are bf16 numbers
+    table = np.array([[3, 0, 6], [5, 1, -1]])
+    seq = [10, 7]
+    q = rng.standard_normal((2, 3, width))
+    a_out, a_lse = mla_decode_reference_fp8(q, codes, table, seq, 0.05, k_scale, kv_lora_rank=16)
+    b_out, b_lse = mla_decode_reference(q, bf16, table, seq, 0.05, kv_lora_rank=16)
+    assert np.array_equal(a_out, b_out) and np.array_equal(a_lse, b_lse)

@@ -62,3 +62,29 @@ def test_named_workloads_have_stated_shapes():
     assert c3.total_tokens == 128 * 8192 and c3.num_blocks == 16384
     c5 = shapes["b256_n128_logu16-32k_outliers"]
     assert c5.batch == 256 and c5.seq_lens.min() >= 16 and c5.seq_lens.max() <= 32768
+
+
+def test_e4m3_quantizer_matches_torch_and_saturates():
+    import torch
+    from mla_latent_cache_paged_gb300.workloads import f32_to_e4m3_bits
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(1 << 16).astype(np.float32) * 60,
+                        rng.standard_normal(1 << 12).astype(np.float32) * 0.01,
+                        np.array([0.0, -0.0, 2 ** -10, 3 * 2 ** -10, 447.0], np.float32)])
+    got = f32_to_e4m3_bits(x)
+    inr = np.abs(x) <= 448
+    ref = torch.from_numpy(x[inr]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got[inr], ref)
+    big = f32_to_e4m3_bits(np.array([464.0, 1e9, -1e9, np.nan], np.float32))
+    assert big.tolist() == [0x7E, 0x7E, 0xFE, 0x7F]
+
+
+def test_fp8_workloads_share_the_bf16_layout():
+    from mla_latent_cache_paged_gb300.workloads import get_workload
+    a = get_workload("b1_n16_l256_pool8")
+    b = get_workload("b1_n16_l256_pool8_fp8")
+    assert b.cache_dtype == "fp8" and b.cache_bits.dtype == np.uint8
+    assert np.array_equal(a.block_table, b.block_table) and np.array_equal(a.q_bits, b.q_bits)
+    assert 0 < b.k_scale < 1
+    # tail rows past L hold the NaN code
+    assert a.seq_lens[0] % 64 == 0 or np.all(b.cache_bits[b.block_table[0, -1], 64:] == 0x7F)
