@@ -77,14 +77,15 @@ def algorithmic_work(w):
     """Bytes the method must move and flops it must do for one decode call.
 
     bytes = 1152 per cached token (one 576-wide bf16 entry read once for all
-    heads) + 1152 per (request, head) for q + 1024 per (request, head) for the
-    bf16 output + 4 per (request, head) for the LSE + 4 per block-table entry
-    used. flops = 2 * (576 + 512) per (token, head).
+    heads; 576 for an fp8 cache) + 1152 per (request, head) for q + 1024 per
+    (request, head) for the bf16 output + 4 per (request, head) for the LSE +
+    4 per block-table entry used. flops = 2 * (576 + 512) per (token, head).
     """
     T = w.total_tokens
     BN = w.batch * w.num_heads
     pages = sum(-(-int(L) // w.page_size) for L in w.seq_lens)
-    nbytes = 1152 * T + 1152 * BN + 1024 * BN + 4 * BN + 4 * pages
+    per_token = 576 if getattr(w, "cache_dtype", "bf16") == "fp8" else 1152
+    nbytes = per_token * T + 1152 * BN + 1024 * BN + 4 * BN + 4 * pages
     flops = 2 * (576 + 512) * w.num_heads * T
     return nbytes, flops
 
@@ -95,8 +96,10 @@ def roofline_of(w, ms, peaks):
     t_s = ms / 1e3
     t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
     gbs = nbytes / t_s / 1e9
-    return {"achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
-            "frac_of_roofline": t_roof / t_s, "t_roof_us": t_roof * 1e6,
+    tflops = flops / t_s / 1e12
+    tensor = flops / (peaks["bf16_tflops"] * 1e12) > nbytes / (peaks["hbm_gbs"] * 1e9)
+    return {"achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"], "achieved_tflops": tflops,
+            "tensor_bound": tensor, "frac_of_roofline": t_roof / t_s, "t_roof_us": t_roof * 1e6,
             "algorithmic_bytes": nbytes, "algorithmic_flops": flops}
 
 
@@ -222,9 +225,11 @@ def cpu_parity(w, got_out_bits, got_lse, strict):
     (out 2e-2, LSE 1e-3; the x8-outlier workload's out bound also allows one
     bf16 ulp of the oracle and 2^-8 max_t |V[t, d]|, the bf16-weight term)."""
     import numpy as np
-    from oracle import mla_decode_reference
+    from oracle import dequantize_e4m3_cache, mla_decode_reference
     from mla_latent_cache_paged_gb300.workloads import bf16_bits_to_f64
 
+    fp8 = w.cache_dtype == "fp8"
+    widen = (lambda c: dequantize_e4m3_cache(c, w.k_scale)) if fp8 else bf16_bits_to_f64
     t0 = time.perf_counter()
     got = bf16_bits_to_f64(got_out_bits)
     e_out = e_lse = 0.0
@@ -232,7 +237,7 @@ def cpu_parity(w, got_out_bits, got_lse, strict):
     for b in range(w.batch):
         L = int(w.seq_lens[b])
         n = -(-L // w.page_size)
-        pool = bf16_bits_to_f64(w.cache_bits[w.block_table[b, :n].astype(np.int64)]) if n else \
+        pool = widen(w.cache_bits[w.block_table[b, :n].astype(np.int64)]) if n else \
             np.zeros((1, w.page_size, 576))
         ref_o, ref_l = mla_decode_reference(bf16_bits_to_f64(w.q_bits[b:b + 1]), pool,
                                             np.arange(max(n, 1))[None, :], [L], w.softmax_scale)
@@ -520,6 +525,7 @@ OTHER_CONFIGS = [
     ("b4_n128_l96k_s64", True),
     ("b4_n128_l128k_s64", True),
     ("b256_n128_logu16-32k_outliers", False),
+    ("b128_n128_l8192_fp8", True),
 ]
 
 
@@ -550,9 +556,14 @@ def run_configs(args, with_parity):
         out = torch.empty((w.batch, w.num_heads, 512), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((w.batch, w.num_heads), dtype=torch.float32, device=dev)
 
-        def call():
-            binding.mla_decode(q, cache, table, lens, w.softmax_scale, plan=plan, out=out,
-                               lse=lse, workspace=ws)
+        if w.cache_dtype == "fp8":
+            def call():
+                binding.mla_decode_fp8(q, cache, table, lens, w.softmax_scale, w.k_scale,
+                                       plan=plan, out=out, lse=lse, workspace=ws)
+        else:
+            def call():
+                binding.mla_decode(q, cache, table, lens, w.softmax_scale, plan=plan, out=out,
+                                   lse=lse, workspace=ws)
 
         for _ in range(5):
             flush.zero_()
@@ -582,15 +593,23 @@ def run_configs(args, with_parity):
         roof = roofline_of(w, ms, peaks)
         row = {
             "workload": name, "batch": w.batch, "heads": w.num_heads,
-            "cached_tokens": w.total_tokens, "ms_per_step": ms,
+            "cached_tokens": w.total_tokens, "cache_dtype": w.cache_dtype,
+            **({"k_scale": w.k_scale} if w.cache_dtype == "fp8" else {}),
+            "ms_per_step": ms,
             "value": w.total_tokens * w.num_heads / (ms / 1e3), "unit": UNIT,
             "reps": len(events), "timing": "median of per-call CUDA events, L2 flushed between",
             "num_kv_splits": plan.num_kv_splits,
             "schedule": (f"page-balanced over {plan.sched_pairs} CTA pairs + merge"
                          if plan.sched_pairs > 0 else f"split S={plan.num_kv_splits}"),
             "kernel": {1: "simt", 2: "tcgen05"}[plan.kernel],
-            "roofline": {"bound": "hbm", "achieved": roof["achieved_gbs"],
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": roof["frac"],
+            "roofline": ({"bound": "tensor", "achieved": roof["achieved_tflops"],
+                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                          "frac": roof["achieved_tflops"] / peaks["bf16_tflops"],
+                          "note": "f16 operands (same dense rate as bf16); HBM at "
+                                  f"{roof['frac']:.3f} of measured"}
+                         if roof["tensor_bound"] else
+                         {"bound": "hbm", "achieved": roof["achieved_gbs"],
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": roof["frac"]}) | {
                          "frac_of_roofline": roof["frac_of_roofline"],
                          "t_roof_us": roof["t_roof_us"],
                          "algorithmic_bytes_per_call": roof["algorithmic_bytes"]},

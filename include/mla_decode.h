@@ -61,6 +61,7 @@ extern "C" {
 #define MLA_ERR_BAD_SEQ_LEN   -6  /* device: seq_len < 0 or > max_blocks_per_seq*page_size */
 #define MLA_ERR_TIMEOUT       -7  /* device: a bounded wait inside a kernel expired */
 #define MLA_ERR_SCRATCH_LIMIT -8  /* mla_decode_noalloc: plan needs more than its fixed scratch */
+#define MLA_ERR_RANGE         -9  /* device: mla_decode_fp8 saw a q entry beyond +-65504 */
 
 /* Kernel variants the planner can choose (mla_decode_plan_t.kernel). */
 #define MLA_KERNEL_SIMT   1  /* CUDA-core split kernel, any 1 <= N <= 128 */
@@ -194,6 +195,36 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* latent_
                int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
                float softmax_scale, void* out, float* lse,
                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode_fp8 -- mla_decode over an fp8 latent cache: E4M3 codes with one
+ * per-tensor scale (vLLM mla_attention API docs, MLAAttention.forward_impl:
+ * an fp8 cache other than fp8_ds_mla is viewed as the platform's fp8 dtype
+ * and read with the layer's _k_scale; raon-1-mini MLA page,
+ * _attn_read_kv_cache: a plain per-tensor fp8 cache is read as E4M3). Entry
+ * t of the cache is k_scale * e4m3(code): K[t] all 576 of them, V[t] the
+ * first 512. The query stays bf16 and the outputs are as for mla_decode.
+ *
+ *   plan            from mla_decode_plan (the same plans as mla_decode; it
+ *                   must use MLA_KERNEL_TC, else MLA_ERR_UNSUPPORTED).
+ *   latent_cache_fp8  device, uint8 [num_blocks, 64, 576] E4M3 codes
+ *                   (OCP 8-bit floating point E4M3: sign, 4 exponent bits with
+ *                   bias 7, 3 mantissa bits, no infinities, 0x7F/0xFF NaN),
+ *                   16-byte aligned. 36,864 bytes per page.
+ *   k_scale         finite, > 0.
+ *   q               bf16 [B, N, 576]; every entry within +-65504 (the kernel
+ *                   multiplies in f16, into which every E4M3 value and every
+ *                   such bf16 value convert exactly; a larger entry is
+ *                   recorded as MLA_ERR_RANGE, detail = its request).
+ *   other arguments as for mla_decode.
+ * The tensor cores take f16 operands (q, the widened cache entries and the
+ * softmax weights, which are rounded to f16 instead of bf16); everything else
+ * is the arithmetic of mla_decode.
+ */
+int mla_decode_fp8(const mla_decode_plan_t* plan, const void* q, const void* latent_cache_fp8,
+                   int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                   float softmax_scale, float k_scale, void* out, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * mla_decode_noalloc -- mla_decode for callers that cannot allocate device

@@ -22,6 +22,7 @@ MLA_ERR_BAD_BLOCK_ID = -5
 MLA_ERR_BAD_SEQ_LEN = -6
 MLA_ERR_TIMEOUT = -7
 MLA_ERR_SCRATCH_LIMIT = -8
+MLA_ERR_RANGE = -9
 
 MLA_KERNEL_SIMT = 1
 MLA_KERNEL_TC = 2
@@ -42,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "mla_decode_noalloc", "mla_dcp_local_seq_lens", "mla_dcp_combine",
     "mla_q_absorb_concat_cache", "mla_v_up_proj", "mla_multi_token_scratch_bytes",
     "mla_decode_multi_token", "mla_debug_loader_pages", "mla_multi_token_row_lens",
+    "mla_decode_fp8",
 )
 
 
@@ -95,6 +97,8 @@ def load_library(path=None):
     lib.mla_workspace_init.argtypes = [vp, sz, vp]
     lib.mla_decode.argtypes = [ctypes.POINTER(MlaDecodePlan), vp, vp, i64, vp, vp, f32, vp, vp,
                                vp, sz, vp]
+    lib.mla_decode_fp8.argtypes = [ctypes.POINTER(MlaDecodePlan), vp, vp, i64, vp, vp, f32, f32,
+                                   vp, vp, vp, sz, vp]
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
     lib.mla_read_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
     lib.mla_status_string.argtypes = [i32]
@@ -243,6 +247,43 @@ def mla_decode(q, latent_cache, block_table, seq_lens, softmax_scale, *, plan=No
         _ptr(block_table), _ptr(seq_lens), float(softmax_scale), _ptr(out), _ptr(lse),
         _ptr(workspace), int(workspace.numel()), _stream_ptr(stream))
     _check(rc, "mla_decode")
+    return out, lse
+
+
+def mla_decode_fp8(q, latent_cache_fp8, block_table, seq_lens, softmax_scale, k_scale, *,
+                   plan=None, num_kv_splits=0, out=None, lse=None, return_lse=True,
+                   workspace=None, stream=None):
+    """Absorbed MLA decode over an fp8 cache (uint8 E4M3 codes ``[num_blocks,
+    64, 576]`` with a per-tensor ``k_scale``). Returns ``(out bf16 [B,N,512],
+    lse fp32 [B,N] | None)``; one ``mla_decode_fp8`` call."""
+    import torch
+    B, N, D = q.shape
+    if D != HEAD_DIM:
+        raise ValueError(f"q last dim must be {HEAD_DIM}")
+    _check_tensor(q, "q", torch.bfloat16)
+    _check_tensor(latent_cache_fp8, "latent_cache_fp8", torch.uint8)
+    if latent_cache_fp8.dim() != 3 or latent_cache_fp8.shape[1:] != (PAGE_SIZE, HEAD_DIM):
+        raise ValueError("latent_cache_fp8 must be [num_blocks, 64, 576]")
+    _check_tensor(block_table, "block_table", torch.int32)
+    _check_tensor(seq_lens, "seq_lens", torch.int32, (B,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks_per_seq]")
+    if plan is None:
+        plan = make_plan(B, N, block_table.shape[1], num_kv_splits=num_kv_splits)
+    if out is None:
+        out = torch.empty((B, N, KV_LORA_RANK), dtype=torch.bfloat16, device=q.device)
+    _check_tensor(out, "out", torch.bfloat16, (B, N, KV_LORA_RANK))
+    if lse is None and return_lse:
+        lse = torch.empty((B, N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32, (B, N))
+    if workspace is None:
+        workspace = new_workspace(plan, q.device, stream)
+    rc = load_library().mla_decode_fp8(
+        ctypes.byref(plan), _ptr(q), _ptr(latent_cache_fp8), int(latent_cache_fp8.shape[0]),
+        _ptr(block_table), _ptr(seq_lens), float(softmax_scale), float(k_scale), _ptr(out),
+        _ptr(lse), _ptr(workspace), int(workspace.numel()), _stream_ptr(stream))
+    _check(rc, "mla_decode_fp8")
     return out, lse
 
 

@@ -50,6 +50,7 @@ DecodeParams make_decode_params(const mla_decode_plan_t* plan, const void* q,
     // same in fp32 (every scaled score rounds 2^x to 1) and keeps the
     // tensor-core kernel's scaled masking sentinel at -inf.
     if (p.scale_log2 == 0.f) p.scale_log2 = FLT_MIN;
+    p.v_scale = 1.f;
     p.out = static_cast<uint16_t*>(out);
     p.lse = lse;
     p.status = status ? status : reinterpret_cast<int32_t*>(ws);
@@ -70,9 +71,11 @@ DecodeParams make_decode_params(const mla_decode_plan_t* plan, const void* q,
     return p;
 }
 
-int launch_decode_and_merge(const DecodeParams& p, const mla_decode_plan_t* plan, void* stream) {
-    int e = plan->kernel == MLA_KERNEL_TC ? launch_decode_tc(p, plan->grid_ctas, stream)
-                                          : launch_decode_simt(p, stream);
+int launch_decode_and_merge(const DecodeParams& p, const mla_decode_plan_t* plan, void* stream,
+                            bool fp8) {
+    int e = fp8 ? launch_decode_tc_fp8(p, plan->grid_ctas, stream)
+            : plan->kernel == MLA_KERNEL_TC ? launch_decode_tc(p, plan->grid_ctas, stream)
+                                            : launch_decode_simt(p, stream);
     if (e != 0) return MLA_ERR_CUDA;
     if (plan->sched_pairs > 0) {
         if (launch_merge_balanced(p, stream) != 0) return MLA_ERR_CUDA;
@@ -116,6 +119,35 @@ extern "C" int mla_decode(const mla_decode_plan_t* plan, const void* q, const vo
     return decode_impl(plan, q, latent_cache, num_blocks, block_table, seq_lens, softmax_scale,
                        out, lse, workspace, workspace_bytes, stream, 1,
                        plan ? plan->num_heads : 1, 0);
+}
+
+extern "C" int mla_decode_fp8(const mla_decode_plan_t* plan, const void* q,
+                              const void* latent_cache_fp8, int64_t num_blocks,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              float softmax_scale, float k_scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = validate_plan(plan);
+    if (rc != MLA_OK) return rc;
+    if (plan->kernel != MLA_KERNEL_TC) return MLA_ERR_UNSUPPORTED;
+    if (!q || !latent_cache_fp8 || !block_table || !seq_lens || !out) return MLA_ERR_INVALID_ARG;
+    if (num_blocks < 1 || !std::isfinite(softmax_scale) || !std::isfinite(k_scale) ||
+        !(k_scale > 0.f))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(latent_cache_fp8, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)))
+        return MLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < plan->workspace_bytes || !aligned(workspace, 256))
+        return MLA_ERR_WORKSPACE;
+    if (num_blocks > tc_max_blocks()) return MLA_ERR_UNSUPPORTED;
+    if (plan->batch == 0) return MLA_OK;
+    // The cache codes times k_scale are the entries: the scale multiplies
+    // every score (folded into the softmax scale) and every output row.
+    DecodeParams p = make_decode_params(plan, q, latent_cache_fp8, num_blocks, block_table,
+                                        seq_lens, softmax_scale * k_scale, out, lse,
+                                        static_cast<char*>(workspace), nullptr, 1,
+                                        plan->num_heads, 0);
+    p.v_scale = k_scale;
+    return launch_decode_and_merge(p, plan, stream, true);
 }
 
 extern "C" int mla_merge_splits(const float* o_part, const float* lse_part, int batch,

@@ -51,6 +51,9 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include <climits>
 #include <cmath>
 
@@ -61,6 +64,8 @@ namespace mla {
 namespace {
 
 constexpr int kThreads = 224;                  // 7 warps
+constexpr int kThreadsFp8 = 352;               // fp8 cache: + 4 warps that widen pages to f16
+constexpr int kFp8BlockBytes = 64 * 64;        // 64 rows x 64 E4M3 columns = 4 KB
 constexpr int kTile = 64;                      // tokens per page
 constexpr int kBlockBytes = kTile * 128;       // 64 rows x 64 bf16 columns = 8 KB
 constexpr int kKPerPage = 5;                   // K-ring blocks per page
@@ -111,6 +116,8 @@ struct TcBars {
     uint64_t q_read;      // staging area read into TMEM (128 arrivals)
     uint64_t final_qk;    // drain of the score warp's MMAs
     uint64_t final_sm[4]; // drain of each softmax warp's P.V MMAs
+    uint64_t kstaged[2];  // fp8 cache: TMA: the K-ring blocks' codes landed
+    uint64_t vstaged[2];  // fp8 cache: TMA: the value blocks' codes landed
     uint32_t p_count[2];  // softmax warps done with the pages of each parity
     uint32_t tmem_base;
     int32_t abort;
@@ -119,7 +126,7 @@ static_assert(sizeof(TcBars) <= 256, "barrier block too large");
 
 enum WaitSite : int32_t {
     kSiteVEmpty = 1, kSiteKEmpty, kSiteSFull, kSiteSFree, kSitePvDone, kSiteQReady,
-    kSiteDrain, kSiteKFull, kSiteVFull
+    kSiteDrain, kSiteKFull, kSiteVFull, kSiteStaged
 };
 
 __device__ __forceinline__ bool aborting(TcBars* bars) {
@@ -161,6 +168,29 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, TcBars
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The two 16-bit weights of a packed pair, as the MMA reads them.
+template <bool kF16>
+__device__ __forceinline__ float2 unpack_x2(uint32_t w) {
+    if constexpr (kF16) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    } else {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+}
+
+// Two bf16 q values (one 32-bit word) as two f16 (exact for |q| <= 65504;
+// `big` is set when a value lies beyond that).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& big) {
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+    big = big || !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+    return pack_f16x2(lo, hi);
 }
 
 // The 64-column block kb (dims 64kb..64kb+63) of a page is one of this CTA's
@@ -322,11 +352,12 @@ __device__ __forceinline__ uint64_t desc_vmn(uint32_t addr) {
 // desc). Called by one elected lane. With bar != 0 the
 // block also tests the mbarrier phase (bar, parity) without blocking, before
 // its first MMA, and reads the answer after its fourth (returned).
-template <int KB>
+template <int KB, bool kF16>
 __device__ __forceinline__ uint32_t score_block(uint32_t d, uint32_t tmem, const uint64_t* desc,
                                                 const uint64_t* bdesc, bool first,
                                                 uint32_t bar = 0, uint32_t parity = 0) {
-    constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(kTile, false);
+    constexpr uint32_t idesc_qk =
+        kF16 ? ptx::idesc_f16_f32(kTile, false) : ptx::idesc_bf16_f32(kTile, false);
     const uint32_t acc0 = first ? 0u : 1u;
     const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(bdesc);
     const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(bdesc + 2);
@@ -356,7 +387,7 @@ __device__ __forceinline__ uint32_t score_block(uint32_t d, uint32_t tmem, const
 // 0..255 (TMEM) and 512..575 (shared memory), its value blocks dims 256..511
 // (shared memory). Pages are numbered across segments (jg) for the rings;
 // each segment waits for its own q.
-template <int RANK>
+template <int RANK, bool kF16>
 __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t* b,
                                            const DecodeParams& p, const int32_t* pfx, int pair) {
     const uint32_t b_kfull = b[0], b_kempty = b[1], b_vfull = b[2], b_sfull = b[3],
@@ -426,19 +457,19 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
                 // late as possible (the P.V of page jc-1 finishes about now).
                 const int jn = jc + 1;
                 const uint32_t phn = uint32_t(jn >> 1) & 1u;
-                score_block<k_block(RANK, 0)>(d, tmem, desc, bk + 0, true);
-                const uint32_t nk = score_block<k_block(RANK, 1)>(
+                score_block<k_block(RANK, 0), kF16>(d, tmem, desc, bk + 0, true);
+                const uint32_t nk = score_block<k_block(RANK, 1), kF16>(
                     d, tmem, desc, bk + 4, false, b_kfull + 8 * (jn & 1), phn);
-                score_block<k_block(RANK, 2)>(d, tmem, desc, bk + 8, false);
-                const uint32_t vr = score_block<k_block(RANK, 3)>(
+                score_block<k_block(RANK, 2), kF16>(d, tmem, desc, bk + 8, false);
+                const uint32_t vr = score_block<k_block(RANK, 3), kF16>(
                     d, tmem, desc, bk + 12, false, b_vf, ph);
-                score_block<k_block(RANK, 4)>(d, tmem, desc, bk + 16, false);
+                score_block<k_block(RANK, 4), kF16>(d, tmem, desc, bk + 16, false);
                 ptx::mma_commit(b_kempty + 8 * sl);
                 if (!vr && !wait_phase(b_vf, ph, a.bars, a.status, kSiteVFull, a.limit_ns)) break;
-                score_block<4 * RANK + 0>(d, tmem, desc, bv + 0, false);
-                score_block<4 * RANK + 1>(d, tmem, desc, bv + 4, false);
-                score_block<4 * RANK + 2>(d, tmem, desc, bv + 8, false);
-                const uint32_t nf = score_block<4 * RANK + 3>(
+                score_block<4 * RANK + 0, kF16>(d, tmem, desc, bv + 0, false);
+                score_block<4 * RANK + 1, kF16>(d, tmem, desc, bv + 4, false);
+                score_block<4 * RANK + 2, kF16>(d, tmem, desc, bv + 8, false);
+                const uint32_t nf = score_block<4 * RANK + 3, kF16>(
                     d, tmem, desc, bv + 12, false, b_pfree + 8 * (jn & 1), phn ^ 1u);
                 ptx::mma_commit(b_sfull + 8 * sl);
                 const bool more = j + 1 < ntiles;
@@ -456,9 +487,11 @@ __device__ __forceinline__ void score_warp(const MmaWarpArgs& a, const uint32_t*
 // O += P V for page np: P the A operand in TMEM, V (MN-major) from the V
 // ring. Issued by one elected lane of the softmax warp that finished the page
 // last; the commits release the V slot and the score buffer.
+template <bool kF16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int np, bool accumulate,
                                          uint32_t b_vempty, uint32_t b_pfree) {
-    constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(256, true);
+    constexpr uint32_t idesc_pv =
+        kF16 ? ptx::idesc_f16_f32(256, true) : ptx::idesc_bf16_f32(256, true);
     const int sl = np & 1;
     const uint32_t pcol = tmem + kTmemS + uint32_t(sl * 64);
     const uint32_t vb = sbase + uint32_t(kOffV + sl * kVBytes);
@@ -498,17 +531,23 @@ __device__ void dump_slot(const DecodeParams& p, const unsigned char* slot, bool
 // the tensor map over the cache viewed as [num_blocks * 64, 576], at row
 // y = block * 64 (block = block_table[b, page]). With kDump the loader runs
 // alone (no consumers free the slots): it waits for each page to land and
-// copies it out with dump_slot.
-template <bool kDump>
+// copies it out with dump_slot. With kFp8 the tensor map is over the E4M3
+// codes (64 x 64 one-byte boxes, unswizzled) and the boxes land in the upper
+// half of the slot, which the converter warps widen in place to f16
+// (b_full is then the barrier the converters wait on).
+template <bool kDump, bool kFp8>
 __device__ __forceinline__ void page_loader(const DecodeParams& p, const CUtensorMap* tmap,
                                             const int32_t* pfx, int pair, uint32_t rank,
                                             bool k_ring, TcBars* bars, unsigned char* smem,
                                             uint32_t sbase, uint32_t b_full, uint32_t b_empty,
                                             uint64_t limit_ns) {
     const int N = p.num_heads;
-    const int bytes = k_ring ? kKBytes : kVBytes;
+    const int slot_bytes = k_ring ? kKBytes : kVBytes;
+    // bytes that land per page: the slot (bf16), or its upper half (E4M3)
+    const int bytes = kFp8 ? slot_bytes / 2 : slot_bytes;
+    const int box_bytes = kFp8 ? kFp8BlockBytes : kBlockBytes;
     const int off0 = k_ring ? kOffK : kOffV;
-    const uint32_t dst0 = sbase + uint32_t(off0);
+    const uint32_t dst0 = sbase + uint32_t(off0 + (kFp8 ? slot_bytes / 2 : 0));
     // Test hook: CTA 0 withholds its first K-ring load, so the score warp's
     // wait for it runs out.
     const bool withhold =
@@ -559,16 +598,16 @@ __device__ __forceinline__ void page_loader(const DecodeParams& p, const CUtenso
             }
             if (withhold && jg == 0) continue;
             ptx::mbar_arrive_expect_tx(b_full + 8 * sl, uint32_t(bytes));
-            const uint32_t dst = dst0 + uint32_t(sl * bytes);
+            const uint32_t dst = dst0 + uint32_t(sl * slot_bytes);
             if (k_ring) {
                 // The five K-ring blocks, in score order.
                 for (int pos = 0; pos < kKPerPage; ++pos)
-                    ptx::tma_load_2d(dst + uint32_t(pos * kBlockBytes), tmap,
+                    ptx::tma_load_2d(dst + uint32_t(pos * box_bytes), tmap,
                                      64 * k_block(int(rank), pos), y, b_full + 8 * sl);
             } else {
                 // This CTA's four value blocks.
                 for (int k = 0; k < 4; ++k)
-                    ptx::tma_load_2d(dst + uint32_t(k * kBlockBytes), tmap,
+                    ptx::tma_load_2d(dst + uint32_t(k * box_bytes), tmap,
                                      256 * int(rank) + 64 * k, y, b_full + 8 * sl);
             }
             if constexpr (kDump) {
@@ -579,7 +618,7 @@ __device__ __forceinline__ void page_loader(const DecodeParams& p, const CUtenso
                     break;
                 }
                 const int t0 = sg.t_lo + j * kTile;
-                dump_slot(p, smem + off0 + sl * bytes, k_ring, rank, sg.b, t0,
+                dump_slot(p, smem + off0 + sl * slot_bytes, k_ring, rank, sg.b, t0,
                           min(kTile, sg.t_hi - t0));
             }
         }
@@ -592,8 +631,82 @@ __device__ __forceinline__ void page_loader(const DecodeParams& p, const CUtenso
     }
 }
 
-template <bool kDump>
-__global__ void __launch_bounds__(kThreads, 1)
+// fp8 cache: widen a page's E4M3 codes to f16 in place. The loader put the
+// ring's blocks of codes (64 rows x 64 bytes each, unswizzled) in the upper
+// half of the slot; block k's f16 copy goes to the k-th 8 KB of the slot in
+// the 128-byte swizzled layout the MMAs read. Block k's f16 bytes overlap
+// only the codes of blocks <= k, so the 64 converter threads of the ring
+// read a whole block, meet at a named barrier, then write it. The
+// conversion is exact (every E4M3 value is an f16 value). Each thread then
+// makes its writes visible to the tensor cores and arrives on b_full (64
+// arrivals per page).
+template <bool kKRing>
+__device__ __forceinline__ void page_converter(const DecodeParams& p, const int32_t* pfx,
+                                               int pair, TcBars* bars, unsigned char* smem,
+                                               uint32_t b_staged, uint32_t b_full, int ct,
+                                               uint64_t limit_ns) {
+    constexpr int nblk = kKRing ? kKPerPage : 4;
+    constexpr int slot_bytes = kKRing ? kKBytes : kVBytes;
+    constexpr uint32_t bar_id = kKRing ? 1u : 2u;
+    unsigned char* ring = smem + (kKRing ? kOffK : kOffV);
+    SegmentWalk walk = walk_begin(p, pfx, pair);
+    Segment sg;
+    int jg = 0;
+    bool ok = true;
+    while (ok && walk_next(p, pfx, pair, walk, sg)) {
+        const int ntiles = seg_pages(sg);
+        for (int j = 0; j < ntiles; ++j, ++jg) {
+            const int sl = jg & 1;
+            const bool landed = wait_phase(b_staged + 8 * sl, uint32_t(jg >> 1) & 1u, bars,
+                                           p.status, kSiteStaged, limit_ns);
+            // One decision for all 64 threads: the named barriers below need
+            // every one of them.
+            if (ptx::named_barrier_or(bar_id, 64, !landed || aborting(bars))) {
+                ok = false;
+                break;
+            }
+            unsigned char* slot = ring + sl * slot_bytes;
+            const unsigned char* codes = slot + slot_bytes / 2;
+#pragma unroll 1
+            for (int blk = 0; blk < nblk; ++blk) {
+                uint4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = ct + 64 * k;          // 256 chunks of 16 codes
+                    v[k] = *reinterpret_cast<const uint4*>(codes + blk * kFp8BlockBytes +
+                                                           (i >> 2) * 64 + (i & 3) * 16);
+                }
+                ptx::named_barrier_sync(bar_id, 64);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = ct + 64 * k;
+                    const int r = i >> 2, cc = i & 3;
+                    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                            __nv_fp8x2_storage_t(w[e] & 0xffffu), __NV_E4M3);
+                        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                            __nv_fp8x2_storage_t(w[e] >> 16), __NV_E4M3);
+                        h[2 * e] = uint32_t(lo.x) | (uint32_t(lo.y) << 16);
+                        h[2 * e + 1] = uint32_t(hi.x) | (uint32_t(hi.y) << 16);
+                    }
+                    unsigned char* row = slot + blk * kBlockBytes + r * 128;
+                    *reinterpret_cast<uint4*>(row + (((2 * cc) ^ (r & 7)) * 16)) =
+                        make_uint4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<uint4*>(row + (((2 * cc + 1) ^ (r & 7)) * 16)) =
+                        make_uint4(h[4], h[5], h[6], h[7]);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(b_full + 8 * sl);
+        }
+    }
+}
+
+template <bool kDump, bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
 mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap) {
     extern __shared__ __align__(1024) unsigned char smem[];
     TcBars* bars = reinterpret_cast<TcBars*>(smem + kOffBar);
@@ -625,16 +738,23 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
     const uint32_t b_qread = ptx::smem_addr(&bars->q_read);
     const uint32_t b_final_qk = ptx::smem_addr(&bars->final_qk);
     const uint32_t b_final_sm = ptx::smem_addr(&bars->final_sm[0]);
+    const uint32_t b_kstaged = ptx::smem_addr(&bars->kstaged[0]);
+    const uint32_t b_vstaged = ptx::smem_addr(&bars->vstaged[0]);
     const uint32_t a_pcount = ptx::smem_addr(&bars->p_count[0]);
 
     if (warp == 0) {
         if (lane == 0) {
             if (!aligned_ok) record_error(p.status, MLA_ERR_UNSUPPORTED, int32_t(sbase));
+            // A slot is full after the TMA landed (bf16), or after the 64
+            // converter threads of its ring widened it (fp8).
+            const uint32_t full_count = kFp8 ? 64u : 1u;
             for (int i = 0; i < 2; ++i) {
-                ptx::mbar_init(b_vfull + 8 * i, 1);
+                ptx::mbar_init(b_vfull + 8 * i, full_count);
                 ptx::mbar_init(b_vempty + 8 * i, 1);
-                ptx::mbar_init(b_kfull + 8 * i, 1);
+                ptx::mbar_init(b_kfull + 8 * i, full_count);
                 ptx::mbar_init(b_kempty + 8 * i, 1);
+                ptx::mbar_init(b_kstaged + 8 * i, 1);
+                ptx::mbar_init(b_vstaged + 8 * i, 1);
                 ptx::mbar_init(b_sfull + 8 * i, 1);
                 ptx::mbar_init(b_pfree + 8 * i, 1);
                 bars->p_count[i] = 0;
@@ -690,19 +810,28 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
         // nothing runs; the error is recorded
     } else if (warp == 0 || warp == 6) {
         // ------------------------------------------------------ TMA producers
+        const uint32_t b_land = kFp8 ? (warp == 0 ? b_kstaged : b_vstaged)
+                                     : (warp == 0 ? b_kfull : b_vfull);
         if (lane == 0)
-            page_loader<kDump>(p, &tmap, pfx, pair, rank, warp == 0, bars, smem, sbase,
-                               warp == 0 ? b_kfull : b_vfull, warp == 0 ? b_kempty : b_vempty,
-                               2 * p.timeout_ns);
+            page_loader<kDump, kFp8>(p, &tmap, pfx, pair, rank, warp == 0, bars, smem, sbase,
+                                     b_land, warp == 0 ? b_kempty : b_vempty, lim_dep);
     } else if (kDump) {
         // loader dump: only the loaders run
+    } else if (kFp8 && warp >= 7) {
+        // fp8 cache: warps 7-8 widen the K-ring blocks, 9-10 the value blocks
+        if (warp < 9)
+            page_converter<true>(p, pfx, pair, bars, smem, b_kstaged, b_kfull,
+                                 (warp - 7) * 32 + lane, lim_dep);
+        else
+            page_converter<false>(p, pfx, pair, bars, smem, b_vstaged, b_vfull,
+                                  (warp - 9) * 32 + lane, lim_dep);
     } else if (warp == 1) {
         // ------------------------------------------------------ score MMAs
         const uint32_t bq[7] = {b_kfull, b_kempty, b_vfull, b_sfull, b_pfree, b_qready, b_final_qk};
         if (rank == 0)
-            score_warp<0>(margs, bq, p, pfx, pair);
+            score_warp<0, kFp8>(margs, bq, p, pfx, pair);
         else
-            score_warp<1>(margs, bq, p, pfx, pair);
+            score_warp<1, kFp8>(margs, bq, p, pfx, pair);
     } else {
         // ------------------------------- softmax / P.V issue / correction / epilogue
         const int quarter = warp & 3;
@@ -720,6 +849,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
         // of padded heads are zero-filled. Called once every score MMA that
         // read the previous q has completed. Returns false if a wait expired.
         int nstage = 0;
+        bool q_big = false;   // fp8 cache: a q entry beyond the f16 range was seen
         auto stage_q = [&](int qb) -> bool {
             const uint16_t* qbase = p.q + size_t(qb) * N * kD;
             const uint32_t ph = uint32_t(nstage++) & 1u;
@@ -748,6 +878,11 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                     r32[4 * i + 2] = v.z;
                     r32[4 * i + 3] = v.w;
                 }
+                if constexpr (kFp8) {
+                    // f16 operands: q widened exactly (bf16 -> f16)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r32[i] = bf16x2_to_f16x2(r32[i], q_big);
+                }
                 ptx::tmem_st32(trow + kTmemQ + uint32_t(blk * 32), r32);
             }
             ptx::mbar_arrive(b_qread);
@@ -763,6 +898,21 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                     qbase + (live ? size_t(r) * kD + 256 + 8 * c : 0), live ? 16u : 0u);
             }
             ptx::cp_async_wait_all();
+            if constexpr (kFp8) {
+                // Each thread widens the chunks it copied, in place.
+#pragma unroll 4
+                for (int k = 0; k < 40; ++k) {
+                    const int i = t + 128 * k;
+                    const int r = i / 40, c = i - 40 * (i / 40);
+                    const int kb = c >> 3, cc = c & 7;
+                    uint4* a = reinterpret_cast<uint4*>(smem + kOffQS + kb * 16384 + r * 128 +
+                                                        ((cc ^ (r & 7)) * 16));
+                    const uint4 v = *a;
+                    *a = make_uint4(bf16x2_to_f16x2(v.x, q_big), bf16x2_to_f16x2(v.y, q_big),
+                                    bf16x2_to_f16x2(v.z, q_big), bf16x2_to_f16x2(v.w, q_big));
+                }
+                if (q_big) record_error(p.status, MLA_ERR_RANGE, qb);
+            }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ptx::mbar_arrive(b_qready);
@@ -864,11 +1014,9 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                         const float2 d = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), sc2, negm2);
                         const float a = ptx::ex2(d.x);
                         const float c = ptx::ex2(d.y);
-                        pk[i] = pack_bf16x2(a, c);
+                        pk[i] = kFp8 ? pack_f16x2(a, c) : pack_bf16x2(a, c);
                         ls2[i & 1] = __fadd2_rn(ls2[i & 1], make_float2(a, c));
-                        lb2[i & 1] = __fadd2_rn(
-                            lb2[i & 1], make_float2(__uint_as_float(pk[i] << 16),
-                                                    __uint_as_float(pk[i] & 0xffff0000u)));
+                        lb2[i & 1] = __fadd2_rn(lb2[i & 1], unpack_x2<kFp8>(pk[i]));
                     }
                     ptx::tmem_st32(sbuf, pk);
                 }
@@ -916,7 +1064,8 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 done_before = __shfl_sync(0xffffffffu, done_before, 0);
                 if (done_before == 4u * uint32_t(jg >> 1) + 3u) {
                     ptx::tc_fence_after();
-                    if (ptx::elect_one()) issue_pv(tmem, sbase, jg, j > 0, b_vempty, b_pfree);
+                    if (ptx::elect_one())
+                        issue_pv<kFp8>(tmem, sbase, jg, j > 0, b_vempty, b_pfree);
                     __syncwarp();
                     issued_pv = true;
                 }
@@ -944,7 +1093,8 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 if (!ok) break;
                 ptx::tc_fence_after();
             }
-            const float inv = l_bf > 0.f ? 1.f / l_bf : 0.f;
+            float inv = l_bf > 0.f ? 1.f / l_bf : 0.f;
+            if constexpr (kFp8) inv *= p.v_scale;   // the cache codes' per-tensor scale
             const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
             const size_t row = size_t(sg.b) * N + h;
             const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0u;
@@ -1046,26 +1196,30 @@ int tc_max_blocks() { return INT_MAX / kTile - 1; }
 
 namespace {
 
-template <bool kDump>
+template <bool kDump, bool kFp8>
 int launch_tc(const DecodeParams& p, int grid_ctas, void* stream) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encoder();
     if (encode == nullptr) return int(cudaErrorNotSupported);
+    // The cache viewed as [num_blocks * 64, 576]: bf16 with 128-byte swizzled
+    // 64 x 64 boxes, or E4M3 codes with unswizzled 64 x 64 one-byte boxes.
     CUtensorMap tmap;
     const cuuint64_t dims[2] = {cuuint64_t(kD), cuuint64_t(p.num_blocks) * kTile};
-    const cuuint64_t strides[1] = {cuuint64_t(kD) * 2};
+    const cuuint64_t strides[1] = {cuuint64_t(kD) * (kFp8 ? 1 : 2)};
     const cuuint32_t box[2] = {64, kTile};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    CUresult r = encode(&tmap,
+                        kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                         const_cast<uint16_t*>(p.cache), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        kFp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return int(cudaErrorInvalidValue);
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel<kDump>,
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel<kDump, kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return int(e);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid_ctas), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kFp8 ? kThreadsFp8 : kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -1075,18 +1229,22 @@ int launch_tc(const DecodeParams& p, int grid_ctas, void* stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<kDump>, p, tmap);
+    e = cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<kDump, kFp8>, p, tmap);
     return int(e);
 }
 
 }  // namespace
 
 int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream) {
-    return launch_tc<false>(p, grid_ctas, stream);
+    return launch_tc<false, false>(p, grid_ctas, stream);
 }
 
 int launch_decode_tc_loader_dump(const DecodeParams& p, int grid_ctas, void* stream) {
-    return launch_tc<true>(p, grid_ctas, stream);
+    return launch_tc<true, false>(p, grid_ctas, stream);
+}
+
+int launch_decode_tc_fp8(const DecodeParams& p, int grid_ctas, void* stream) {
+    return launch_tc<false, true>(p, grid_ctas, stream);
 }
 
 }  // namespace mla

@@ -59,7 +59,8 @@ struct DecodeParams {
     int32_t num_heads;
     int32_t num_splits;           // S of the split schedule (1 when sched_pairs > 0)
     int32_t sched_pairs;          // > 0: page-balanced schedule over this many CTA pairs
-    float scale_log2;             // softmax_scale * log2(e)
+    float scale_log2;             // softmax_scale * log2(e) (* k_scale for an fp8 cache)
+    float v_scale;                // multiplies the output: 1, or k_scale for an fp8 cache
     uint16_t* out;                // bf16 [B, N, 512]
     float* lse;                   // fp32 [B, N] or null
     float* o_part;                // fp32 partial rows: [B, N, S, 512] (split, S > 1)
@@ -89,6 +90,8 @@ int launch_decode_tc(const DecodeParams& p, int grid_ctas, void* stream);
 // The tensor-core kernel's page loaders alone (no MMAs): every page each CTA
 // receives is copied from its shared-memory rings to p.dump.
 int launch_decode_tc_loader_dump(const DecodeParams& p, int grid_ctas, void* stream);
+// The tensor-core kernel over an fp8 (E4M3) cache: p.cache holds the codes.
+int launch_decode_tc_fp8(const DecodeParams& p, int grid_ctas, void* stream);
 int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,
                  int v_dim, uint16_t* out, float* lse, void* stream);
 // Combine of per-rank results in rank-major layout: bf16 [world, rows, v_dim]
@@ -107,8 +110,10 @@ DecodeParams make_decode_params(const mla_decode_plan_t* plan, const void* q,
                                 const int32_t* block_table, const int32_t* seq_lens,
                                 float softmax_scale, void* out, float* lse, char* ws,
                                 int32_t* status, int q_len, int heads_per_token, int causal);
-// The decode kernel of `plan`, then its merge (S > 1 or page-balanced).
-int launch_decode_and_merge(const DecodeParams& p, const mla_decode_plan_t* plan, void* stream);
+// The decode kernel of `plan` (the fp8-cache kernel with `fp8`), then its
+// merge (S > 1 or page-balanced).
+int launch_decode_and_merge(const DecodeParams& p, const mla_decode_plan_t* plan, void* stream,
+                            bool fp8 = false);
 
 // mla_decode with multi-token rows (q_len query tokens' heads as the rows;
 // q_len = 1 is the plain decode).

@@ -292,6 +292,7 @@ extern "C" const char* mla_status_string(int status) {
         case MLA_ERR_TIMEOUT: return "bounded device wait expired";
         case MLA_ERR_SCRATCH_LIMIT:
             return "plan needs more scratch than the 32 MiB of mla_decode_noalloc";
+        case MLA_ERR_RANGE: return "q entry beyond the f16 range of the fp8-cache decode";
         default: return "unknown status";
     }
 }

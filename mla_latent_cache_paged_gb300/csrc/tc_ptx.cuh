@@ -336,5 +336,29 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int n, bool b_mn_major) {
            (uint32_t(n >> 3) << 17) | (uint32_t(128 >> 4) << 24);
 }
 
+// The same with f16 A and B (format field 0 for both operands).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int n, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | (uint32_t(n >> 3) << 17) |
+           (uint32_t(128 >> 4) << 24);
+}
+
+// Named barrier over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// The same barrier, returning the OR of `v` over the `count` threads (one
+// answer for all of them).
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %3, 0;\n"
+        " bar.red.or.pred q, %1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(id), "r"(count), "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
 }  // namespace ptx
 }  // namespace mla

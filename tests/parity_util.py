@@ -150,3 +150,72 @@ def oracle_rows(w, requests):
         table[i, :n] = [remap[int(x)] for x in w.block_table[b, :n]]
     q = bf16_bits_to_f64(w.q_bits[np.array(requests, dtype=np.int64)])
     return mla_decode_reference(q, pool, table, w.seq_lens[requests], w.softmax_scale)
+
+
+def run_decode_fp8(w, num_kv_splits=None, device="cuda", schedule="auto", num_sms=None):
+    """The fp8-cache CUDA path on an fp8 workload; returns (out_f64, lse, plan, tensors)."""
+    import torch
+    q, cache, table, lens = to_torch(w, device)
+    splits = w.num_kv_splits if num_kv_splits is None else num_kv_splits
+    plan = binding.make_plan(w.batch, w.num_heads, w.max_blocks_per_seq, schedule=schedule,
+                             num_sms=num_sms, seq_lens_host=w.seq_lens,
+                             max_seq_len=max(w.max_seq_len, 0), num_kv_splits=splits)
+    ws = binding.new_workspace(plan, device)
+    out, lse = binding.mla_decode_fp8(q, cache, table, lens, w.softmax_scale, w.k_scale,
+                                      plan=plan, workspace=ws)
+    torch.cuda.synchronize()
+    status = binding.read_error(ws)
+    assert status == 0, f"device status {status}: {binding.status_string(status)}"
+    got = bf16_bits_to_f64(bf16_tensor_bits(out))
+    return got, lse.double().cpu().numpy(), plan, dict(q=q, cache=cache, table=table,
+                                                       lens=lens, ws=ws, out=out, lse=lse)
+
+
+def oracle_rows_fp8(w, requests, max_tokens=1 << 18):
+    """Oracle out/lse of an fp8 workload for the listed requests, in groups of
+    at most `max_tokens` cached tokens: the blocks they reference, renumbered
+    into a compact pool (pure re-indexing), handed as E4M3 codes with the
+    workload's k_scale to ``oracle.mla_decode_reference_fp8``."""
+    from oracle import mla_decode_reference_fp8
+    requests = list(requests)
+    ps = w.page_size
+    outs, lses = [], []
+    group, tokens = [], 0
+    for b in requests + [None]:
+        L = 0 if b is None else int(w.seq_lens[b])
+        if group and (b is None or tokens + L > max_tokens):
+            used = []
+            for g in group:
+                used.extend(int(x) for x in w.block_table[g, :-(-int(w.seq_lens[g]) // ps)])
+            ids = sorted(set(used))
+            remap = {old: new for new, old in enumerate(ids)}
+            pool = w.cache_bits[np.array(ids, dtype=np.int64)] if ids else \
+                np.zeros((1, ps, w.cache_bits.shape[2]), dtype=np.uint8)
+            table = np.full((len(group), w.block_table.shape[1]), -1, dtype=np.int64)
+            for i, g in enumerate(group):
+                n = -(-int(w.seq_lens[g]) // ps)
+                table[i, :n] = [remap[int(x)] for x in w.block_table[g, :n]]
+            q = bf16_bits_to_f64(w.q_bits[np.array(group, dtype=np.int64)])
+            o, l = mla_decode_reference_fp8(q, pool, table, w.seq_lens[group], w.softmax_scale,
+                                            w.k_scale)
+            outs.append(o)
+            lses.append(l)
+            group, tokens = [], 0
+        if b is not None:
+            group.append(b)
+            tokens += L
+    return np.concatenate(outs), np.concatenate(lses)
+
+
+def value_abs_max_fp8(w, requests):
+    """max_t |V[t, d]| of the dequantized rows per listed request: [len, 1, 512]."""
+    from oracle import dequantize_e4m3_cache
+    out = np.zeros((len(requests), 1, 512))
+    for i, b in enumerate(requests):
+        L = int(w.seq_lens[b])
+        if L == 0:
+            continue
+        t = np.arange(L)
+        rows = w.cache_bits[w.block_table[b, t // w.page_size], t % w.page_size, :512]
+        out[i, 0] = np.abs(dequantize_e4m3_cache(rows, w.k_scale)).max(axis=0)
+    return out
