@@ -53,6 +53,8 @@ def parse_args():
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--dcp-world", type=int, default=2,
                     help="ranks whose results --stage dcp_combine merges")
+    ap.add_argument("--splits", type=int, default=32,
+                    help="split partials per row for --stage merge_v_up_proj")
     ap.add_argument("--q-len", type=int, default=2,
                     help="query tokens per request for --stage multi_token")
     ap.add_argument("--stage", choices=["decode"] + sorted(STAGES), default="decode",
@@ -314,6 +316,8 @@ STAGES = {
                    "one launch",
     "multi_token": "MLA uniform multi-token decode (causal query block of --q-len tokens per "
                    "request)",
+    "merge_v_up_proj": "MLA split merge fused with the up-projection by W_UV (--splits partials "
+                       "per row), one launch; the separate merge + up-projection timed beside it",
 }
 
 
@@ -325,6 +329,13 @@ def stage_work(stage, batch, heads, world=2):
     (2 * B * 576) + slot ids (8 B each). Up-projection: x (B*N*512) + W_UV
     (N*512*128) + out (B*N*128). Both: 2 * B * N * 128 * 512 flops.
     """
+    if stage == "merge_v_up_proj":
+        # fp32 partials and their LSEs read, W_UV read, out (bf16 [B, N, 128])
+        # and the merged LSE written; the separate path also writes and reads
+        # the bf16 latent rows [B, N, 512].
+        nbytes = (batch * heads * world * (2048 + 4) + 2 * heads * 512 * 128 +
+                  2 * batch * heads * 128 + 4 * batch * heads)
+        return nbytes, 2 * batch * heads * 128 * 512
     if stage == "front_end":
         nbytes = 2 * (heads * 128 * 512 + batch * heads * 192 + batch * heads * 576 +
                       2 * batch * 576) + 8 * batch
@@ -429,7 +440,8 @@ def run_stage(args, stage):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    nbytes, flops = stage_work(stage, B, N, args.dcp_world)
+    nbytes, flops = stage_work(stage, B, N,
+                               args.splits if stage == "merge_v_up_proj" else args.dcp_world)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     nsets = max(2, -(-2 * l2 // nbytes) + 1)
     gen = torch.Generator(device=dev).manual_seed(20260100)
@@ -439,7 +451,27 @@ def run_stage(args, stage):
 
     ws = binding.new_status_workspace(dev)
     sets = []
-    if stage == "dcp_combine":
+    call_sep = None
+    if stage == "merge_v_up_proj":
+        S = args.splits
+        for i in range(nsets):
+            lse_parts = torch.randn((B, N, S), generator=gen, device=dev) * 3
+            sets.append(dict(o=torch.randn((B, N, S, 512), generator=gen, device=dev),
+                             lse=lse_parts, w=rnd((N, 512, 128), 512 ** -0.5),
+                             out=torch.empty((B, N, 128), dtype=torch.bfloat16, device=dev),
+                             lse_out=torch.empty((B, N), dtype=torch.float32, device=dev),
+                             lat=torch.empty((B, N, 512), dtype=torch.bfloat16, device=dev)))
+
+        def call(i):
+            t = sets[i % nsets]
+            binding.mla_merge_splits_v_up_proj(t["o"], t["lse"], t["w"], workspace=ws,
+                                               out=t["out"], lse=t["lse_out"])
+
+        def call_sep(i):
+            t = sets[i % nsets]
+            binding.mla_merge_splits(t["o"], t["lse"], out=t["lat"], lse=t["lse_out"])
+            binding.mla_v_up_proj(t["lat"], t["w"], workspace=ws, out=t["out"])
+    elif stage == "dcp_combine":
         R = args.dcp_world
         for i in range(nsets):
             lse_parts = torch.randn((R, B, N), generator=gen, device=dev) * 3
@@ -494,9 +526,26 @@ def run_stage(args, stage):
     if binding.read_error(ws) != 0:
         raise RuntimeError("device status after timing")
     ms = e0.elapsed_time(e1) / steps
+    extra = {}
+    if call_sep is not None:
+        for i in range(3):
+            call_sep(i)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(steps):
+            call_sep(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if binding.read_error(ws) != 0:
+            raise RuntimeError("device status after the separate calls")
+        ms_sep = e0.elapsed_time(e1) / steps
+        extra = {"splits": args.splits, "separate_ms_per_step": ms_sep,
+                 "separate_launches_per_step": 2, "fused_speedup": ms_sep / ms,
+                 "separate_extra_bytes": 2 * B * N * 512 * 2}
     peaks, peak_kind = load_peaks()
     achieved = nbytes / (ms / 1e3) / 1e9
     return {
+        **extra,
         "metric": STAGES[stage] + ": algorithmic bytes / time", "value": achieved,
         "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": max(args.warmup, 3),
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -436,6 +436,49 @@ int mla_v_up_proj(const void* x, const void* w_uv, int batch, int num_heads, voi
                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mla_merge_splits_v_up_proj -- the split merge and the up-projection in one
+ * launch: for every (b, n) the S partials are merged as mla_merge_splits does,
+ * the merged row is rounded to bf16 (the precision of mla_decode's output)
+ * and multiplied by W_UV[n] on the tensor cores without leaving the SM:
+ *     x[b, n, :]   = bf16(sum_s exp(lse_part[b,n,s] - lse) * o_part[b,n,s,:])
+ *     out[b, n, :] = sum_l x[b, n, l] * w_uv[n, l, 0:128]
+ * (vLLM mla_attention API docs: the split partials' merge_attn_states, then
+ * _v_up_proj; the weight layout is the raon-1-mini page's W_UV as (N, Lkv, V)).
+ * The [B, N, 512] merged rows never go through HBM unless latent_out is given.
+ *
+ *   o_part, lse_part  device, fp32 [B, N, S, 512] and [B, N, S].
+ *   num_splits        1 <= S <= 512 (more: MLA_ERR_UNSUPPORTED).
+ *   w_uv              device, bf16 [N, 512, 128].
+ *   out               device, bf16 [B, N, 128].
+ *   lse, latent_out   device, fp32 [B, N] and bf16 [B, N, 512], each optional.
+ *   workspace         a status header (>= 8192 bytes, 256-byte aligned).
+ * One kernel launch on `stream`; every pointer 16-byte aligned (lse_part and
+ * lse 4-byte).
+ */
+int mla_merge_splits_v_up_proj(const float* o_part, const float* lse_part, int batch,
+                               int num_heads, int num_splits, const void* w_uv, void* out,
+                               float* lse, void* latent_out, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode_v_up_proj -- the decode followed by the up-projection: out[b, n, :]
+ * = mla_decode's out[b, n, :] (bf16) times w_uv[n] (bf16 [N, 512, 128]),
+ * i.e. forward_mqa then _v_up_proj of the vLLM mla_attention API docs. With a
+ * split plan (S > 1, at most 512) the decode kernel's fp32 partials go
+ * straight into mla_merge_splits_v_up_proj, and the latent rows are written
+ * only if latent_out is given. Otherwise (S = 1 or the page-balanced
+ * schedule) the decode writes latent_out (then required) and mla_v_up_proj
+ * reads it back. Arguments as mla_decode, plus w_uv and out (bf16
+ * [B, N, 128]); lse optional. Two launches (three with a page-balanced
+ * merge), no synchronisation.
+ */
+int mla_decode_v_up_proj(const mla_decode_plan_t* plan, const void* q, const void* latent_cache,
+                         int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                         float softmax_scale, const void* w_uv, void* out, float* lse,
+                         void* latent_out, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
  * mla_read_error -- synchronise `stream`, then read and clear the device
  * status word of `workspace`. *device_status receives MLA_OK or the first
  * MLA_ERR_* a kernel recorded since the last read. Returns MLA_ERR_CUDA if

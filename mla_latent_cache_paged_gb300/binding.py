@@ -43,7 +43,7 @@ EXPORTED_SYMBOLS = (
     "mla_decode_noalloc", "mla_dcp_local_seq_lens", "mla_dcp_combine",
     "mla_q_absorb_concat_cache", "mla_v_up_proj", "mla_multi_token_scratch_bytes",
     "mla_decode_multi_token", "mla_debug_loader_pages", "mla_multi_token_row_lens",
-    "mla_decode_fp8",
+    "mla_decode_fp8", "mla_merge_splits_v_up_proj", "mla_decode_v_up_proj",
 )
 
 
@@ -100,6 +100,10 @@ def load_library(path=None):
     lib.mla_decode_fp8.argtypes = [ctypes.POINTER(MlaDecodePlan), vp, vp, i64, vp, vp, f32, f32,
                                    vp, vp, vp, sz, vp]
     lib.mla_merge_splits.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
+    lib.mla_merge_splits_v_up_proj.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz,
+                                               vp]
+    lib.mla_decode_v_up_proj.argtypes = [ctypes.POINTER(MlaDecodePlan), vp, vp, i64, vp, vp, f32,
+                                         vp, vp, vp, vp, vp, sz, vp]
     lib.mla_read_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
     lib.mla_status_string.argtypes = [i32]
     lib.mla_status_string.restype = ctypes.c_char_p
@@ -373,6 +377,46 @@ def mla_merge_splits(o_part, lse_part, *, out=None, lse=None, return_lse=True, s
                                          _ptr(lse), _stream_ptr(stream))
     _check(rc, "mla_merge_splits")
     return out, lse
+
+
+def mla_merge_splits_v_up_proj(o_part, lse_part, w_uv, *, workspace, out=None, lse=None,
+                               latent_out=None, stream=None):
+    """Split merge and up-projection in one launch: fp32 ``[B,N,S,512]`` /
+    ``[B,N,S]`` partials and ``W_UV [N,512,128]`` -> bf16 ``out [B,N,128]``
+    (``lse`` and the merged ``latent_out`` rows only if given)."""
+    import torch
+    B, N, S, V = o_part.shape
+    _check_tensor(o_part, "o_part", torch.float32)
+    _check_tensor(lse_part, "lse_part", torch.float32, (B, N, S))
+    _check_tensor(w_uv, "w_uv", torch.bfloat16, (N, 512, 128))
+    if V != KV_LORA_RANK:
+        raise ValueError("partials must be 512 wide")
+    if out is None:
+        out = torch.empty((B, N, 128), dtype=torch.bfloat16, device=o_part.device)
+    _check_tensor(out, "out", torch.bfloat16, (B, N, 128))
+    rc = load_library().mla_merge_splits_v_up_proj(
+        _ptr(o_part), _ptr(lse_part), B, N, S, _ptr(w_uv), _ptr(out), _ptr(lse),
+        _ptr(latent_out), _ptr(workspace), int(workspace.numel()), _stream_ptr(stream))
+    _check(rc, "mla_merge_splits_v_up_proj")
+    return out
+
+
+def mla_decode_v_up_proj(q, latent_cache, block_table, seq_lens, softmax_scale, w_uv, *, plan,
+                         workspace, out=None, lse=None, latent_out=None, stream=None):
+    """Decode then up-projection (fused with the split merge for split plans):
+    returns bf16 ``out [B, N, 128]``."""
+    import torch
+    B, N, _ = q.shape
+    _check_tensor(w_uv, "w_uv", torch.bfloat16, (N, 512, 128))
+    if out is None:
+        out = torch.empty((B, N, 128), dtype=torch.bfloat16, device=q.device)
+    _check_tensor(out, "out", torch.bfloat16, (B, N, 128))
+    rc = load_library().mla_decode_v_up_proj(
+        ctypes.byref(plan), _ptr(q), _ptr(latent_cache), int(latent_cache.shape[0]),
+        _ptr(block_table), _ptr(seq_lens), float(softmax_scale), _ptr(w_uv), _ptr(out), _ptr(lse),
+        _ptr(latent_out), _ptr(workspace), int(workspace.numel()), _stream_ptr(stream))
+    _check(rc, "mla_decode_v_up_proj")
+    return out
 
 
 def dcp_local_seq_lens(seq_lens_host, world, rank, interleave):

@@ -150,6 +150,54 @@ extern "C" int mla_decode_fp8(const mla_decode_plan_t* plan, const void* q,
     return launch_decode_and_merge(p, plan, stream, true);
 }
 
+extern "C" int mla_decode_v_up_proj(const mla_decode_plan_t* plan, const void* q,
+                                    const void* latent_cache, int64_t num_blocks,
+                                    const int32_t* block_table, const int32_t* seq_lens,
+                                    float softmax_scale, const void* w_uv, void* out, float* lse,
+                                    void* latent_out, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+    int rc = validate_plan(plan);
+    if (rc != MLA_OK) return rc;
+    if (!q || !latent_cache || !block_table || !seq_lens || !w_uv || !out)
+        return MLA_ERR_INVALID_ARG;
+    if (num_blocks < 1 || !std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(latent_cache, 16) || !aligned(out, 16) ||
+        !aligned(w_uv, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+        (lse && !aligned(lse, 4)) || (latent_out && !aligned(latent_out, 16)))
+        return MLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < plan->workspace_bytes || !aligned(workspace, 256))
+        return MLA_ERR_WORKSPACE;
+    if (plan->kernel == MLA_KERNEL_TC && num_blocks > tc_max_blocks()) return MLA_ERR_UNSUPPORTED;
+    const bool fused = plan->sched_pairs == 0 && plan->num_kv_splits > 1 &&
+                       plan->num_kv_splits <= kMaxFusedMergeSplits;
+    // Without a split merge to fuse into, the decode writes the latent rows
+    // and the up-projection reads them back: the caller provides them.
+    if (!fused && !latent_out) return MLA_ERR_INVALID_ARG;
+    if (plan->batch == 0) return MLA_OK;
+    char* ws = static_cast<char*>(workspace);
+    if (!fused) {
+        const DecodeParams p = make_decode_params(plan, q, latent_cache, num_blocks, block_table,
+                                                  seq_lens, softmax_scale, latent_out, lse, ws,
+                                                  nullptr, 1, plan->num_heads, 0);
+        rc = launch_decode_and_merge(p, plan, stream);
+        if (rc != MLA_OK) return rc;
+        return mla_v_up_proj(latent_out, w_uv, plan->batch, plan->num_heads, out, workspace,
+                             workspace_bytes, stream);
+    }
+    // Split schedule: the decode leaves fp32 partials, merged straight into
+    // the up-projection's operand tile.
+    const DecodeParams p = make_decode_params(plan, q, latent_cache, num_blocks, block_table,
+                                              seq_lens, softmax_scale, out, lse, ws, nullptr, 1,
+                                              plan->num_heads, 0);
+    int e = plan->kernel == MLA_KERNEL_TC ? launch_decode_tc(p, plan->grid_ctas, stream)
+                                          : launch_decode_simt(p, stream);
+    if (e != 0) return MLA_ERR_CUDA;
+    e = launch_merge_up_proj(p.o_part, p.lse_part, plan->batch, plan->num_heads,
+                             plan->num_kv_splits, w_uv, static_cast<uint16_t*>(out), lse,
+                             static_cast<uint16_t*>(latent_out), p.status, stream);
+    return e == 0 ? MLA_OK : MLA_ERR_CUDA;
+}
+
 extern "C" int mla_merge_splits(const float* o_part, const float* lse_part, int batch,
                                 int num_heads, int num_splits, int v_dim, void* out, float* lse,
                                 void* stream) {

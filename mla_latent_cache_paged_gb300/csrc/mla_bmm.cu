@@ -6,6 +6,10 @@
 //       cache row `slot_mapping[b]` = [kv_c[b] | k_pe[b]]
 //   up-projection (mla_v_up_proj):
 //       out[b, n, :]     = x[b, n, :] . W_UV[n]            W_UV bf16 [N, 512, 128]
+//   merge + up-projection (mla_merge_splits_v_up_proj):
+//       x[b, n, :]       = LSE-weighted merge of the S split partials of (b, n),
+//                          rounded to bf16 in shared memory (never written out
+//                          unless asked), then the up-projection above
 //
 // vLLM mla_attention API docs, MLAAttention.forward_impl (torch.bmm of
 // (N, B, P) by W_UK_T, then the q concat) and _v_up_proj (torch.bmm by W_UV);
@@ -40,6 +44,11 @@ namespace mla {
 namespace {
 
 constexpr int kBmmThreads = 128;
+constexpr int kMergeUpThreads = 256;         // + six warps that merge the A tile
+constexpr int kMergeWarps = 6;
+constexpr int kMaxFusedSplits = 512;         // merge weights: 6 warps x 512 fp32 in the q_pe area
+// Kernel modes: the up-projection, the front end, the merge + up-projection.
+constexpr int kModeUp = 0, kModeFront = 1, kModeMergeUp = 2;
 constexpr int kM = 128;                      // batch rows per CTA
 constexpr int kChunk = 64;                   // K per ring stage
 constexpr int kABytes = kM * kChunk * 2;     // 16 KB
@@ -86,6 +95,11 @@ struct BmmParams {
     uint16_t* cache;             // front end: [num_blocks, 64, 576]
     int64_t num_blocks;
     int32_t* status;
+    const float* o_part;         // merge + up-projection: fp32 [B, N, S, 512]
+    const float* lse_part;       //                        fp32 [B, N, S]
+    int splits;
+    float* lse;                  //                        merged LSE [B, N] or null
+    uint16_t* latent;            //                        merged rows bf16 [B, N, 512] or null
 };
 
 __device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort,
@@ -119,12 +133,98 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-template <int J, int KD, int STAGES, bool kFrontEnd>
-__global__ void __launch_bounds__(kBmmThreads, 1)
+// Merge + up-projection: the merger warps build the A tile (row r = request
+// m0 + r of head n) from the split partials: per row the S log-sum-exps give
+// the merged LSE and one weight per split (merge_attn_states, vLLM
+// mla_attention API docs, "Chunked Prefill"; a -inf partial weighs 0), lane
+// l sums columns 16l..16l+15 over the splits in split order, and the bf16
+// result goes to A chunk l / 4 in the 128-byte swizzled K-major layout the
+// MMAs read. Rows past the batch are left as they are (their products are
+// never stored).
+__device__ void merge_rows_into_a(const BmmParams& p, unsigned char* smem, float* wts, int m0,
+                                  int n, int mw, int lane) {
+    const int S = p.splits;
+    const int rows = min(kM, p.batch - m0);
+    for (int r = mw; r < rows; r += kMergeWarps) {
+        const int64_t row = int64_t(m0 + r) * p.heads + n;
+        const float* ls = p.lse_part + row * S;
+        float m = -INFINITY;
+        for (int s = lane; s < S; s += 32) m = fmaxf(m, ls[s]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float total = -INFINITY;
+        if (m != -INFINITY) {
+            float z = 0.f;
+            for (int s = lane; s < S; s += 32) z += expf(ls[s] - m);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            total = m + logf(z);
+            for (int s = lane; s < S; s += 32) wts[s] = expf(ls[s] - total);
+        } else {
+            for (int s = lane; s < S; s += 32) wts[s] = 0.f;
+        }
+        __syncwarp();
+        if (lane == 0 && p.lse != nullptr) p.lse[row] = total;
+        float4 acc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* base = p.o_part + row * S * kLkv + lane * 16;
+        for (int s0 = 0; s0 < S; s0 += 4) {
+            // four partials' loads in flight before their sums
+            float4 v[4][4];
+            float ws[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int s = s0 + q;
+                ws[q] = s < S ? wts[s] : 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    v[q][k] = ws[q] != 0.f
+                                  ? __ldg(reinterpret_cast<const float4*>(base + s * kLkv) + k)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    acc[k].x = fmaf(ws[q], v[q][k].x, acc[k].x);
+                    acc[k].y = fmaf(ws[q], v[q][k].y, acc[k].y);
+                    acc[k].z = fmaf(ws[q], v[q][k].z, acc[k].z);
+                    acc[k].w = fmaf(ws[q], v[q][k].w, acc[k].w);
+                }
+        }
+        __syncwarp();
+        uint32_t h[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            h[2 * k] = uint32_t(f32_to_bf16_bits_rn(acc[k].x)) |
+                       (uint32_t(f32_to_bf16_bits_rn(acc[k].y)) << 16);
+            h[2 * k + 1] = uint32_t(f32_to_bf16_bits_rn(acc[k].z)) |
+                           (uint32_t(f32_to_bf16_bits_rn(acc[k].w)) << 16);
+        }
+        // columns 16 lane .. 16 lane + 15: chunk lane / 4, 16-byte pieces
+        // 2 (lane % 4) and 2 (lane % 4) + 1 of the row
+        unsigned char* arow = smem + (lane >> 2) * kABytes + r * 128;
+        const int pc = 2 * (lane & 3);
+        *reinterpret_cast<uint4*>(arow + ((pc ^ (r & 7)) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(arow + (((pc + 1) ^ (r & 7)) * 16)) =
+            make_uint4(h[4], h[5], h[6], h[7]);
+        if (p.latent != nullptr) {
+            uint4* dst = reinterpret_cast<uint4*>(p.latent + row * kLkv + lane * 16);
+            dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+    }
+}
+
+template <int J, int KD, int STAGES, int kMode>
+__global__ void __launch_bounds__(kMode == kModeMergeUp ? kMergeUpThreads : kBmmThreads, 1)
 mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_w,
                const __grid_constant__ CUtensorMap tmap_o) {
     using Sh = BmmShape<J, KD, STAGES>;
+    constexpr bool kFrontEnd = kMode == kModeFront;
+    constexpr bool kMergeA = kMode == kModeMergeUp;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -147,7 +247,7 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
     // waits for its predecessor below.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
-        ptx::mbar_init(b_afull, 1);
+        ptx::mbar_init(b_afull, kMergeA ? kMergeWarps * 32 : 1);
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(b_full + 8 * s, 1);
             ptx::mbar_init(b_empty + 8 * s, 1);
@@ -171,10 +271,12 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
         // into stage c % STAGES once its previous use is done.
         int issued = 0;
         if (ptx::elect_one()) {
-            ptx::mbar_arrive_expect_tx(b_afull, Sh::kAllABytes + (kFrontEnd ? kABytes : 0));
-            for (int c = 0; c < Sh::kChunks; ++c)
-                ptx::tma_load_2d(sbase + uint32_t(c * kABytes), &tmap_a,
-                                 n * p.a_head + c * kChunk, m0, b_afull);
+            if constexpr (!kMergeA) {
+                ptx::mbar_arrive_expect_tx(b_afull, Sh::kAllABytes + (kFrontEnd ? kABytes : 0));
+                for (int c = 0; c < Sh::kChunks; ++c)
+                    ptx::tma_load_2d(sbase + uint32_t(c * kABytes), &tmap_a,
+                                     n * p.a_head + c * kChunk, m0, b_afull);
+            }
             if (kFrontEnd)   // q_pe: columns 128..191 of the head, next to q_nope
                 ptx::tma_load_2d(sbase + Sh::kPeOff, &tmap_a, n * p.a_head + kNope, m0, b_afull);
             for (int c = 0; c < Sh::kChunks; ++c) {
@@ -192,7 +294,7 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
                 ++issued;
             }
             // Copies still in flight (after an abort) land before the CTA exits.
-            bmm_wait(b_afull, 0, abort, p.status, kSiteRingDrain, true);
+            if constexpr (!kMergeA) bmm_wait(b_afull, 0, abort, p.status, kSiteRingDrain, true);
             for (int c = issued - STAGES < 0 ? 0 : issued - STAGES; c < issued; ++c)
                 bmm_wait(b_full + 8 * (c % STAGES), (c / STAGES) & 1, abort, p.status,
                          kSiteRingDrain, true);
@@ -234,6 +336,12 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
             ptx::mma_commit(b_acc);
         }
         __syncwarp();
+    } else if (kMergeA) {
+        // warps 2-7: the A tile from the split partials, then A is full
+        float* wts = reinterpret_cast<float*>(smem + Sh::kPeOff) + (warp - 2) * kMaxFusedSplits;
+        merge_rows_into_a(p, smem, wts, m0, n, warp - 2, lane);
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(b_afull);
     } else if (kFrontEnd) {
         const int t = threadIdx.x - 64;   // warps 2-3
         // q_pe: the tile that landed with stage 0 goes out as four 32-row boxes
@@ -286,8 +394,8 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
     // rows, 64 columns at a time, in the (now idle) ring in the 128-byte
     // swizzled layout of the output tensor map and stores them by TMA; rows
     // past the batch fall outside the map and are not written.
-    bool acc_ok = true;
-    if (lane == 0)
+    bool acc_ok = warp < 4;   // the four warps of the accumulator's lanes
+    if (acc_ok && lane == 0)
         acc_ok = bmm_wait(b_acc, 0, abort, p.status, kSiteAccFull, true);
     acc_ok = __shfl_sync(0xffffffffu, acc_ok ? 1 : 0, 0) != 0 && *abort == 0;
     ptx::tc_fence_after();
@@ -357,21 +465,25 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int J, int KD, int STAGES, bool kFrontEnd>
+template <int J, int KD, int STAGES, int kMode>
 int launch_bmm(const BmmParams& p, const void* a, const void* w, cudaStream_t st) {
     using Sh = BmmShape<J, KD, STAGES>;
     CUtensorMap ta, tw, to;
-    if (!encode_2d(&ta, a, uint64_t(p.heads) * p.a_head, uint64_t(p.batch), kM) ||
+    // (merge + up-projection: A is built in shared memory; the map over the
+    // output stands in for the unused A map)
+    if (!encode_2d(&ta, kMode == kModeMergeUp ? static_cast<const void*>(p.out) : a,
+                   uint64_t(p.heads) * (kMode == kModeMergeUp ? p.out_head : p.a_head),
+                   uint64_t(p.batch), kMode == kModeMergeUp ? 32 : kM) ||
         !encode_2d(&tw, w, J, uint64_t(p.heads) * KD, kChunk) ||
         !encode_2d(&to, p.out, uint64_t(p.heads) * p.out_head, uint64_t(p.batch), 32))
         return int(cudaErrorInvalidValue);
-    auto kernel = mla_bmm_kernel<J, KD, STAGES, kFrontEnd>;
+    auto kernel = mla_bmm_kernel<J, KD, STAGES, kMode>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Sh::kSmemBytes);
     if (e != cudaSuccess) return int(e);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned((p.batch + kM - 1) / kM), unsigned(p.heads));
-    cfg.blockDim = dim3(kBmmThreads, 1, 1);
+    cfg.blockDim = dim3(kMode == kModeMergeUp ? kMergeUpThreads : kBmmThreads, 1, 1);
     cfg.dynamicSmemBytes = Sh::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -422,7 +534,7 @@ extern "C" int mla_q_absorb_concat_cache(const void* q, const void* w_uk_t, cons
     p.cache = static_cast<uint16_t*>(latent_cache);
     p.num_blocks = num_blocks;
     p.status = static_cast<int32_t*>(workspace);
-    return status_of(launch_bmm<kLkv, kNope, 2, true>(p, q, w_uk_t,
+    return status_of(launch_bmm<kLkv, kNope, 2, kModeFront>(p, q, w_uk_t,
                                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -443,6 +555,53 @@ extern "C" int mla_v_up_proj(const void* x, const void* w_uv, int batch, int num
     p.out_row = int64_t(num_heads) * kNope;
     p.out_head = kNope;
     p.status = static_cast<int32_t*>(workspace);
-    return status_of(launch_bmm<kNope, kLkv, 4, false>(p, x, w_uv,
-                                                       static_cast<cudaStream_t>(stream)));
+    return status_of(launch_bmm<kNope, kLkv, 4, kModeUp>(p, x, w_uv,
+                                                         static_cast<cudaStream_t>(stream)));
+}
+
+namespace mla {
+
+int launch_merge_up_proj(const float* o_part, const float* lse_part, int batch, int num_heads,
+                         int num_splits, const void* w_uv, uint16_t* out, float* lse,
+                         uint16_t* latent, int32_t* status, void* stream) {
+    BmmParams p{};
+    p.batch = batch;
+    p.heads = num_heads;
+    p.a_head = kLkv;
+    p.out = out;
+    p.out_row = int64_t(num_heads) * kNope;
+    p.out_head = kNope;
+    p.status = status;
+    p.o_part = o_part;
+    p.lse_part = lse_part;
+    p.splits = num_splits;
+    p.lse = lse;
+    p.latent = latent;
+    return launch_bmm<kNope, kLkv, 4, kModeMergeUp>(p, nullptr, w_uv,
+                                                    static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace mla
+
+extern "C" int mla_merge_splits_v_up_proj(const float* o_part, const float* lse_part, int batch,
+                                          int num_heads, int num_splits, const void* w_uv,
+                                          void* out, float* lse, void* latent_out,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+    if (batch < 0 || num_heads < 0 || num_heads > kMaxHeads || num_splits < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (num_splits > kMaxFusedSplits) return MLA_ERR_UNSUPPORTED;
+    if (batch == 0 || num_heads == 0) return MLA_OK;
+    if (!o_part || !lse_part || !w_uv || !out) return MLA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kStatusBytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return MLA_ERR_WORKSPACE;
+    if (!aligned16(o_part) || (reinterpret_cast<uintptr_t>(lse_part) & 3u) != 0 ||
+        !aligned16(w_uv) || !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+        (latent_out && !aligned16(latent_out)))
+        return MLA_ERR_INVALID_ARG;
+    return status_of(launch_merge_up_proj(o_part, lse_part, batch, num_heads, num_splits, w_uv,
+                                          static_cast<uint16_t*>(out), lse,
+                                          static_cast<uint16_t*>(latent_out),
+                                          static_cast<int32_t*>(workspace), stream));
 }

@@ -99,6 +99,13 @@ int launch_merge(const float* o_part, const float* lse_part, int rows, int num_s
 int launch_rank_combine(const uint16_t* out_parts, const float* lse_parts, int world, int rows,
                         int v_dim, uint16_t* out, float* lse, void* stream);
 int launch_merge_balanced(const DecodeParams& p, void* stream);
+// Merge of split partials [B, N, S, 512] straight into the up-projection by
+// W_UV [N, 512, 128] (mla_bmm.cu): out bf16 [B, N, 128], lse [B, N] and the
+// merged bf16 rows [B, N, 512] (each optional: null skips it).
+int launch_merge_up_proj(const float* o_part, const float* lse_part, int batch, int num_heads,
+                         int num_splits, const void* w_uv, uint16_t* out, float* lse,
+                         uint16_t* latent, int32_t* status, void* stream);
+constexpr int kMaxFusedMergeSplits = 512;
 int launch_gather(const uint16_t* cache, int64_t num_blocks, const int32_t* block_table,
                   const int32_t* seq_lens, int batch, int max_blocks, int dst_max_tokens,
                   uint16_t* dst, int32_t* status, void* stream);

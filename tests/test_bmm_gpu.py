@@ -152,3 +152,91 @@ def test_decode_step_front_end_decode_up_projection():
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert rel < 1e-2, rel
     np.testing.assert_allclose(lse.double().cpu().numpy(), ref_lse, atol=5e-3)
+
+
+# ------------------------------------------------ merge fused with the up-projection
+
+@pytest.mark.parametrize("B,N,S", [(1, 1, 1), (3, 5, 3), (130, 128, 2), (32, 128, 32),
+                                   (4, 16, 64), (7, 3, 512)])
+def test_merge_splits_v_up_proj_against_the_oracle(B, N, S):
+    """The merged rows (returned through latent_out) are within one bf16 ulp
+    of the oracle's merge, and the output is within one ulp of the oracle's
+    up-projection of those very rows; neutral partials (-inf LSE, NaN rows)
+    carry no weight, and a row whose partials are all neutral gives 0."""
+    import torch
+    from oracle import merge_partials
+    rng = np.random.default_rng(1400 + B + N + S)
+    o = rng.standard_normal((B, N, S, 512)).astype(np.float32)
+    ls = (rng.standard_normal((B, N, S)) * 3).astype(np.float32)
+    ls[0, 0, :] = -np.inf
+    if S > 1:
+        ls[-1, -1, ::2] = -np.inf
+        o[-1, -1, ::2] = np.nan
+    o[0, 0] = np.nan
+    w = _bf16(rng, (N, 512, 128), 1 / np.sqrt(512))
+    ws = binding.new_status_workspace()
+    lat = torch.empty((B, N, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, N), dtype=torch.float32, device="cuda")
+    out = binding.mla_merge_splits_v_up_proj(torch.from_numpy(o).cuda(),
+                                             torch.from_numpy(ls).cuda(), _dev(w),
+                                             workspace=ws, lse=lse, latent_out=lat)
+    torch.cuda.synchronize()
+    assert binding.read_error(ws) == 0
+    o_ref = np.where(np.isneginf(ls)[..., None], 0.0, o.astype(np.float64))
+    ref_lat, ref_lse = merge_partials(o_ref, ls.astype(np.float64))
+    _assert_within_one_ulp(bf16_tensor_bits(lat), ref_lat, "merged rows")
+    got_lse = lse.double().cpu().numpy()
+    assert np.isneginf(got_lse[0, 0]) and np.isneginf(ref_lse[0, 0])
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(got_lse[fin], ref_lse[fin], rtol=0, atol=1e-5)
+    ref = v_up_proj(bf16_bits_to_f64(bf16_tensor_bits(lat)), bf16_bits_to_f64(w))
+    _assert_within_one_ulp(bf16_tensor_bits(out), ref, "fused up-projection")
+    assert np.all(bf16_tensor_bits(out)[0, 0] == 0)
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_decode_v_up_proj_matches_the_separate_calls_and_the_oracle(splits):
+    """mla_decode_v_up_proj: a split plan merges straight into the
+    up-projection (no latent rows written), S = 1 goes through latent_out.
+    Against mla_decode + mla_v_up_proj on the same inputs, and against the
+    oracle's decode and up-projection with the latent rounded to bf16."""
+    import torch
+    from parity_util import oracle_rows
+    B, N = 5, 128
+    lens = [1, 100, 700, 2048, 65]
+    w_l = make_workload("decode_up", B, N, lens, seed=1500 + splits, extra_blocks=2,
+                        num_kv_splits=splits)
+    rng = np.random.default_rng(1501)
+    w_uv = _dev(_bf16(rng, (N, 512, 128), 1 / np.sqrt(512)))
+    q, cache, table, seq = to_torch(w_l)
+    plan = binding.make_plan(B, N, w_l.max_blocks_per_seq, seq_lens_host=w_l.seq_lens,
+                             max_seq_len=w_l.max_seq_len, num_kv_splits=splits, schedule="split")
+    assert plan.num_kv_splits == splits
+    ws = binding.new_workspace(plan)
+    lat = torch.empty((B, N, 512), dtype=torch.bfloat16, device="cuda")
+    if splits == 1:
+        with pytest.raises(binding.MlaError):    # the latent rows have nowhere to go
+            binding.mla_decode_v_up_proj(q, cache, table, seq, w_l.softmax_scale, w_uv,
+                                         plan=plan, workspace=ws)
+    out = binding.mla_decode_v_up_proj(q, cache, table, seq, w_l.softmax_scale, w_uv, plan=plan,
+                                       workspace=ws, latent_out=lat if splits == 1 else None)
+    torch.cuda.synchronize()
+    assert binding.read_error(ws) == 0
+    sep_lat, _ = binding.mla_decode(q, cache, table, seq, w_l.softmax_scale, plan=plan,
+                                    workspace=ws)
+    sep = binding.mla_v_up_proj(sep_lat, w_uv, workspace=ws)
+    torch.cuda.synchronize()
+    got = bf16_bits_to_f64(bf16_tensor_bits(out))
+    ref_sep = bf16_bits_to_f64(bf16_tensor_bits(sep))
+    if splits == 1:
+        assert torch.equal(out, sep)                 # the same two kernels
+    else:
+        # the fused merge sums the splits in the same order as one of the
+        # merge kernel's layouts, not necessarily this one: a merged row may
+        # round one ulp apart
+        assert np.abs(got - ref_sep).max() <= 2e-2
+    ref_lat, _ = oracle_rows(w_l, range(B))
+    ref_lat = bf16_bits_to_f64(f32_to_bf16_bits(ref_lat.astype(np.float32)))
+    ref = v_up_proj(ref_lat, bf16_bits_to_f64(bf16_tensor_bits(w_uv)))
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel < 1e-2, rel
