@@ -34,6 +34,7 @@ DECODE_KERNEL_SOURCES = {
     1: ["mla_decode_simt.cu", "mla_device.cuh", "mla_internal.h"],
     2: ["mla_decode_tc.cu", "tc_ptx.cuh", "mla_device.cuh", "mla_internal.h"],
 }
+# the recorded-traffic key of a kernel: its variant and the cache dtype
 
 
 def parse_args():
@@ -718,9 +719,15 @@ def run_ours(args, w, rank, world):
     out = torch.empty((w.batch, w.num_heads, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.batch, w.num_heads), dtype=torch.float32, device=dev)
 
+    fp8 = w.cache_dtype == "fp8"
+
     def step():
-        binding.mla_decode(q, cache, table, lens, w.softmax_scale, plan=plan, out=out, lse=lse,
-                           workspace=ws)
+        if fp8:
+            binding.mla_decode_fp8(q, cache, table, lens, w.softmax_scale, w.k_scale, plan=plan,
+                                   out=out, lse=lse, workspace=ws)
+        else:
+            binding.mla_decode(q, cache, table, lens, w.softmax_scale, plan=plan, out=out,
+                               lse=lse, workspace=ws)
 
     def barrier():
         if world > 1:
@@ -791,8 +798,14 @@ def run_ours(args, w, rank, world):
             bf["ev_in"].record(s_in)
         stream.wait_event(bf["ev_in"])
         stream.wait_event(bf["ev_out"])         # step k-2's outputs have been read back
-        binding.mla_decode(bf["q"], cache, bf["table"], bf["lens"], w.softmax_scale, plan=plan,
-                           out=bf["out"], lse=bf["lse"], workspace=ws, stream=stream)
+        if fp8:
+            binding.mla_decode_fp8(bf["q"], cache, bf["table"], bf["lens"], w.softmax_scale,
+                                   w.k_scale, plan=plan, out=bf["out"], lse=bf["lse"],
+                                   workspace=ws, stream=stream)
+        else:
+            binding.mla_decode(bf["q"], cache, bf["table"], bf["lens"], w.softmax_scale,
+                               plan=plan, out=bf["out"], lse=bf["lse"], workspace=ws,
+                               stream=stream)
         bf["ev_comp"].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(bf["ev_comp"])
@@ -848,8 +861,10 @@ def run_ours(args, w, rank, world):
             "num_kv_splits": plan.num_kv_splits,
             "schedule": (f"page-balanced over {plan.sched_pairs} CTA pairs + merge"
                          if plan.sched_pairs > 0 else f"split S={plan.num_kv_splits}"),
-            "kernel": {1: "simt", 2: "tcgen05"}[plan.kernel],
-            "l2": "inputs larger than L2 (%.2f GB cache), no flush" % (cache.numel() * 2 / 1e9),
+            "kernel": {1: "simt", 2: "tcgen05"}[plan.kernel] + (" fp8 cache" if fp8 else ""),
+            "cache_dtype": w.cache_dtype,
+            "l2": "inputs larger than L2 (%.2f GB cache), no flush" % (
+                cache.numel() * cache.element_size() / 1e9),
             "parallelism": f"requests replicated per rank x{world} (weak)" if world > 1 else "1 GPU",
         },
         "roofline": {

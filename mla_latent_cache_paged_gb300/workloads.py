@@ -249,6 +249,13 @@ def _c3_small(with_data=True):
                          num_kv_splits=0, with_data=with_data)
 
 
+def _c3_mid(with_data=True):
+    # The headline shape at 32 requests: 604 MB of bf16 cache (302 MB as fp8),
+    # larger than L2 either way; the small case for full-section profiles.
+    return make_workload("b32_n128_l8192", 32, 128, [8192] * 32, seed=20260007,
+                         num_kv_splits=0, with_data=with_data)
+
+
 def _c4(length):
     def build(with_data=True):
         return make_workload(f"b4_n128_l{length // 1024}k_s64", 4, 128, [length] * 4,
@@ -284,6 +291,7 @@ WORKLOADS = {
     "b32_n128_l1k-4k": _c2,
     "b128_n128_l8192": _c3,
     "b16_n128_l8192": _c3_small,
+    "b32_n128_l8192": _c3_mid,
     "b4_n128_l32k_s64": _c4(32768),
     "b4_n128_l64k_s64": _c4(65536),
     "b4_n128_l96k_s64": _c4(98304),
@@ -292,7 +300,7 @@ WORKLOADS = {
 }
 
 _SEEDS = {"b1_n16_l256_pool8": 20260001, "b32_n128_l1k-4k": 20260002,
-          "b128_n128_l8192": 20260003, "b16_n128_l8192": 20260006,
+          "b128_n128_l8192": 20260003, "b16_n128_l8192": 20260006, "b32_n128_l8192": 20260007,
           "b4_n128_l32k_s64": 20260004 * 10 + 1, "b4_n128_l64k_s64": 20260004 * 10 + 2,
           "b4_n128_l96k_s64": 20260004 * 10 + 3, "b4_n128_l128k_s64": 20260004 * 10 + 4,
           "b256_n128_logu16-32k_outliers": 20260005}
