@@ -72,6 +72,8 @@ extern "C" {
 #define MLA_PLAN_SPLIT_ONLY  0x2u  /* never choose the page-balanced schedule */
 #define MLA_PLAN_FORCE_BALANCED 0x4u  /* with num_kv_splits = 0: the page-balanced schedule
                                          wherever it applies, whatever the estimate */
+#define MLA_PLAN_FP32_PARTIALS 0x8u  /* keep the split schedule's partial rows in fp32 (default
+                                        bf16, the precision of the decode's output) */
 /* Test only (failure detection without a fault): the tensor-core kernel's
  * CTA 0 never issues its first K-ring load and every bounded wait of the call
  * is shortened to 2 ms (the merge's to 8 ms). The score warp's wait for that
@@ -91,9 +93,11 @@ extern "C" {
  * request b covers tokens [s*C_b, min((s+1)*C_b, L_b)) with
  * C_b = page_size * ceil(ceil(L_b/page_size)/S); empty splits contribute
  * nothing. With S = 1 the decode kernel writes `out` and `lse` itself; with
- * S > 1 it writes fp32 partials [B,N,S,Lkv] / [B,N,S] into the workspace and
- * mla_merge_splits combines them (an empty split writes only its LSE, -inf:
- * its weight is 0 and its row is never read). The tensor-core kernel runs
+ * S > 1 it writes partial rows [B,N,S,Lkv] (each normalised by its own
+ * weights; bf16, rounded to nearest even like the final output, or fp32 with
+ * MLA_PLAN_FP32_PARTIALS) and their fp32 LSEs [B,N,S] into the workspace,
+ * and the LSE-weighted merge combines them in fp32 (an empty split writes
+ * only its LSE, -inf: its weight is 0 and its row is never read). The tensor-core kernel runs
  * min(B*S, num_sms/2) CTA pairs, each over a contiguous run of the B*S
  * (request, split) items in request-major order, and stages a request's q
  * once for the consecutive splits it takes.
@@ -125,7 +129,7 @@ typedef struct mla_decode_plan {
     int32_t  grid_ctas;           /* CTAs the decode kernel launches */
     uint32_t flags;               /* MLA_PLAN_* as requested */
     uint64_t workspace_bytes;     /* bytes of `workspace` mla_decode needs */
-    uint64_t partial_offset;      /* byte offset of o_part [B,N,S,Lkv] fp32 */
+    uint64_t partial_offset;      /* byte offset of o_part [B,N,S,Lkv] (bf16, or fp32) */
     uint64_t lse_partial_offset;  /* byte offset of lse_part [B,N,S] fp32 */
     int32_t  sched_pairs;         /* 0: split schedule; C > 0: page-balanced schedule */
     uint32_t reserved[7];
@@ -240,9 +244,11 @@ int mla_decode_fp8(const mla_decode_plan_t* plan, const void* q, const void* lat
  * partial rows live in one fixed device array of 32 MiB inside the library;
  * every GPU that loads the library holds it until the process exits. A plan
  * whose workspace_bytes exceeds 32 MiB is rejected with MLA_ERR_SCRATCH_LIMIT.
- * The partials take 2,052 bytes per row, and 8 KiB go to the status header:
- * up to 16,348 rows fit (split schedule: B*N*S rows, e.g. B=32, N=128, S=3
- * fits and S=4 does not; page-balanced over C CTA pairs: 2*C*N rows, e.g.
+ * 8 KiB go to the status header; a split-schedule row (request, head,
+ * split) takes 1,028 bytes (2,052 with MLA_PLAN_FP32_PARTIALS) and a
+ * page-balanced row 2,052: up to 32,632 split rows fit (B*N*S: e.g. B=32,
+ * N=128, S=7 fits and S=8 does not; with fp32 rows 16,348: S=3 fits, S=4
+ * does not), or 16,348 page-balanced rows (2*C*N over C CTA pairs: e.g.
  * C=32, N=128).
  *
  *   plan, q, latent_cache, num_blocks, block_table, seq_lens, softmax_scale,

@@ -29,6 +29,7 @@ MLA_KERNEL_TC = 2
 MLA_PLAN_FORCE_SIMT = 0x1
 MLA_PLAN_SPLIT_ONLY = 0x2
 MLA_PLAN_FORCE_BALANCED = 0x4
+MLA_PLAN_FP32_PARTIALS = 0x8
 MLA_PLAN_DEBUG_WITHHOLD_LOAD = 0x100
 
 KV_LORA_RANK = 512

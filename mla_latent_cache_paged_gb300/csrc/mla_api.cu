@@ -67,6 +67,7 @@ DecodeParams make_decode_params(const mla_decode_plan_t* plan, const void* q,
     if (S > 1 || plan->sched_pairs > 0) {
         p.o_part = reinterpret_cast<float*>(ws + plan->partial_offset);
         p.lse_part = reinterpret_cast<float*>(ws + plan->lse_partial_offset);
+        p.part_bf16 = plan->sched_pairs == 0 && !(plan->flags & MLA_PLAN_FP32_PARTIALS);
     }
     return p;
 }
@@ -80,8 +81,12 @@ int launch_decode_and_merge(const DecodeParams& p, const mla_decode_plan_t* plan
     if (plan->sched_pairs > 0) {
         if (launch_merge_balanced(p, stream) != 0) return MLA_ERR_CUDA;
     } else if (plan->num_kv_splits > 1) {
-        e = launch_merge(p.o_part, p.lse_part, plan->batch * plan->num_heads,
-                         plan->num_kv_splits, kLkv, p.out, p.lse, stream);
+        e = p.part_bf16
+                ? launch_merge_bf16(reinterpret_cast<const uint16_t*>(p.o_part), p.lse_part,
+                                    plan->batch * plan->num_heads, plan->num_kv_splits, kLkv,
+                                    p.out, p.lse, stream)
+                : launch_merge(p.o_part, p.lse_part, plan->batch * plan->num_heads,
+                               plan->num_kv_splits, kLkv, p.out, p.lse, stream);
         if (e != 0) return MLA_ERR_CUDA;
     }
     return MLA_OK;
@@ -192,7 +197,7 @@ extern "C" int mla_decode_v_up_proj(const mla_decode_plan_t* plan, const void* q
     int e = plan->kernel == MLA_KERNEL_TC ? launch_decode_tc(p, plan->grid_ctas, stream)
                                           : launch_decode_simt(p, stream);
     if (e != 0) return MLA_ERR_CUDA;
-    e = launch_merge_up_proj(p.o_part, p.lse_part, plan->batch, plan->num_heads,
+    e = launch_merge_up_proj(p.o_part, p.part_bf16 != 0, p.lse_part, plan->batch, plan->num_heads,
                              plan->num_kv_splits, w_uv, static_cast<uint16_t*>(out), lse,
                              static_cast<uint16_t*>(latent_out), p.status, stream);
     return e == 0 ? MLA_OK : MLA_ERR_CUDA;

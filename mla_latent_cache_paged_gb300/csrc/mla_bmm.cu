@@ -95,7 +95,8 @@ struct BmmParams {
     uint16_t* cache;             // front end: [num_blocks, 64, 576]
     int64_t num_blocks;
     int32_t* status;
-    const float* o_part;         // merge + up-projection: fp32 [B, N, S, 512]
+    const void* o_part;          // merge + up-projection: [B, N, S, 512] fp32 or bf16
+    bool part_bf16;
     const float* lse_part;       //                        fp32 [B, N, S]
     int splits;
     float* lse;                  //                        merged LSE [B, N] or null
@@ -168,7 +169,7 @@ __device__ void merge_rows_into_a(const BmmParams& p, unsigned char* smem, float
         float4 acc[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* base = p.o_part + row * S * kLkv + lane * 16;
+        const int64_t base = row * S * kLkv + lane * 16;   // element index of split 0
         for (int s0 = 0; s0 < S; s0 += 4) {
             // four partials' loads in flight before their sums
             float4 v[4][4];
@@ -177,11 +178,23 @@ __device__ void merge_rows_into_a(const BmmParams& p, unsigned char* smem, float
             for (int q = 0; q < 4; ++q) {
                 const int s = s0 + q;
                 ws[q] = s < S ? wts[s] : 0.f;
+                const int64_t e0 = base + int64_t(s) * kLkv;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    v[q][k] = ws[q] != 0.f
-                                  ? __ldg(reinterpret_cast<const float4*>(base + s * kLkv) + k)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < 4; ++k) {
+                    if (ws[q] == 0.f) {
+                        v[q][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else if (p.part_bf16) {
+                        const uint2 u = __ldg(reinterpret_cast<const uint2*>(
+                            static_cast<const uint16_t*>(p.o_part) + e0 + 4 * k));
+                        v[q][k] = make_float4(__uint_as_float(u.x << 16),
+                                              __uint_as_float(u.x & 0xffff0000u),
+                                              __uint_as_float(u.y << 16),
+                                              __uint_as_float(u.y & 0xffff0000u));
+                    } else {
+                        v[q][k] = __ldg(reinterpret_cast<const float4*>(
+                            static_cast<const float*>(p.o_part) + e0) + k);
+                    }
+                }
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -561,9 +574,9 @@ extern "C" int mla_v_up_proj(const void* x, const void* w_uv, int batch, int num
 
 namespace mla {
 
-int launch_merge_up_proj(const float* o_part, const float* lse_part, int batch, int num_heads,
-                         int num_splits, const void* w_uv, uint16_t* out, float* lse,
-                         uint16_t* latent, int32_t* status, void* stream) {
+int launch_merge_up_proj(const void* o_part, bool part_bf16, const float* lse_part, int batch,
+                         int num_heads, int num_splits, const void* w_uv, uint16_t* out,
+                         float* lse, uint16_t* latent, int32_t* status, void* stream) {
     BmmParams p{};
     p.batch = batch;
     p.heads = num_heads;
@@ -573,6 +586,7 @@ int launch_merge_up_proj(const float* o_part, const float* lse_part, int batch, 
     p.out_head = kNope;
     p.status = status;
     p.o_part = o_part;
+    p.part_bf16 = part_bf16;
     p.lse_part = lse_part;
     p.splits = num_splits;
     p.lse = lse;
@@ -600,7 +614,8 @@ extern "C" int mla_merge_splits_v_up_proj(const float* o_part, const float* lse_
         !aligned16(w_uv) || !aligned16(out) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
         (latent_out && !aligned16(latent_out)))
         return MLA_ERR_INVALID_ARG;
-    return status_of(launch_merge_up_proj(o_part, lse_part, batch, num_heads, num_splits, w_uv,
+    return status_of(launch_merge_up_proj(o_part, false, lse_part, batch, num_heads, num_splits,
+                                          w_uv,
                                           static_cast<uint16_t*>(out), lse,
                                           static_cast<uint16_t*>(latent_out),
                                           static_cast<int32_t*>(workspace), stream));

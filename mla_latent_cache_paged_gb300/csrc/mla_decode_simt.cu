@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 2) mla_decode_simt_kernel(DecodePara
         __syncthreads();
     }
 
-    // 6. Epilogue: normalise; final bf16 output or fp32 split partial.
+    // 6. Epilogue: normalise; final bf16 output or the split's partial row
+    // (bf16, or fp32).
     const int d = 2 * tid;
 #pragma unroll
     for (int h = 0; h < kHG; ++h) {
@@ -211,8 +212,15 @@ __global__ void __launch_bounds__(kThreads, 2) mla_decode_simt_kernel(DecodePara
             *reinterpret_cast<uint32_t*>(p.out + row * kLkv + d) = packed;
             if (tid == 0 && p.lse != nullptr) p.lse[row] = lse;
         } else {
-            float2 v = make_float2(acc[h][0] * inv, acc[h][1] * inv);
-            *reinterpret_cast<float2*>(p.o_part + (row * S + split) * kLkv + d) = v;
+            const size_t prow = (row * S + split) * kLkv + d;
+            if (p.part_bf16) {
+                *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.o_part) + prow) =
+                    uint32_t(f32_to_bf16_bits_rn(acc[h][0] * inv)) |
+                    (uint32_t(f32_to_bf16_bits_rn(acc[h][1] * inv)) << 16);
+            } else {
+                *reinterpret_cast<float2*>(p.o_part + prow) =
+                    make_float2(acc[h][0] * inv, acc[h][1] * inv);
+            }
             if (tid == 0) p.lse_part[row * S + split] = lse;
         }
     }

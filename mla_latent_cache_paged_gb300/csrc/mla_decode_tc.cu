@@ -1131,6 +1131,16 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                         for (int i = 0; i < 4; ++i)
                             d4[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     }
+                } else if (p.part_bf16) {
+                    // bf16 split partial row (workspace rows 1 KB apart).
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.o_part) + prow * kLkv + col;
+                    uint32_t v[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        v[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv,
+                                           __uint_as_float(o[2 * i + 1]) * inv);
+                    ptx::st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(v));
+                    ptx::st_global_v8(dst + 16, *reinterpret_cast<const uint32_t(*)[8]>(v + 8));
                 } else {
                     // fp32 partial row (workspace: 256-byte aligned rows).
                     float* dst = p.o_part + prow * kLkv + col;

@@ -66,6 +66,7 @@ struct DecodeParams {
     float* o_part;                // fp32 partial rows: [B, N, S, 512] (split, S > 1)
                                   //                    or [2 * pairs, N, 512] (balanced)
     float* lse_part;              // fp32 [B, N, S] or [2 * pairs, N]
+    int32_t part_bf16;            // split schedule: partial rows stored as bf16
     int32_t* status;              // error word and its detail (int32[2])
     int32_t* counters;            // status header holding the page-balanced merge's
                                   // per-request counters ([kReadyWord + b], [kDoneWord + b])
@@ -94,6 +95,9 @@ int launch_decode_tc_loader_dump(const DecodeParams& p, int grid_ctas, void* str
 int launch_decode_tc_fp8(const DecodeParams& p, int grid_ctas, void* stream);
 int launch_merge(const float* o_part, const float* lse_part, int rows, int num_splits,
                  int v_dim, uint16_t* out, float* lse, void* stream);
+// The same over bf16 partial rows.
+int launch_merge_bf16(const uint16_t* o_part, const float* lse_part, int rows, int num_splits,
+                      int v_dim, uint16_t* out, float* lse, void* stream);
 // Combine of per-rank results in rank-major layout: bf16 [world, rows, v_dim]
 // and fp32 [world, rows] -> bf16 [rows, v_dim], fp32 [rows].
 int launch_rank_combine(const uint16_t* out_parts, const float* lse_parts, int world, int rows,
@@ -102,9 +106,10 @@ int launch_merge_balanced(const DecodeParams& p, void* stream);
 // Merge of split partials [B, N, S, 512] straight into the up-projection by
 // W_UV [N, 512, 128] (mla_bmm.cu): out bf16 [B, N, 128], lse [B, N] and the
 // merged bf16 rows [B, N, 512] (each optional: null skips it).
-int launch_merge_up_proj(const float* o_part, const float* lse_part, int batch, int num_heads,
-                         int num_splits, const void* w_uv, uint16_t* out, float* lse,
-                         uint16_t* latent, int32_t* status, void* stream);
+// (o_part holds bf16 rows when part_bf16.)
+int launch_merge_up_proj(const void* o_part, bool part_bf16, const float* lse_part, int batch,
+                         int num_heads, int num_splits, const void* w_uv, uint16_t* out,
+                         float* lse, uint16_t* latent, int32_t* status, void* stream);
 constexpr int kMaxFusedMergeSplits = 512;
 int launch_gather(const uint16_t* cache, int64_t num_blocks, const int32_t* block_table,
                   const int32_t* seq_lens, int batch, int max_blocks, int dst_max_tokens,

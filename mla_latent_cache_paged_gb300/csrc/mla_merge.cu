@@ -379,6 +379,13 @@ int launch_merge(const float* o_part, const float* lse_part, int rows, int num_s
     return launch_merge_strided(o_part, a, static_cast<cudaStream_t>(stream));
 }
 
+int launch_merge_bf16(const uint16_t* o_part, const float* lse_part, int rows, int num_splits,
+                      int v_dim, uint16_t* out, float* lse, void* stream) {
+    const MergeArgs a{lse_part, rows, num_splits, v_dim, int64_t(num_splits) * v_dim, v_dim,
+                      num_splits, 1, out, lse};
+    return launch_merge_strided(o_part, a, static_cast<cudaStream_t>(stream));
+}
+
 int launch_rank_combine(const uint16_t* out_parts, const float* lse_parts, int world, int rows,
                         int v_dim, uint16_t* out, float* lse, void* stream) {
     const MergeArgs a{lse_parts, rows, world, v_dim, v_dim, int64_t(rows) * v_dim,

@@ -19,10 +19,12 @@
 namespace mla {
 namespace {
 
-// 32 MiB: room for the 8 KiB status header plus split partials of 2,052
-// bytes per (request, head, split) row, each of the two arrays rounded up to
-// 256 bytes: up to 16,348 rows, e.g. B=32, N=128, S=3 (12,288 rows; S=4 is 16,384).
-// A page-balanced plan over C CTA pairs has 2*C*N rows (C=32, N=128: 8,192).
+// 32 MiB: room for the 8 KiB status header plus the partial rows of a plan,
+// each of its two arrays rounded up to 256 bytes. A split row (request, head,
+// split) takes 1,028 bytes (bf16 row + fp32 LSE): up to 32,632 rows, e.g.
+// B=32, N=128, S=7 (28,672 rows; S=8 is 32,768); with MLA_PLAN_FP32_PARTIALS
+// 2,052 bytes: up to 16,348 rows. A page-balanced plan over C CTA pairs has
+// 2*C*N fp32 rows (C=32, N=128: 8,192).
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -37,22 +37,26 @@ int heads_per_simt_cta() { return 16; }
 // tensor-core kernel, in pages: q staging, pipeline fill and the epilogue.
 constexpr double kTcItemPages = 4.0;
 
-// Workspace layout for a plan: status header, then the fp32 partial rows and
-// their LSEs. Split schedule: [B, N, S, Lkv] and [B, N, S] (S > 1 only);
-// balanced schedule: [2 * pairs, N, Lkv] and [2 * pairs, N].
-void workspace_layout(int batch, int num_heads, int S, int pairs, uint64_t* part_off,
-                      uint64_t* lse_off, uint64_t* bytes) {
+// Workspace layout for a plan: status header, then the partial rows and
+// their fp32 LSEs. Split schedule: [B, N, S, Lkv] (bf16, or fp32 with
+// MLA_PLAN_FP32_PARTIALS) and [B, N, S] (S > 1 only); balanced schedule:
+// [2 * pairs, N, Lkv] fp32 and [2 * pairs, N].
+void workspace_layout(int batch, int num_heads, int S, int pairs, uint32_t flags,
+                      uint64_t* part_off, uint64_t* lse_off, uint64_t* bytes) {
     uint64_t rows = 0;
-    if (pairs > 0)
+    uint64_t elem = sizeof(float);
+    if (pairs > 0) {
         rows = uint64_t(2) * pairs * num_heads;
-    else if (S > 1)
+    } else if (S > 1) {
         rows = uint64_t(batch) * num_heads * S;
+        if (!(flags & MLA_PLAN_FP32_PARTIALS)) elem = 2;
+    }
     uint64_t off = kStatusBytes;
     *part_off = 0;
     *lse_off = 0;
     if (rows > 0) {
         *part_off = off;
-        off = align_up(off + rows * kLkv * sizeof(float), 256);
+        off = align_up(off + rows * kLkv * elem, 256);
         *lse_off = off;
         off = align_up(off + rows * sizeof(float), 256);
     }
@@ -93,7 +97,7 @@ double estimate(int kernel, int S, int batch, int num_heads, const std::vector<i
     double t = list_schedule(costs, workers);
     if (S > 1) {
         const double page_bytes = double(kPageSize) * kD * 2.0;
-        double partial = double(batch) * num_heads * S * (kLkv * 4.0 + 4.0) * 2.0;
+        double partial = double(batch) * num_heads * S * (kLkv * 2.0 + 4.0) * 2.0;
         double per_round = page_bytes * (kernel == MLA_KERNEL_TC ? workers : workers / 2.0);
         t += partial / per_round + 4.0;  // + the merge launch
     }
@@ -142,8 +146,8 @@ int validate_plan(const mla_decode_plan_t* p) {
                p->batch * p->num_kv_splits;
     if (grid != p->grid_ctas) return MLA_ERR_INVALID_ARG;
     uint64_t part_off, lse_off, bytes;
-    workspace_layout(p->batch, p->num_heads, p->num_kv_splits, p->sched_pairs, &part_off, &lse_off,
-                     &bytes);
+    workspace_layout(p->batch, p->num_heads, p->num_kv_splits, p->sched_pairs, p->flags, &part_off,
+                     &lse_off, &bytes);
     if (p->partial_offset != part_off || p->lse_partial_offset != lse_off ||
         p->workspace_bytes != bytes)
         return MLA_ERR_INVALID_ARG;
@@ -239,8 +243,8 @@ extern "C" int mla_decode_plan(int batch, int num_heads, int kv_lora_rank, int r
     else
         plan->grid_ctas = ((num_heads + heads_per_simt_cta() - 1) / heads_per_simt_cta()) * batch * S;
 
-    workspace_layout(batch, num_heads, S, pairs, &plan->partial_offset, &plan->lse_partial_offset,
-                     &plan->workspace_bytes);
+    workspace_layout(batch, num_heads, S, pairs, flags, &plan->partial_offset,
+                     &plan->lse_partial_offset, &plan->workspace_bytes);
     return MLA_OK;
 }
 

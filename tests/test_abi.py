@@ -70,12 +70,17 @@ def _plan(lib, batch=4, heads=128, max_blocks=32, max_seq=2048, lens=None, split
 
 
 def test_plan_fixed_splits_and_workspace_layout(lib):
+    rows = 4 * 128 * 64
     rc, p = _plan(lib, batch=4, heads=128, splits=64)
     assert rc == 0 and p.num_kv_splits == 64
     assert p.partial_offset == binding.STATUS_BYTES   # status header, then the partials
-    assert p.lse_partial_offset >= p.partial_offset + 4 * 128 * 64 * 512 * 4
-    assert p.workspace_bytes >= p.lse_partial_offset + 4 * 128 * 64 * 4
+    # bf16 partial rows by default, then the fp32 LSEs
+    assert p.lse_partial_offset == p.partial_offset + rows * 512 * 2
+    assert p.workspace_bytes == p.lse_partial_offset + rows * 4
     assert p.workspace_bytes % 256 == 0
+    rc, p32 = _plan(lib, batch=4, heads=128, splits=64, flags=binding.MLA_PLAN_FP32_PARTIALS)
+    assert rc == 0 and p32.lse_partial_offset == p32.partial_offset + rows * 512 * 4
+    assert p32.workspace_bytes == p32.lse_partial_offset + rows * 4
     rc, p1 = _plan(lib, splits=1)
     assert rc == 0 and p1.num_kv_splits == 1 and p1.workspace_bytes == binding.STATUS_BYTES
 

@@ -6,8 +6,8 @@ import numpy as np
 import pytest
 
 from mla_latent_cache_paged_gb300 import binding
-from mla_latent_cache_paged_gb300.workloads import (BF16_NAN, bf16_tensor_bits, get_workload,
-                                                    make_workload, to_torch)
+from mla_latent_cache_paged_gb300.workloads import (BF16_NAN, bf16_bits_to_f64, bf16_tensor_bits,
+                                                    get_workload, make_workload, to_torch)
 from oracle import merge_partials, mla_decode_split_partials
 from parity_util import (OUT_ATOL, assert_lse_close, assert_out_close, max_abs_err,
                          oracle_rows, oracle_rows_chunked, run_decode, value_abs_max)
@@ -81,31 +81,51 @@ def test_page_permutation_gives_bit_identical_output(kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_split_partials_follow_the_page_aligned_partition(kernel):
+@pytest.mark.parametrize("fp32", [False, True])
+def test_split_partials_follow_the_page_aligned_partition(kernel, fp32):
+    """Every (request, head, split) partial row against the oracle's split
+    algorithm: bf16 rows by default, fp32 with MLA_PLAN_FP32_PARTIALS."""
     import torch
     lens = [1, 65, 640, 1000]
     S = 5
     w = make_workload("partials", 4, 128, lens, seed=21, extra_blocks=1, num_kv_splits=S)
-    _, _, plan, t = run_decode(w, force_simt=_force(kernel))
-    ws = t["ws"]
+    q, cache, table, seq = to_torch(w)
+    plan = binding.make_plan(4, 128, w.max_blocks_per_seq, seq_lens_host=w.seq_lens,
+                             max_seq_len=w.max_seq_len, num_kv_splits=S,
+                             force_simt=_force(kernel),
+                             extra_flags=binding.MLA_PLAN_FP32_PARTIALS if fp32 else 0)
+    ws = binding.new_workspace(plan)
+    out, lse = binding.mla_decode(q, cache, table, seq, w.softmax_scale, plan=plan, workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.read_error(ws) == 0
     B, N = w.batch, w.num_heads
-    o_part = ws[plan.partial_offset:plan.partial_offset + B * N * S * 512 * 4]
-    o_part = o_part.view(torch.float32).view(B, N, S, 512).double().cpu().numpy()
+    esize = 4 if fp32 else 2
+    o_part = ws[plan.partial_offset:plan.partial_offset + B * N * S * 512 * esize]
+    if fp32:
+        o_part = o_part.view(torch.float32).view(B, N, S, 512).double().cpu().numpy()
+    else:
+        o_part = bf16_bits_to_f64(bf16_tensor_bits(o_part.view(torch.bfloat16))).reshape(
+            B, N, S, 512)
+    assert plan.lse_partial_offset == plan.partial_offset + B * N * S * 512 * esize
     l_part = ws[plan.lse_partial_offset:plan.lse_partial_offset + B * N * S * 4]
     l_part = l_part.view(torch.float32).view(B, N, S).double().cpu().numpy()
     ref_o, ref_l = mla_decode_split_partials(w.q_f64(), w.cache_f64(), w.block_table,
                                              w.seq_lens, w.softmax_scale, S)
     assert np.array_equal(np.isneginf(l_part), np.isneginf(ref_l))
     assert_lse_close(l_part, ref_l, "lse partials")
-    # fp32 partials: the tensor-core kernel rounds P to bf16 for the P.V MMA
-    # (relative 2^-9 per weight, so up to ~2^-9 * max|V| ~ 0.01 here); the
-    # bound is the one the bf16 output is held to. An empty split's row is
-    # only defined by its LSE of -inf (the merge gives it weight 0 and never
-    # reads the row), so the rows are compared where the split has tokens.
+    # The tensor-core kernel rounds P to bf16 for the P.V MMA (relative 2^-9
+    # per weight, so up to ~2^-9 * max|V| ~ 0.01 here), and a bf16 row adds
+    # half an ulp of rounding; the bound is the one the bf16 output is held
+    # to. An empty split's row is only defined by its LSE of -inf (the merge
+    # gives it weight 0 and never reads the row), so the rows are compared
+    # where the split has tokens.
     live = ~np.isneginf(ref_l)
     assert live.any() and (~live).any()
     err = np.abs(o_part - ref_o)[live].max()
     assert err < 2e-2, err
+    ref_out, ref_lse = oracle_rows(w, range(B))
+    assert_out_close(bf16_bits_to_f64(bf16_tensor_bits(out)), ref_out, "merged",
+                     value_abs_max(w, range(B)))
 
 
 def test_merge_splits_against_oracle():

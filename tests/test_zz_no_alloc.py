@@ -53,9 +53,15 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
     build.build()
     plan = binding.make_plan(4, 128, 2048, num_kv_splits=64)   # 4*128*64*2052 B of partials
     assert plan.workspace_bytes > (32 << 20)
-    # The stated bound: 16,348 partial rows fit, e.g. B=32, N=128, S=3, and S=4 does not.
-    assert binding.make_plan(32, 128, 64, num_kv_splits=3).workspace_bytes <= (32 << 20)
-    assert binding.make_plan(32, 128, 64, num_kv_splits=4).workspace_bytes > (32 << 20)
+    # The stated bounds: 32,632 bf16 split rows fit (B=32, N=128: S=7 fits, S=8
+    # does not); with fp32 rows 16,348 (S=3 fits, S=4 does not).
+    fp32 = binding.MLA_PLAN_FP32_PARTIALS
+    assert binding.make_plan(32, 128, 64, num_kv_splits=7).workspace_bytes <= (32 << 20)
+    assert binding.make_plan(32, 128, 64, num_kv_splits=8).workspace_bytes > (32 << 20)
+    assert binding.make_plan(32, 128, 64, num_kv_splits=3,
+                             extra_flags=fp32).workspace_bytes <= (32 << 20)
+    assert binding.make_plan(32, 128, 64, num_kv_splits=4,
+                             extra_flags=fp32).workspace_bytes > (32 << 20)
     import torch
     q = torch.zeros((4, 128, 576), dtype=torch.bfloat16, device="cuda")
     cache = torch.zeros((8, 64, 576), dtype=torch.bfloat16, device="cuda")
