@@ -1000,30 +1000,27 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                 // Weights: P row of this head, 64 tokens as bf16 pairs, written
                 // over the first 32 columns of the score buffer (all read
                 // above). Masked tokens (x = -inf) get 0.
-                float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                float2 lb2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                // The weights go to TMEM first; their two sums are formed
+                // after the P.V hand-off below, off the path from these
+                // scores to the MMA that frees their buffer (x keeps the
+                // fp32 weights, pk the rounded ones).
+                uint32_t pk[32];
                 {
                     // A row that has seen no token yet keeps m_ref = -inf:
                     // its weights are exp2(-inf) = 0, not NaN.
                     const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;
                     const float2 negm2 = make_float2(mneg, mneg);
                     const float2 sc2 = make_float2(sc, sc);
-                    uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const float2 d = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), sc2, negm2);
-                        const float a = ptx::ex2(d.x);
-                        const float c = ptx::ex2(d.y);
-                        pk[i] = kFp8 ? pack_f16x2(a, c) : pack_bf16x2(a, c);
-                        ls2[i & 1] = __fadd2_rn(ls2[i & 1], make_float2(a, c));
-                        lb2[i & 1] = __fadd2_rn(lb2[i & 1], unpack_x2<kFp8>(pk[i]));
+                        x[2 * i] = ptx::ex2(d.x);
+                        x[2 * i + 1] = ptx::ex2(d.y);
+                        pk[i] = kFp8 ? pack_f16x2(x[2 * i], x[2 * i + 1])
+                                     : pack_bf16x2(x[2 * i], x[2 * i + 1]);
                     }
                     ptx::tmem_st32(sbuf, pk);
                 }
-                const float2 ls = __fadd2_rn(ls2[0], ls2[1]);
-                const float2 lb = __fadd2_rn(lb2[0], lb2[1]);
-                l_sum = l_sum * alpha + (ls.x + ls.y);
-                l_bf = l_bf * alpha + (lb.x + lb.y);
 
                 // O rescale once the P.V of the previous page is done.
                 if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -1068,6 +1065,19 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
                         issue_pv<kFp8>(tmem, sbase, jg, j > 0, b_vempty, b_pfree);
                     __syncwarp();
                     issued_pv = true;
+                }
+                {
+                    float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    float2 lb2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        ls2[i & 1] = __fadd2_rn(ls2[i & 1], make_float2(x[2 * i], x[2 * i + 1]));
+                        lb2[i & 1] = __fadd2_rn(lb2[i & 1], unpack_x2<kFp8>(pk[i]));
+                    }
+                    const float2 ls = __fadd2_rn(ls2[0], ls2[1]);
+                    const float2 lb = __fadd2_rn(lb2[0], lb2[1]);
+                    l_sum = l_sum * alpha + (ls.x + ls.y);
+                    l_bf = l_bf * alpha + (lb.x + lb.y);
                 }
             }
             if (!ok) break;
