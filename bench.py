@@ -402,10 +402,16 @@ def run_multi_token(args):
     ms = e0.elapsed_time(e1) / steps
     rows = w.batch * T
     pages = sum(-(-int(L) // 64) for L in w.seq_lens)
-    # The method needs each request's cache once, q and out per query row.
+    # The method needs each request's cache once, q and out per query row;
+    # every query row does 2 * (576 + 512) flops per (visible token, head).
     nbytes_alg = 1152 * w.total_tokens + rows * w.num_heads * (1152 + 1024 + 4) + 4 * pages
+    visible = int(binding.multi_token_row_lens(w.seq_lens, T, True).astype("int64").sum())
+    flops = 2 * (576 + 512) * w.num_heads * visible
     peaks, peak_kind = load_peaks()
     achieved = nbytes_alg / (ms / 1e3) / 1e9
+    t_s = ms / 1e3
+    t_hbm = nbytes_alg / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     return {
         "metric": STAGES["multi_token"] + ": cached-tokens x heads x query-tokens / s",
         "value": w.total_tokens * w.num_heads * T / (ms / 1e3),
@@ -418,11 +424,19 @@ def run_multi_token(args):
                    "schedule": (f"page-balanced over {plan.sched_pairs} CTA pairs + merge"
                                 if plan.sched_pairs > 0 else f"split S={plan.num_kv_splits}"),
                    "l2": "inputs larger than L2, no flush"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                     "algorithmic_bytes_per_launch": nbytes_alg,
-                     "note": "each query row reads its request's pages: the cache is read "
-                             f"{T} times per call"},
+        "roofline": ({"bound": "tensor", "achieved": flops / t_s / 1e12,
+                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                      "frac": flops / t_s / 1e12 / peaks["bf16_tflops"]}
+                     if t_tc > t_hbm else
+                     {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]}) | {
+                     "traffic": None, "algorithmic_bytes_per_launch": nbytes_alg,
+                     "algorithmic_flops_per_launch": flops,
+                     "frac_of_roofline": max(t_hbm, t_tc) / t_s,
+                     "hbm_frac": achieved / peaks["hbm_gbs"],
+                     "note": "T query tokens per request: T times the flops over the same "
+                             "cache bytes; the rows of a request each read its pages (L2 "
+                             "serves the rereads when the rows run together)"},
         "gpu_launches": steps * (2 + (1 if plan.num_kv_splits > 1 or plan.sched_pairs else 0)),
         "clocks": clocks,
     }

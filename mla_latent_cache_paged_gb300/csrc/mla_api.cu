@@ -96,7 +96,7 @@ int decode_impl(const mla_decode_plan_t* plan, const void* q, const void* latent
                 int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
                 float softmax_scale, void* out, float* lse, void* workspace,
                 size_t workspace_bytes, void* stream, int q_len, int heads_per_token,
-                int causal) {
+                int causal, int row_tokens) {
     int rc = validate_plan(plan);
     if (rc != MLA_OK) return rc;
     if (!q || !latent_cache || !block_table || !seq_lens || !out) return MLA_ERR_INVALID_ARG;
@@ -108,10 +108,14 @@ int decode_impl(const mla_decode_plan_t* plan, const void* q, const void* latent
         return MLA_ERR_WORKSPACE;
     if (plan->kernel == MLA_KERNEL_TC && num_blocks > tc_max_blocks()) return MLA_ERR_UNSUPPORTED;
     if (plan->batch == 0) return MLA_OK;
-    const DecodeParams p = make_decode_params(plan, q, latent_cache, num_blocks, block_table,
-                                              seq_lens, softmax_scale, out, lse,
-                                              static_cast<char*>(workspace), nullptr, q_len,
-                                              heads_per_token, causal);
+    DecodeParams p = make_decode_params(plan, q, latent_cache, num_blocks, block_table,
+                                        seq_lens, softmax_scale, out, lse,
+                                        static_cast<char*>(workspace), nullptr, q_len,
+                                        heads_per_token, causal);
+    if (row_tokens > 1) {
+        p.row_tokens = row_tokens;
+        p.row_batch = plan->batch / row_tokens;
+    }
     return launch_decode_and_merge(p, plan, stream);
 }
 

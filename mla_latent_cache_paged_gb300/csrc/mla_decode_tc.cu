@@ -573,7 +573,7 @@ __device__ __forceinline__ void page_loader(const DecodeParams& p, const CUtenso
             if (q_next < 0) return;
             const uint32_t qbytes = uint32_t(N) * kD * 2;   // a multiple of 16
             const unsigned char* qb =
-                reinterpret_cast<const unsigned char*>(p.q + size_t(q_next) * N * kD);
+                reinterpret_cast<const unsigned char*>(p.q + size_t(io_row(p, q_next)) * N * kD);
             const uint32_t half = (qbytes / 2) & ~15u;
             ptx::prefetch_l2(qb + rank * half, rank == 0 ? half : qbytes - half);
         };
@@ -851,7 +851,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
         int nstage = 0;
         bool q_big = false;   // fp8 cache: a q entry beyond the f16 range was seen
         auto stage_q = [&](int qb) -> bool {
-            const uint16_t* qbase = p.q + size_t(qb) * N * kD;
+            const uint16_t* qbase = p.q + size_t(io_row(p, qb)) * N * kD;
             const uint32_t ph = uint32_t(nstage++) & 1u;
             const int t = tid - 64;   // 0..127 over the four softmax warps
 #pragma unroll 4
@@ -1106,7 +1106,7 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap t
             float inv = l_bf > 0.f ? 1.f / l_bf : 0.f;
             if constexpr (kFp8) inv *= p.v_scale;   // the cache codes' per-tensor scale
             const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-            const size_t row = size_t(sg.b) * N + h;
+            const size_t row = size_t(io_row(p, sg.b)) * N + h;
             const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0u;
             const size_t prow = size_t(sg.prow0) + size_t(h) * sg.prow_stride;
             // An empty split's partial row is never read (its LSE of -inf

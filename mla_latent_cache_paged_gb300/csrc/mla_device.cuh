@@ -24,6 +24,11 @@ __device__ __forceinline__ int row_shift(const DecodeParams& p, int h) {
     return tok < p.q_len ? p.q_len - 1 - tok : 0;
 }
 
+// The q / out / lse tensor row of work row r (token-major multi-token rows).
+__device__ __forceinline__ int io_row(const DecodeParams& p, int r) {
+    return p.row_tokens > 1 ? (r % p.row_batch) * p.row_tokens + r / p.row_batch : r;
+}
+
 // Record the first device-side error of a call; later ones are dropped.
 __device__ __forceinline__ void record_error(int32_t* status, int32_t code, int32_t detail) {
     if (status != nullptr && atomicCAS(status, 0, code) == 0) {

@@ -82,6 +82,11 @@ struct DecodeParams {
     int32_t q_len;
     int32_t heads_per_token;
     int32_t causal;
+    // Multi-token rows in token-major order (row r = i * row_batch + b is
+    // query token i of request b): q, out and lse of row r are at tensor row
+    // b * row_tokens + i. row_tokens <= 1: row r is tensor row r.
+    int32_t row_tokens;
+    int32_t row_batch;
 };
 
 
@@ -133,7 +138,7 @@ int decode_impl(const mla_decode_plan_t* plan, const void* q, const void* latent
                 int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
                 float softmax_scale, void* out, float* lse, void* workspace,
                 size_t workspace_bytes, void* stream, int q_len, int heads_per_token,
-                int causal);
+                int causal, int row_tokens = 1);
 
 // Host-side helpers from mla_plan.cpp.
 int validate_plan(const mla_decode_plan_t* plan);

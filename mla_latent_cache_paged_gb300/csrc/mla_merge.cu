@@ -246,9 +246,10 @@ __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel
     if (pages_b == 0) {
         // No pages: O = 0, LSE = -inf.
         if (h < N) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t(b) * N + h) * kLkv);
+            const size_t orow = size_t(io_row(p, b)) * N + h;
+            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kLkv);
             for (int i = lane; i < kLkv / 8; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
-            if (lane == 0 && p.lse != nullptr) p.lse[size_t(b) * N + h] = -INFINITY;
+            if (lane == 0 && p.lse != nullptr) p.lse[orow] = -INFINITY;
         }
         return;
     }
@@ -305,7 +306,8 @@ __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel
             for (int i = lane; i < pieces; i += 32) w[i] = 0.f;
         }
         __syncwarp();
-        if (lane == 0 && p.lse != nullptr) p.lse[size_t(b) * N + h] = lse_h;
+        const size_t orow = size_t(io_row(p, b)) * N + h;
+        if (lane == 0 && p.lse != nullptr) p.lse[orow] = lse_h;
         // Lane l owns columns 4l + 128k (k = 0..3): four independent 16-byte
         // loads per piece in flight (L2 only: the rows were written by
         // another grid that may still be running).
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(kBalMergeWarps * 32) mla_merge_balanced_kernel
                 acc[k].w = fmaf(wi, v[k].w, acc[k].w);
             }
         }
-        uint16_t* dst = p.out + (size_t(b) * N + h) * kLkv + lane * 4;
+        uint16_t* dst = p.out + orow * kLkv + lane * 4;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             uint2 packed;

@@ -14,11 +14,16 @@
 //     causal limit.
 //   * otherwise (the plan has B * T rows of N heads): each (request, query
 //     token) becomes a row of the decode: a small kernel writes, into caller
-//     scratch, row r = b * T + i's block-table row (a copy of request b's) and
-//     its visible length, and the decode runs over the B * T rows, whose q,
-//     out and lse are already laid out row after row in the caller's tensors.
-//     Every row reads its request's pages, so a request's cache is read T
-//     times.
+//     scratch, each row's block-table row (a copy of its request's) and its
+//     visible length, and the decode runs over the B * T rows. Every row reads
+//     its request's pages. Under the page-balanced schedule the rows go in
+//     token-major order (row r = i * B + b: every request's token 0, then
+//     every request's token 1, ...), so the equal cut gives the CTA pairs of
+//     token i the same requests' pages at the same time as those of token 0
+//     and the rereads of a page mostly hit L2; q, out and lse stay
+//     [B, T, N, ...] (the decode maps row r to tensor row b * T + i). Under
+//     the split schedule the rows are request-major (r = b * T + i), the
+//     tensors' own order.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,11 +35,12 @@ namespace {
 
 __global__ void mla_expand_rows_kernel(const int32_t* __restrict__ block_table,
                                        const int32_t* __restrict__ seq_lens, int q_len,
-                                       int causal, int max_blocks, int32_t* __restrict__ table_out,
+                                       int causal, int max_blocks, int batch, int token_major,
+                                       int32_t* __restrict__ table_out,
                                        int32_t* __restrict__ lens_out) {
     const int r = blockIdx.x;
-    const int b = r / q_len;
-    const int i = r - b * q_len;
+    const int b = token_major ? r % batch : r / q_len;
+    const int i = token_major ? r / batch : r - b * q_len;
     const int32_t* src = block_table + int64_t(b) * max_blocks;
     int32_t* dst = table_out + int64_t(r) * max_blocks;
     for (int j = threadIdx.x; j < max_blocks; j += blockDim.x) dst[j] = src[j];
@@ -89,10 +95,12 @@ extern "C" int mla_decode_multi_token(const mla_decode_plan_t* plan, int q_len, 
     int32_t* lens_rows = reinterpret_cast<int32_t*>(static_cast<char*>(scratch) +
                                                     round256(rows * size_t(max_blocks) * 4));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int token_major = plan->sched_pairs > 0 ? 1 : 0;
     mla_expand_rows_kernel<<<unsigned(rows), 128, 0, st>>>(block_table, seq_lens, q_len,
-                                                           causal ? 1 : 0, max_blocks,
-                                                           table_rows, lens_rows);
+                                                           causal ? 1 : 0, max_blocks, batch,
+                                                           token_major, table_rows, lens_rows);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
-    return mla_decode(plan, q, latent_cache, num_blocks, table_rows, lens_rows, softmax_scale,
-                      out, lse, workspace, workspace_bytes, stream);
+    return decode_impl(plan, q, latent_cache, num_blocks, table_rows, lens_rows, softmax_scale,
+                       out, lse, workspace, workspace_bytes, stream, 1, num_heads, 0,
+                       token_major ? q_len : 1);
 }
