@@ -142,12 +142,60 @@ __device__ __forceinline__ void bulk_wait_all() {
 // result goes to A chunk l / 4 in the 128-byte swizzled K-major layout the
 // MMAs read. Rows past the batch are left as they are (their products are
 // never stored).
+// Four partials' values for the 16 columns of one lane (fp32 or bf16 rows).
+// A partial past S reads as zero.
+__device__ __forceinline__ void load_group(const BmmParams& p, int64_t base, int s0, int S,
+                                           float4 (&v)[4][4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int s = s0 + q;
+        const int64_t e0 = base + int64_t(s) * kLkv;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (s >= S) {
+                v[q][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (p.part_bf16) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(
+                    static_cast<const uint16_t*>(p.o_part) + e0 + 4 * k));
+                v[q][k] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+            } else {
+                v[q][k] = __ldg(reinterpret_cast<const float4*>(
+                    static_cast<const float*>(p.o_part) + e0) + k);
+            }
+        }
+    }
+}
+
+// acc += w * v over a group, a partial of weight 0 (a neutral split, whose
+// row may hold anything) contributing nothing.
+__device__ __forceinline__ void fma_group(const float* wts, int s0, int S, const float4 (&v)[4][4],
+                                          float4 (&acc)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float w = s0 + q < S ? wts[s0 + q] : 0.f;
+        if (w == 0.f) continue;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc[k].x = fmaf(w, v[q][k].x, acc[k].x);
+            acc[k].y = fmaf(w, v[q][k].y, acc[k].y);
+            acc[k].z = fmaf(w, v[q][k].z, acc[k].z);
+            acc[k].w = fmaf(w, v[q][k].w, acc[k].w);
+        }
+    }
+}
+
 __device__ void merge_rows_into_a(const BmmParams& p, unsigned char* smem, float* wts, int m0,
                                   int n, int mw, int lane) {
     const int S = p.splits;
     const int rows = min(kM, p.batch - m0);
     for (int r = mw; r < rows; r += kMergeWarps) {
         const int64_t row = int64_t(m0 + r) * p.heads + n;
+        const int64_t base = row * S * kLkv + lane * 16;   // element index of split 0
+        // The first partials' loads go out with the LSEs' (their addresses do
+        // not depend on the weights), so a row costs one round trip to memory.
+        float4 va[4][4], vb[4][4];
+        load_group(p, base, 0, S, va);
         const float* ls = p.lse_part + row * S;
         float m = -INFINITY;
         for (int s = lane; s < S; s += 32) m = fmaxf(m, ls[s]);
@@ -169,42 +217,13 @@ __device__ void merge_rows_into_a(const BmmParams& p, unsigned char* smem, float
         float4 acc[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int64_t base = row * S * kLkv + lane * 16;   // element index of split 0
-        for (int s0 = 0; s0 < S; s0 += 4) {
-            // four partials' loads in flight before their sums
-            float4 v[4][4];
-            float ws[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int s = s0 + q;
-                ws[q] = s < S ? wts[s] : 0.f;
-                const int64_t e0 = base + int64_t(s) * kLkv;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (ws[q] == 0.f) {
-                        v[q][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    } else if (p.part_bf16) {
-                        const uint2 u = __ldg(reinterpret_cast<const uint2*>(
-                            static_cast<const uint16_t*>(p.o_part) + e0 + 4 * k));
-                        v[q][k] = make_float4(__uint_as_float(u.x << 16),
-                                              __uint_as_float(u.x & 0xffff0000u),
-                                              __uint_as_float(u.y << 16),
-                                              __uint_as_float(u.y & 0xffff0000u));
-                    } else {
-                        v[q][k] = __ldg(reinterpret_cast<const float4*>(
-                            static_cast<const float*>(p.o_part) + e0) + k);
-                    }
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    acc[k].x = fmaf(ws[q], v[q][k].x, acc[k].x);
-                    acc[k].y = fmaf(ws[q], v[q][k].y, acc[k].y);
-                    acc[k].z = fmaf(ws[q], v[q][k].z, acc[k].z);
-                    acc[k].w = fmaf(ws[q], v[q][k].w, acc[k].w);
-                }
+        // The next group's loads go out before this group's sums.
+        for (int s0 = 0; s0 < S; s0 += 8) {
+            if (s0 + 4 < S) load_group(p, base, s0 + 4, S, vb);
+            fma_group(wts, s0, S, va, acc);
+            if (s0 + 4 >= S) break;
+            if (s0 + 8 < S) load_group(p, base, s0 + 8, S, va);
+            fma_group(wts, s0 + 4, S, vb, acc);
         }
         __syncwarp();
         uint32_t h[8];
