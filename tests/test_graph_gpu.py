@@ -83,3 +83,64 @@ def test_decode_step_replays_in_a_cuda_graph(schedule, splits):
                                           eager[k].view(torch.int16 if k != "lse" else torch.int32)
                                           .cpu().numpy(), err_msg=f"{k} replay {rnd}")
         assert torch.equal(cache_g.view(torch.int16), cache_e.view(torch.int16))
+
+
+@pytest.mark.parametrize("kind", ["fp8", "v_up_proj"])
+def test_fp8_decode_and_fused_up_projection_replay_in_a_cuda_graph(kind):
+    """mla_decode_fp8 (page-balanced plan, its merge's counters) and
+    mla_decode_v_up_proj (split plan: the decode, then the merge fused into
+    the up-projection) captured into a graph and replayed: every replay
+    matches the same call run eagerly bit for bit, with new q each time."""
+    import torch
+    B, N = 6, 128
+    lens_host = [64, 200, 1, 1000, 130, 77]
+    fp8 = kind == "fp8"
+    w = make_workload("graph2", B, N, lens_host, seed=1710, extra_blocks=2,
+                      cache_dtype="fp8" if fp8 else "bf16")
+    q, cache, table, lens = to_torch(w)
+    plan = binding.make_plan(B, N, w.max_blocks_per_seq, seq_lens_host=w.seq_lens,
+                             num_kv_splits=0 if fp8 else 4,
+                             schedule="balanced" if fp8 else "split", num_sms=16)
+    assert (plan.sched_pairs > 0) == fp8
+    gen = torch.Generator(device="cuda").manual_seed(1711)
+    w_uv = (torch.randn((N, 512, 128), generator=gen, device="cuda") * 512 ** -0.5).to(
+        torch.bfloat16)
+    ws = binding.new_workspace(plan)
+
+    def new_outs():
+        return dict(o=torch.empty((B, N, 128 if not fp8 else 512), dtype=torch.bfloat16,
+                                  device="cuda"),
+                    lse=torch.empty((B, N), dtype=torch.float32, device="cuda"))
+
+    def call(qq, o, workspace):
+        if fp8:
+            binding.mla_decode_fp8(qq, cache, table, lens, w.softmax_scale, w.k_scale, plan=plan,
+                                   out=o["o"], lse=o["lse"], workspace=workspace)
+        else:
+            binding.mla_decode_v_up_proj(qq, cache, table, lens, w.softmax_scale, w_uv,
+                                         plan=plan, workspace=workspace, out=o["o"],
+                                         lse=o["lse"])
+
+    q_static = q.clone()
+    out_static = new_outs()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(q_static, out_static, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(q_static, out_static, ws)
+    for rnd in range(3):
+        if rnd:
+            q_static.copy_((torch.randn(q.shape, generator=gen, device="cuda")).to(torch.bfloat16))
+        eager = new_outs()
+        ws_e = binding.new_workspace(plan)
+        call(q_static, eager, ws_e)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert binding.read_error(ws) == 0 and binding.read_error(ws_e) == 0
+        assert torch.equal(out_static["o"], eager["o"]), (kind, rnd)
+        assert torch.equal(out_static["lse"], eager["lse"]), (kind, rnd)
+        header = ws[:binding.STATUS_BYTES].view(torch.int32).cpu().numpy()
+        assert not header.any(), np.nonzero(header)
