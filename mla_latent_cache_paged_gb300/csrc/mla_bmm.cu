@@ -27,7 +27,7 @@
 // tcgen05.mma (M = 128, N = min(J, 256), K = 16), and all four warps read the
 // accumulator back (thread = row), round to bf16, stage it in shared memory
 // (the idle ring, 128-byte swizzled) and write it with TMA stores. In the
-// front end the q_pe tile arrives by TMA with the first chunk and leaves by
+// front end the q_pe tile arrives by TMA after the A chunks and leaves by
 // TMA store, and warps 2-3 insert the new tokens' latent rows (the CTAs of
 // a batch tile share them out by head) while the MMAs run. Every wait is bounded (MLA_ERR_TIMEOUT);
 // a slot outside the cache is recorded (MLA_ERR_BAD_BLOCK_ID), not written.
@@ -60,10 +60,11 @@ constexpr int kQHead = kNope + kRope;        // q head width (P + R)
 
 enum BmmSite : int32_t { kSiteRingEmpty = 30, kSiteRingFull, kSiteAccFull, kSiteRingDrain };
 
-// Shared memory: the whole A tile (all K chunks, loaded at once so that each
-// request's row is read in one burst), a ring of STAGES weight chunks, the
-// front end's q_pe tile, then the barriers. The result is staged over the A
-// tile and the ring once the MMAs are done.
+// Shared memory: the whole A tile (all K chunks, all requested up front so
+// that each request's row is read in one burst, each chunk with its own
+// barrier so that its MMAs start as soon as it lands), a ring of STAGES
+// weight chunks, the front end's q_pe tile, then the barriers. The result is
+// staged over the A tile and the ring once the MMAs are done.
 template <int J, int KD, int STAGES>
 struct BmmShape {
     static constexpr int kWBytes = (J / 64) * kWBlockBytes;   // one weight chunk
@@ -75,10 +76,12 @@ struct BmmShape {
     static constexpr int kTmemCols = J < 32 ? 32 : J;
     static constexpr int kPeOff = kRingOff + STAGES * kWBytes;   // front end: q_pe, 128 x 64
     static constexpr int kBarOff = kPeOff + kABytes;   // a_full, w_full[S], w_empty[S], acc, slot, abort
+    static constexpr int kAChunkBarOff = kBarOff + 128;  // one "A chunk landed" barrier per chunk
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;   // + alignment slack
     static_assert(KD % kChunk == 0 && J % 64 == 0 && J <= 512, "shape");
     static_assert((J & (J - 1)) == 0, "TMEM allocation is a power of two");
     static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(16 * STAGES + 24 <= 128 && 128 + 8 * kChunks <= 256, "barrier area");
     static_assert(kPeOff >= (J / 64) * kM * 128, "epilogue staging fits A and the ring");
 };
 
@@ -266,6 +269,7 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
     const uint32_t b_full = b_afull + 8;
     const uint32_t b_empty = b_full + 8 * STAGES;
     const uint32_t b_acc = b_empty + 8 * STAGES;
+    const uint32_t b_achunk = sbase + Sh::kAChunkBarOff;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::kBarOff + 16 * STAGES + 16);
     volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
@@ -280,6 +284,7 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         ptx::mbar_init(b_afull, kMergeA ? kMergeWarps * 32 : 1);
+        for (int c = 0; c < Sh::kChunks; ++c) ptx::mbar_init(b_achunk + 8 * c, 1);
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(b_full + 8 * s, 1);
             ptx::mbar_init(b_empty + 8 * s, 1);
@@ -299,34 +304,50 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
-        // Producer: the whole A tile (and q_pe) at once, then weight chunk c
-        // into stage c % STAGES once its previous use is done.
+        // Producer: A chunk c and weight chunk c side by side while the ring
+        // has room, the rest of A (and q_pe), then weight chunk c into stage
+        // c % STAGES once its previous use is done.
         int issued = 0;
         if (ptx::elect_one()) {
-            if constexpr (!kMergeA) {
-                ptx::mbar_arrive_expect_tx(b_afull, Sh::kAllABytes + (kFrontEnd ? kABytes : 0));
-                for (int c = 0; c < Sh::kChunks; ++c)
-                    ptx::tma_load_2d(sbase + uint32_t(c * kABytes), &tmap_a,
-                                     n * p.a_head + c * kChunk, m0, b_afull);
-            }
-            if (kFrontEnd)   // q_pe: columns 128..191 of the head, next to q_nope
-                ptx::tma_load_2d(sbase + Sh::kPeOff, &tmap_a, n * p.a_head + kNope, m0, b_afull);
-            for (int c = 0; c < Sh::kChunks; ++c) {
+            auto load_a = [&](int c) {
+                ptx::mbar_arrive_expect_tx(b_achunk + 8 * c, kABytes);
+                ptx::tma_load_2d(sbase + uint32_t(c * kABytes), &tmap_a,
+                                 n * p.a_head + c * kChunk, m0, b_achunk + 8 * c);
+            };
+            auto load_w = [&](int c) {
                 const int s = c % STAGES;
-                if (c >= STAGES &&
-                    !bmm_wait(b_empty + 8 * s, ((c / STAGES) - 1) & 1, abort, p.status,
-                              kSiteRingEmpty, false))
-                    break;
                 const uint32_t st = sbase + uint32_t(Sh::kRingOff + s * Sh::kWBytes);
                 ptx::mbar_arrive_expect_tx(b_full + 8 * s, Sh::kWBytes);
 #pragma unroll
                 for (int jb = 0; jb < J / 64; ++jb)
                     ptx::tma_load_2d(st + uint32_t(jb * kWBlockBytes), &tmap_w, jb * 64,
                                      n * KD + c * kChunk, b_full + 8 * s);
+            };
+            constexpr int kFirst = Sh::kChunks < STAGES ? Sh::kChunks : STAGES;
+            for (int c = 0; c < kFirst; ++c) {
+                if constexpr (!kMergeA) load_a(c);
+                load_w(c);
+            }
+            issued = kFirst;
+            if constexpr (!kMergeA)
+                for (int c = kFirst; c < Sh::kChunks; ++c) load_a(c);
+            if constexpr (kFrontEnd) {   // q_pe: columns 128..191 of the head, next to q_nope
+                ptx::mbar_arrive_expect_tx(b_afull, kABytes);
+                ptx::tma_load_2d(sbase + Sh::kPeOff, &tmap_a, n * p.a_head + kNope, m0, b_afull);
+            }
+            for (int c = kFirst; c < Sh::kChunks; ++c) {
+                const int s = c % STAGES;
+                if (!bmm_wait(b_empty + 8 * s, ((c / STAGES) - 1) & 1, abort, p.status,
+                              kSiteRingEmpty, false))
+                    break;
+                load_w(c);
                 ++issued;
             }
             // Copies still in flight (after an abort) land before the CTA exits.
-            if constexpr (!kMergeA) bmm_wait(b_afull, 0, abort, p.status, kSiteRingDrain, true);
+            if constexpr (!kMergeA)
+                for (int c = 0; c < Sh::kChunks; ++c)
+                    bmm_wait(b_achunk + 8 * c, 0, abort, p.status, kSiteRingDrain, true);
+            if constexpr (kFrontEnd) bmm_wait(b_afull, 0, abort, p.status, kSiteRingDrain, true);
             for (int c = issued - STAGES < 0 ? 0 : issued - STAGES; c < issued; ++c)
                 bmm_wait(b_full + 8 * (c % STAGES), (c / STAGES) & 1, abort, p.status,
                          kSiteRingDrain, true);
@@ -336,9 +357,11 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
         // MMA issuer.
         constexpr uint32_t idesc = ptx::idesc_bf16_f32(Sh::kPiece, true);
         if (ptx::elect_one()) {
-            bool ok = bmm_wait(b_afull, 0, abort, p.status, kSiteRingFull, false);
+            bool ok = !kMergeA || bmm_wait(b_afull, 0, abort, p.status, kSiteRingFull, false);
             for (int c = 0; c < Sh::kChunks && ok; ++c) {
                 const int s = c % STAGES;
+                if constexpr (!kMergeA)
+                    if (!bmm_wait(b_achunk + 8 * c, 0, abort, p.status, kSiteRingFull, false)) break;
                 ok = bmm_wait(b_full + 8 * s, (c / STAGES) & 1, abort, p.status, kSiteRingFull,
                               false);
                 if (!ok) break;
@@ -376,7 +399,7 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
         ptx::mbar_arrive(b_afull);
     } else if (kFrontEnd) {
         const int t = threadIdx.x - 64;   // warps 2-3
-        // q_pe: the tile that landed with stage 0 goes out as four 32-row boxes
+        // q_pe: its tile (on the a_full barrier) goes out as four 32-row boxes
         // to columns 512..575 of the head.
         if (t == 0 && bmm_wait(b_afull, 0, abort, p.status, kSiteRingFull, false)) {
             for (int slab = 0; slab < kM / 32 && m0 + 32 * slab < p.batch; ++slab)
