@@ -879,7 +879,6 @@ def run_ours(args, w, rank, world):
                          else f"{int(w.seq_lens.min())}..{int(w.seq_lens.max())}"),
             "cached_tokens": w.total_tokens, "page_size": w.page_size,
             "kv_lora_rank": 512, "rope_dim": 64, "softmax_scale": w.softmax_scale,
-            "num_kv_splits_requested": w.num_kv_splits if splits is None else splits,
             "num_kv_splits": plan.num_kv_splits,
             "schedule": (f"page-balanced over {plan.sched_pairs} CTA pairs + merge"
                          if plan.sched_pairs > 0 else f"split S={plan.num_kv_splits}"),
