@@ -71,6 +71,30 @@ def test_fp8_single_token_returns_its_dequantized_row_bit_exact():
         assert np.array_equal(out_bits[b], np.broadcast_to(want, (128, 512))), b
 
 
+def test_fp8_every_finite_code_widens_exactly():
+    """L = 1 with the token's 512 value codes running through every finite
+    E4M3 code, forwards in one request and backwards in the other (the two
+    NaN codes, 0x7f and 0xff, replaced by 0): each output element is its
+    code's value times the power-of-two k_scale, exactly. (Values, not bits:
+    the code for -0 comes out as +0, since the P.V sum adds the masked
+    tokens' +0 products to it.)"""
+    from mla_latent_cache_paged_gb300.workloads import bf16_bits_to_f64
+    from oracle import dequantize_e4m3_cache
+    w = _fp8("fp8_codes", 2, 16, [1, 1], 8, 1, extra=2)
+    codes = np.arange(256, dtype=np.uint8)
+    codes[[0x7F, 0xFF]] = 0
+    rows = [np.concatenate([codes, codes[::-1]]), np.concatenate([codes[::-1], codes])]
+    for b in range(2):
+        w.cache_bits[w.block_table[b, 0], 0, :512] = rows[b]
+    w.k_scale = 2.0 ** -5
+    _, _, _, t = run_decode_fp8(w)
+    got = bf16_bits_to_f64(bf16_tensor_bits(t["out"]))
+    for b in range(2):
+        want = dequantize_e4m3_cache(rows[b], w.k_scale)
+        bad = np.nonzero(got[b] != want[None, :])
+        assert bad[0].size == 0, (b, bad[1][:8], got[b][bad][:8], want[bad[1][:8]])
+
+
 def test_fp8_page_permutation_gives_bit_identical_output():
     lens = [70, 640, 129]
     w1 = _fp8("fp8_perm", 3, 128, lens, 11, 1, extra=5)
