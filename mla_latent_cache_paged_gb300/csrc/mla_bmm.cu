@@ -89,6 +89,7 @@ struct BmmParams {
     int batch, heads;
     int a_head;                  // columns from one head's A to the next (192 or 512)
     const uint16_t* q;           // front end: q [B, N, 192] (for q_pe)
+    const uint16_t* w;           // the weights [N, KD, J] (for the L2 prefetch)
     uint16_t* out;               // element (b, n, j) at out + b * out_row + n * out_head + j
     int64_t out_row;
     int out_head;
@@ -329,6 +330,14 @@ mla_bmm_kernel(const BmmParams p, const __grid_constant__ CUtensorMap tmap_a,
                 load_w(c);
             }
             issued = kFirst;
+            // The weight chunks that wait for a free ring stage are pulled
+            // into L2 now, so that their loads are L2 round trips (not in the
+            // merge mode, whose A tile is built from partials meanwhile:
+            // measured slower there).
+            if constexpr (!kMergeA)
+                for (int c = kFirst; c < Sh::kChunks; ++c)
+                    ptx::prefetch_l2(p.w + (size_t(n) * KD + size_t(c) * kChunk) * J,
+                                     uint32_t(kChunk * J * 2));
             if constexpr (!kMergeA)
                 for (int c = kFirst; c < Sh::kChunks; ++c) load_a(c);
             if constexpr (kFrontEnd) {   // q_pe: columns 128..191 of the head, next to q_nope
@@ -532,6 +541,8 @@ int launch_bmm(const BmmParams& p, const void* a, const void* w, cudaStream_t st
         !encode_2d(&tw, w, J, uint64_t(p.heads) * KD, kChunk) ||
         !encode_2d(&to, p.out, uint64_t(p.heads) * p.out_head, uint64_t(p.batch), 32))
         return int(cudaErrorInvalidValue);
+    BmmParams pw = p;
+    pw.w = static_cast<const uint16_t*>(w);
     auto kernel = mla_bmm_kernel<J, KD, STAGES, kMode>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Sh::kSmemBytes);
@@ -546,7 +557,7 @@ int launch_bmm(const BmmParams& p, const void* a, const void* w, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return int(cudaLaunchKernelEx(&cfg, kernel, p, ta, tw, to));
+    return int(cudaLaunchKernelEx(&cfg, kernel, pw, ta, tw, to));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
