@@ -67,3 +67,47 @@ def test_multi_token_against_the_oracle(T, causal, N, plan_kw):
         assert (got[0, :T - 1] == 0).all()
     # The empty request: every query token sees nothing.
     assert np.isneginf(lse[-1]).all() and (got[-1] == 0).all()
+
+
+def _random_mt_case(i):
+    rng = np.random.default_rng(7000 + i)
+    T = int(rng.integers(1, 9))
+    causal = bool(rng.random() < 0.7)
+    N = int(rng.choice([1, 5, 16, 32, 64, 100, 128]))
+    B = int(rng.integers(1, 7))
+    edge = [0, 1, max(T - 1, 0), T, 63, 64, 65]
+    lens = [int(rng.choice(edge)) if rng.random() < 0.4 else int(rng.integers(1, 1200))
+            for _ in range(B)]
+    kind = str(rng.choice(["auto", "split", "balanced", "expand", "simt"]))
+    kw = {"num_sms": int(rng.choice([8, 30, 152]))}
+    if kind == "split":
+        kw["num_kv_splits"] = int(rng.choice([1, 2, 3, 5]))
+    elif kind == "balanced":
+        kw["schedule"] = "balanced"
+    elif kind == "expand":
+        kw["expand"] = True
+        kw["schedule"] = str(rng.choice(["auto", "balanced"]))
+    elif kind == "simt":
+        kw["force_simt"] = True
+        kw["num_kv_splits"] = int(rng.choice([1, 2]))
+    return T, causal, N, lens, kw
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_multi_token_random_case_against_the_oracle(i):
+    """Seeded random multi-token problems: T 1-8, causal or not, head counts
+    from 1 to 128 (both the packed and the row-expanded form), ragged lengths
+    with requests shorter than T, every schedule, both kernels, several SM
+    counts."""
+    T, causal, N, lens, kw = _random_mt_case(i)
+    w = make_workload("mt_rand", len(lens), N, lens, seed=7100 + i)
+    rng = np.random.default_rng(7200 + i)
+    q_bits = f32_to_bf16_bits(rng.standard_normal((len(lens), T, N, 576)).astype(np.float32))
+    got, lse, plan = _run(w, T, causal, q_bits, **kw)
+    ref, ref_lse = mla_decode_multi_token_reference(bf16_bits_to_f64(q_bits), w.cache_f64(),
+                                                    w.block_table, w.seq_lens, w.softmax_scale,
+                                                    causal=causal)
+    vmax = value_abs_max(w, range(w.batch))[:, None]
+    what = f"case {i}: T={T} causal={causal} N={N} lens={lens} {kw}"
+    assert_out_close(got, ref, what, vmax)
+    assert_lse_close(lse, ref_lse, what)
