@@ -40,7 +40,8 @@ def _assert_within_one_ulp(got_bits, ref, what):
                            f"{float(err.max())} at {np.unravel_index(err.argmax(), err.shape)}")
 
 
-@pytest.mark.parametrize("B,N", [(1, 1), (5, 16), (128, 128), (200, 8), (300, 3)])
+@pytest.mark.parametrize("B,N", [(1, 1), (5, 16), (128, 128), (200, 8), (300, 3), (129, 37),
+                                 (384, 2), (511, 7), (64, 128)])
 def test_front_end_against_the_oracle(B, N):
     import torch
     rng = np.random.default_rng(1000 + 7 * B + N)
@@ -99,7 +100,8 @@ def test_front_end_without_insert_and_with_a_bad_slot():
     np.testing.assert_array_equal(bf16_bits_to_f64(bf16_tensor_bits(cache_d)), ref_cache)
 
 
-@pytest.mark.parametrize("B,N", [(1, 1), (3, 8), (128, 128), (257, 5)])
+@pytest.mark.parametrize("B,N", [(1, 1), (3, 8), (128, 128), (257, 5), (127, 100), (384, 3),
+                                 (640, 1), (255, 64)])
 def test_v_up_proj_against_the_oracle(B, N):
     import torch
     rng = np.random.default_rng(1200 + 7 * B + N)
