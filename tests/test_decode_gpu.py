@@ -9,8 +9,9 @@ from mla_latent_cache_paged_gb300 import binding
 from mla_latent_cache_paged_gb300.workloads import (BF16_NAN, bf16_bits_to_f64, bf16_tensor_bits,
                                                     get_workload, make_workload, to_torch)
 from oracle import merge_partials, mla_decode_split_partials
-from parity_util import (OUT_ATOL, assert_lse_close, assert_out_close, max_abs_err,
-                         oracle_rows, oracle_rows_chunked, run_decode, value_abs_max)
+from parity_util import (OUT_ATOL, assert_lse_close, assert_out_close, assert_out_rel_rms,
+                         max_abs_err, oracle_rows, oracle_rows_chunked, run_decode,
+                         value_abs_max)
 
 pytestmark = pytest.mark.gpu
 
@@ -215,9 +216,10 @@ def test_full_size_configs(name, strict):
     else:
         assert_out_close(got, ref_out, name, value_abs_max(w, reqs))
     assert_lse_close(lse, ref_lse, name)
+    rel = assert_out_rel_rms(got, ref_out, name)
     print(f"{name}: kernel={plan.kernel} S={plan.num_kv_splits} pairs={plan.sched_pairs} "
           f"max|out err|={max_abs_err(got, ref_out):.3g} "
-          f"max|lse err|={max_abs_err(lse, ref_lse):.3g}")
+          f"max|lse err|={max_abs_err(lse, ref_lse):.3g} rel rms={rel:.3g}")
 
 
 def test_output_at_a_16_byte_offset_matches_aligned_output():

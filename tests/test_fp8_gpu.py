@@ -13,8 +13,8 @@ import pytest
 from mla_latent_cache_paged_gb300 import binding
 from mla_latent_cache_paged_gb300.workloads import (bf16_tensor_bits, get_workload,
                                                     make_workload, to_torch)
-from parity_util import (OUT_ATOL, assert_lse_close, assert_out_close, max_abs_err,
-                         oracle_rows_fp8, run_decode_fp8, value_abs_max_fp8)
+from parity_util import (OUT_ATOL, assert_lse_close, assert_out_close, assert_out_rel_rms,
+                         max_abs_err, oracle_rows_fp8, run_decode_fp8, value_abs_max_fp8)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +33,7 @@ def _check(w, got, lse, strict=True):
     else:
         assert_out_close(got, ref_out, w.name, value_abs_max_fp8(w, reqs))
     assert_lse_close(lse, ref_lse, w.name)
+    assert_out_rel_rms(got, ref_out, w.name)
     return max_abs_err(got, ref_out), max_abs_err(lse, ref_lse)
 
 
