@@ -12,8 +12,8 @@ import pytest
 
 from mla_latent_cache_paged_gb300.workloads import (bf16_bits_to_f64, bf16_tensor_bits,
                                                     make_workload, to_torch)
-from parity_util import (assert_lse_close, assert_out_close, oracle_rows, run_decode,
-                         value_abs_max)
+from parity_util import (assert_lse_close, assert_out_close, assert_out_rel_rms, oracle_rows,
+                         run_decode, value_abs_max)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +65,7 @@ def test_balanced_parity(lens, num_sms):
     assert plan.grid_ctas == 2 * plan.sched_pairs
     ref_out, ref_lse = oracle_rows(w, range(w.batch))
     assert_out_close(got, ref_out, "balanced", value_abs_max(w, range(w.batch)))
+    assert_out_rel_rms(got, ref_out, "balanced")
     assert_lse_close(lse, ref_lse, "balanced lse")
 
 

@@ -13,7 +13,7 @@ from mla_latent_cache_paged_gb300 import binding
 from mla_latent_cache_paged_gb300.workloads import (bf16_bits_to_f64, bf16_tensor_bits,
                                                     f32_to_bf16_bits, make_workload, to_torch)
 from oracle import mla_decode_multi_token_reference
-from parity_util import assert_lse_close, assert_out_close, value_abs_max
+from parity_util import assert_lse_close, assert_out_close, assert_out_rel_rms, value_abs_max
 
 pytestmark = pytest.mark.gpu
 
@@ -110,4 +110,5 @@ def test_multi_token_random_case_against_the_oracle(i):
     vmax = value_abs_max(w, range(w.batch))[:, None]
     what = f"case {i}: T={T} causal={causal} N={N} lens={lens} {kw}"
     assert_out_close(got, ref, what, vmax)
+    assert_out_rel_rms(got, ref, what)
     assert_lse_close(lse, ref_lse, what)
