@@ -68,6 +68,9 @@ template <typename TP, int kMode>   // 0: whole rows, 1: column groups, 2: few p
 __global__ void __launch_bounds__(kMergeThreads, 4) mla_merge_kernel(const TP* __restrict__ o_part,
                                                                    const MergeArgs a) {
     __shared__ float weights[kRowsPerCta][kMaxMergeSplits];
+    // Launched as a programmatic dependent of the decode kernel: the CTAs may
+    // be placed while its grid finishes; this waits for it (and its writes).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * kRowsPerCta + warp;
@@ -176,14 +179,29 @@ int launch_merge_strided(const TP* o_part, const MergeArgs& a, cudaStream_t st) 
     if (a.v_dim % 4 != 0 || a.o_row % 4 != 0 || a.o_split % 4 != 0)
         return int(cudaErrorInvalidValue);
     const dim3 rows_grid((a.rows + kRowsPerCta - 1) / kRowsPerCta);
-    if (a.rows < kChunkedMergeRows)
-        mla_merge_kernel<TP, 1>
-                <<<dim3(rows_grid.x, (a.v_dim + 127) / 128), kMergeThreads, 0, st>>>(o_part, a);
-    else if (a.S <= kFewSplits && a.v_dim == 512)
-        mla_merge_kernel<TP, 2><<<rows_grid, kMergeThreads, 0, st>>>(o_part, a);
-    else
-        mla_merge_kernel<TP, 0><<<rows_grid, kMergeThreads, 0, st>>>(o_part, a);
-    return int(cudaGetLastError());
+    // A programmatic dependent of the kernel before it on the stream (the
+    // decode kernel lets its dependents launch as soon as it starts); the
+    // kernel waits for that grid before reading anything.
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kMergeThreads, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (a.rows < kChunkedMergeRows) {
+        cfg.gridDim = dim3(rows_grid.x, (a.v_dim + 127) / 128);
+        e = cudaLaunchKernelEx(&cfg, mla_merge_kernel<TP, 1>, o_part, a);
+    } else if (a.S <= kFewSplits && a.v_dim == 512) {
+        cfg.gridDim = rows_grid;
+        e = cudaLaunchKernelEx(&cfg, mla_merge_kernel<TP, 2>, o_part, a);
+    } else {
+        cfg.gridDim = rows_grid;
+        e = cudaLaunchKernelEx(&cfg, mla_merge_kernel<TP, 0>, o_part, a);
+    }
+    return int(e);
 }
 
 // Merge of the page-balanced schedule: CTA (b, y) handles request b, heads
