@@ -6,8 +6,9 @@ of CTA pairs and the page-balanced cut vary), softmax scale (zero and
 negative included), kernel and cache type (bf16, or fp8 E4M3 on the
 tensor-core kernel), and is checked against the oracle: bf16 out within
 max(2e-2, one bf16 ulp, 2^-8 max_t |V[t, d]|) (the weight-rounding allowance
-of the bf16 tests), the whole output's RMS error within 1e-2 of its RMS, and
-LSE within 1e-3.
+of the bf16 tests; with the split schedule's bf16 partial rows, rounded
+twice, max(2e-2, one ulp + 2^-8 max_t |V[t, d]|)), the whole output's RMS
+error within 1e-2 of its RMS, and LSE within 1e-3.
 """
 
 import numpy as np
@@ -81,6 +82,7 @@ def test_random_case_against_the_oracle(i):
         vmax = value_abs_max(w, reqs)
     what = f"case {i}: {c} plan S={plan.num_kv_splits} pairs={plan.sched_pairs}"
     got = bf16_bits_to_f64(bf16_tensor_bits(out))
-    assert_out_close(got, ref_out, what, vmax)
+    bf16_partials = plan.sched_pairs == 0 and plan.num_kv_splits > 1
+    assert_out_close(got, ref_out, what, vmax, bf16_partials)
     assert_out_rel_rms(got, ref_out, what)
     assert_lse_close(lse.double().cpu().numpy(), ref_lse, what)
