@@ -100,7 +100,9 @@ def test_multi_token_random_case_against_the_oracle(i):
     with requests shorter than T, every schedule, both kernels, several SM
     counts."""
     T, causal, N, lens, kw = _random_mt_case(i)
-    w = make_workload("mt_rand", len(lens), N, lens, seed=7100 + i)
+    # (one spare block: a batch whose requests are all empty still passes a
+    # cache of at least one block, as the interface asks)
+    w = make_workload("mt_rand", len(lens), N, lens, seed=7100 + i, extra_blocks=1)
     rng = np.random.default_rng(7200 + i)
     q_bits = f32_to_bf16_bits(rng.standard_normal((len(lens), T, N, 576)).astype(np.float32))
     got, lse, plan = _run(w, T, causal, q_bits, **kw)
@@ -109,6 +111,6 @@ def test_multi_token_random_case_against_the_oracle(i):
                                                     causal=causal)
     vmax = value_abs_max(w, range(w.batch))[:, None]
     what = f"case {i}: T={T} causal={causal} N={N} lens={lens} {kw}"
-    assert_out_close(got, ref, what, vmax)
+    assert_out_close(got, ref, what, vmax, plan.sched_pairs == 0 and plan.num_kv_splits > 1)
     assert_out_rel_rms(got, ref, what)
     assert_lse_close(lse, ref_lse, what)
