@@ -34,7 +34,6 @@ DECODE_KERNEL_SOURCES = {
     1: ["mla_decode_simt.cu", "mla_device.cuh", "mla_internal.h"],
     2: ["mla_decode_tc.cu", "tc_ptx.cuh", "mla_device.cuh", "mla_internal.h"],
 }
-# the recorded-traffic key of a kernel: its variant and the cache dtype
 
 
 def parse_args():
