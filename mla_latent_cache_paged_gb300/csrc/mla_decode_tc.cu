@@ -15,9 +15,12 @@
 // everything else it does on its own, with no traffic between the two:
 //   * Scores: the full tile S = Q K^T for all (up to) 128 heads and the 64
 //     tokens of a page, tcgen05.mma M=128, N=64, K=16 (36 steps). An MMA with
-//     N <= 64 costs the tensor pipe about as much as one with N = 64, so the
-//     score tile is computed in both CTAs; that keeps the softmax local. q's
-//     dims 0..255 are the A operand in TMEM, dims 256..575 in shared memory.
+//     N = 32 costs the tensor pipe about as much as one with N = 64 (so
+//     splitting a page's tokens between the CTAs would save no tensor time),
+//     and splitting its dims needs the partial scores exchanged, which costs
+//     more than it saves; so the score tile is computed in both CTAs, which
+//     keeps the softmax local. q's dims 0..255 are the A operand in TMEM,
+//     dims 256..575 in shared memory.
 //   * Each page is TMA-loaded by both CTAs (the second read of a page is
 //     served from L2; pulling pages into L2 ahead of the loads measured
 //     slower). Its 64-column blocks go to two page rings: this CTA's four
